@@ -1,0 +1,348 @@
+"""Pins of the oracle to things other than itself (CPU only).
+
+Each test is chosen so that a plausible slip in the oracle -- a dropped or
+extra term, a sign, a swapped index or transposed operand, rounding through
+binary32, ties away from zero -- fails at least one of them.
+"""
+import bisect
+import json
+import math
+import os
+import random
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from dense_tensor_core_bf16_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _bits_to_fraction(h: int) -> Fraction:
+    """bf16 bit pattern -> exact rational, decoded by hand from the format."""
+    sign = -1 if h & 0x8000 else 1
+    e = (h >> 7) & 0xFF
+    f = h & 0x7F
+    assert e != 0xFF
+    if e == 0:
+        return sign * Fraction(f, 1 << 7) * Fraction(1, 1 << 126)
+    v = Fraction(128 + f, 128)
+    return sign * (v * (Fraction(2) ** (e - 127)))
+
+
+def _storage(X_logical: np.ndarray, col_major: bool) -> np.ndarray:
+    return np.ascontiguousarray(X_logical.T if col_major else X_logical)
+
+
+# --- bf16 widening ----------------------------------------------------------
+
+def test_bf16_to_f64_known_values(oracle_lib):
+    cases = {0x3F80: 1.0, 0xC000: -2.0, 0x4049: 3.140625, 0x0001: 2.0 ** -133,
+             0x0080: 2.0 ** -126, 0x7F7F: (2 - 2.0 ** -7) * 2.0 ** 127, 0x8000: -0.0,
+             0x3E80: 0.25, 0x7F80: math.inf, 0xFF80: -math.inf}
+    got = oracle_lib.bf16_to_f64(np.array(list(cases), dtype=np.uint16))
+    for (h, want), g in zip(cases.items(), got):
+        assert g == want and math.copysign(1, g) == math.copysign(1, want), hex(h)
+
+
+def test_bf16_to_f64_matches_hand_decoding(oracle_lib):
+    hs = [h for h in range(0, 1 << 16, 7) if ((h >> 7) & 0xFF) != 0xFF]
+    got = oracle_lib.bf16_to_f64(np.array(hs, dtype=np.uint16))
+    for h, g in zip(hs, got):
+        assert Fraction(g) == _bits_to_fraction(h), hex(h)
+
+
+# --- binary64 -> bf16 rounding ----------------------------------------------
+
+def _golden_rne_cases():
+    out = []
+    with open(os.path.join(GOLDEN, "bf16_rne_cases.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            expr, want = line.rsplit(None, 1)
+            out.append((expr, eval(expr, {"float": float}), int(want, 16)))  # noqa: S307
+    return out
+
+
+def test_f64_to_bf16_golden_cases(oracle_lib):
+    cases = _golden_rne_cases()
+    assert len(cases) >= 25
+    got = oracle_lib.f64_to_bf16(np.array([v for _, v, _ in cases]))
+    for (expr, _, want), g in zip(cases, got):
+        assert int(g) == want, f"{expr}: got {int(g):#06x} want {want:#06x}"
+
+
+def test_f64_to_bf16_nan_stays_nan(oracle_lib):
+    g = int(oracle_lib.f64_to_bf16(np.array([math.nan]))[0])
+    assert (g >> 7) & 0xFF == 0xFF and g & 0x7F != 0
+
+
+def _all_finite_bf16():
+    vals = []
+    for h in range(1 << 16):
+        if ((h >> 7) & 0xFF) == 0xFF:
+            continue
+        if h == 0x8000:   # -0 and +0 are the same value; keep +0 for the search
+            continue
+        vals.append((_bits_to_fraction(h), h))
+    vals.sort()
+    return vals
+
+
+def _nearest_even(x: Fraction, table, keys):
+    """Brute force: nearest finite bf16 to x, ties to the even encoding."""
+    i = bisect.bisect_left(keys, x)
+    cands = [table[j] for j in (i - 1, i) if 0 <= j < len(table)]
+    best = min(abs(v - x) for v, _ in cands)
+    near = [(v, h) for v, h in cands if abs(v - x) == best]
+    if len(near) == 2:
+        near = [c for c in near if (c[1] & 1) == 0]
+    return near[0][1]
+
+
+def test_f64_to_bf16_brute_force_nearest(oracle_lib):
+    table = _all_finite_bf16()
+    keys = [v for v, _ in table]
+    rng = random.Random(7)
+    xs = []
+    for _ in range(3000):
+        e = rng.uniform(-133, 127.9)
+        xs.append(rng.choice([-1, 1]) * (2.0 ** e) * rng.uniform(1, 2) / 2)
+    # exact midpoints between neighbours, and values a hair off them
+    for _ in range(1500):
+        j = rng.randrange(1, len(table) - 1)
+        lo, hi = table[j][0], table[j + 1][0]
+        mid = (lo + hi) / 2
+        xs.append(float(mid))
+        xs.append(float(mid) * (1 + 2.0 ** -45))
+        xs.append(float(mid) * (1 - 2.0 ** -45))
+    got = oracle_lib.f64_to_bf16(np.array(xs))
+    biggest = table[-1][0]
+    for x, g in zip(xs, got):
+        fx = Fraction(x)
+        if abs(fx) > biggest:  # past the largest finite value: defined by the golden cases
+            continue
+        want = _nearest_even(fx, table, keys)
+        if want == 0x0000 and x < 0:
+            want = 0x8000
+        assert int(g) == want, f"x={x!r}: got {int(g):#06x} want {want:#06x}"
+
+
+# --- the triple loop ----------------------------------------------------------
+
+@pytest.mark.parametrize("a_cm", [False, True])
+@pytest.mark.parametrize("b_cm", [False, True])
+def test_gemm_exact_rational_tiny(oracle_lib, a_cm, b_cm):
+    """All (M, N, K) in {1..4}^3 against exact rational sums."""
+    for M in range(1, 5):
+        for N in range(1, 5):
+            for K in range(1, 5):
+                seed = 1000 * M + 100 * N + 10 * K + 2 * a_cm + b_cm
+                A = inputs.matrix(M, K, dist="normal", seed=seed, stream=0, scale=3.0)
+                B = inputs.matrix(K, N, dist="normal", seed=seed, stream=1, scale=0.7)
+                C, S = oracle_lib.gemm(_storage(A, a_cm), _storage(B, b_cm), M, N, K,
+                                       a_col_major=a_cm, b_col_major=b_cm)
+                for i in range(M):
+                    for j in range(N):
+                        terms = [_bits_to_fraction(int(A[i, k])) * _bits_to_fraction(int(B[k, j]))
+                                 for k in range(K)]
+                        exact = sum(terms, Fraction(0))
+                        sabs = sum((abs(t) for t in terms), Fraction(0))
+                        bound = (K - 1) * Fraction(1, 2 ** 53) * sabs
+                        assert abs(Fraction(C[i, j]) - exact) <= bound, (M, N, K, i, j)
+                        assert abs(Fraction(S[i, j]) - sabs) <= bound, (M, N, K, i, j)
+
+
+@pytest.mark.parametrize("a_cm,b_cm", [(False, True), (False, False), (True, True), (True, False)])
+def test_gemm_identity(oracle_lib, a_cm, b_cm):
+    M, K = 37, 29
+    A = inputs.matrix(M, K, dist="normal", seed=11, stream=0)
+    ident = np.zeros((K, K), dtype=np.uint16)
+    ident[np.arange(K), np.arange(K)] = 0x3F80
+    C, _ = oracle_lib.gemm(_storage(A, a_cm), _storage(ident, b_cm), M, K, K,
+                           a_col_major=a_cm, b_col_major=b_cm)
+    assert np.array_equal(C, oracle_lib.bf16_to_f64(A))
+    # and I_M A == A
+    identM = np.zeros((M, M), dtype=np.uint16)
+    identM[np.arange(M), np.arange(M)] = 0x3F80
+    C2, _ = oracle_lib.gemm(_storage(identM, a_cm), _storage(A, b_cm), M, K, M,
+                            a_col_major=a_cm, b_col_major=b_cm)
+    assert np.array_equal(C2, oracle_lib.bf16_to_f64(A))
+
+
+@pytest.mark.parametrize("a_cm,b_cm", [(False, True), (True, False)])
+def test_gemm_permutation(oracle_lib, a_cm, b_cm):
+    K, N = 23, 19
+    rng = np.random.default_rng(5)
+    sigma = rng.permutation(K)
+    P = np.zeros((K, K), dtype=np.uint16)
+    P[np.arange(K), sigma] = 0x3F80          # row i of P selects row sigma(i)
+    B = inputs.matrix(K, N, dist="uniform", seed=12, stream=1)
+    C, _ = oracle_lib.gemm(_storage(P, a_cm), _storage(B, b_cm), K, N, K,
+                           a_col_major=a_cm, b_col_major=b_cm)
+    assert np.array_equal(C, oracle_lib.bf16_to_f64(B)[sigma, :])
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1), (7, 5, 3), (64, 48, 200), (33, 70, 515)])
+@pytest.mark.parametrize("a_cm,b_cm", [(False, True), (True, False)])
+def test_gemm_small_integers_exact(oracle_lib, shape, a_cm, b_cm):
+    """Integers in [-4, 4]: every partial sum is an integer below 2^24, so the
+    binary64 definition equals an int64 product exactly (numpy integer matmul,
+    no floating point involved)."""
+    M, N, K = shape
+    A = inputs.matrix(M, K, dist="int4", seed=M + K, stream=0)
+    B = inputs.matrix(K, N, dist="int4", seed=N + K, stream=1)
+    C, S = oracle_lib.gemm(_storage(A, a_cm), _storage(B, b_cm), M, N, K,
+                           a_col_major=a_cm, b_col_major=b_cm)
+    Ai = oracle_lib.bf16_to_f64(A).astype(np.int64)
+    Bi = oracle_lib.bf16_to_f64(B).astype(np.int64)
+    assert np.abs(Ai).max() <= 4 and np.abs(Bi).max() <= 4
+    assert np.array_equal(C, (Ai @ Bi).astype(np.float64))
+    assert np.array_equal(S, (np.abs(Ai) @ np.abs(Bi)).astype(np.float64))
+
+
+def test_gemm_matches_numpy_matmul(oracle_lib):
+    """numpy's binary64 matmul (a library routine, its own summation order)
+    agrees within the binary64 bound on random inputs."""
+    M, N, K = 96, 80, 333
+    A = inputs.matrix(M, K, dist="normal", seed=21, stream=0, scale=K ** -0.5)
+    Bt = inputs.matrix(N, K, dist="normal", seed=21, stream=1, scale=K ** -0.5)
+    C, S = oracle_lib.gemm(A, Bt, M, N, K)
+    ref = oracle_lib.bf16_to_f64(A) @ oracle_lib.bf16_to_f64(Bt).T
+    assert np.all(np.abs(C - ref) <= 2 * K * 2.0 ** -53 * S)
+    refabs = np.abs(oracle_lib.bf16_to_f64(A)) @ np.abs(oracle_lib.bf16_to_f64(Bt)).T
+    assert np.all(np.abs(S - refabs) <= 2 * K * 2.0 ** -53 * refabs)
+
+
+def test_gemm_leading_dimensions(oracle_lib):
+    """Padded leading dimensions read only the logical block."""
+    M, N, K, lda, ldb = 9, 7, 13, 24, 16
+    A = inputs.matrix(M, K, dist="uniform", seed=3, stream=0)
+    Bt = inputs.matrix(N, K, dist="uniform", seed=3, stream=1)
+    Ap = np.full((M, lda), 0x7FC0, dtype=np.uint16)   # NaN padding must never be read
+    Ap[:, :K] = A
+    Bp = np.full((N, ldb), 0x7FC0, dtype=np.uint16)
+    Bp[:, :K] = Bt
+    C1, _ = oracle_lib.gemm(A, Bt, M, N, K)
+    C2, _ = oracle_lib.gemm(Ap, Bp, M, N, K, lda=lda, ldb=ldb)
+    assert np.array_equal(C1, C2)
+
+
+def test_gemm_k_zero_and_empty(oracle_lib):
+    A = np.zeros((3, 0), dtype=np.uint16)
+    Bt = np.zeros((4, 0), dtype=np.uint16)
+    C, S = oracle_lib.gemm(A, Bt, 3, 4, 0, lda=1, ldb=1)
+    assert C.shape == (3, 4) and not C.any() and not S.any()
+    C, _ = oracle_lib.gemm(np.zeros((0, 5), dtype=np.uint16), np.zeros((2, 5), dtype=np.uint16), 0, 2, 5)
+    assert C.shape == (0, 2)
+
+
+def test_gemm_entries_match_full(oracle_lib):
+    M, N, K = 50, 45, 77
+    A = inputs.matrix(M, K, dist="normal", seed=8, stream=0)
+    Bt = inputs.matrix(N, K, dist="normal", seed=8, stream=1)
+    C, S = oracle_lib.gemm(A, Bt, M, N, K)
+    rng = np.random.default_rng(1)
+    r = rng.integers(0, M, 300)
+    c = rng.integers(0, N, 300)
+    e, s = oracle_lib.gemm_entries(A, Bt, M, N, K, r, c)
+    assert np.array_equal(e, C[r, c]) and np.array_equal(s, S[r, c])
+
+
+def test_gemm_threads_do_not_change_results(oracle_lib):
+    M, N, K = 40, 33, 129
+    A = inputs.matrix(M, K, dist="normal", seed=4, stream=0)
+    Bt = inputs.matrix(N, K, dist="normal", seed=4, stream=1)
+    C1, _ = oracle_lib.gemm(A, Bt, M, N, K, threads=1)
+    C4, _ = oracle_lib.gemm(A, Bt, M, N, K, threads=4)
+    assert np.array_equal(C1, C4)
+
+
+# --- closed forms (pages' formulas against hand-computed numbers) -------------
+
+def test_flops():
+    from oracle import plan_forms as pf
+    assert pf.flops(4096, 4096, 4096) == 137_438_953_472
+    assert pf.flops(16384, 8192, 8192) == 2_199_023_255_552
+    assert pf.flops(128, 256, 65536) == 4_294_967_296
+
+
+def test_grid_and_eta_wave_hand_values():
+    """Hand arithmetic for 128x256 tiles on 148 SMs at one CTA per SM:
+    4096^3 -> 32 * 16 = 512 CTAs, 4 waves of 148 (592 slots), 512/592."""
+    from oracle import plan_forms as pf
+    S, b = 148, 1
+    rows = [  # (M, N, G, eta_wave numerator/denominator)
+        (4096, 4096, 512, (512, 592)),
+        (4095, 4096, 512, (512, 592)),
+        (4097, 4096, 528, (528, 592)),
+        (4096, 4104, 544, (544, 592)),
+        (3968, 4096, 496, (496, 592)),
+        (16384, 8192, 4096, (4096, 4144)),
+    ]
+    for M, N, G, (num, den) in rows:
+        assert pf.grid(M, N, 128, 256) == G
+        assert pf.eta_wave(G, S, b) == Fraction(num, den)
+    # 152 SMs: 512 CTAs need 4 waves of 152 = 608 slots
+    assert pf.eta_wave(512, 152, 1) == Fraction(512, 608)
+    # 128 x 128 tiles: 1024 CTAs, 7 waves of 148 = 1036 slots
+    assert pf.grid(4096, 4096, 128, 128) == 1024
+    assert pf.eta_wave(1024, 148, 1) == Fraction(1024, 1036)
+
+
+def test_grid_small_grids_from_the_profile():
+    """Grid 24 and grid 12 on 148 SMs use 24/148 and 12/148 of the device --
+    both under a fifth, as the profile says; their busy shares add to about 35%."""
+    from oracle import plan_forms as pf
+    with open(os.path.join(GOLDEN, "occupancy_grid24.json")) as f:
+        g = json.load(f)["grid_example"]
+    S = g["sms"]
+    conv, gemm = g["kernels"][0], g["kernels"][1]
+    assert pf.eta_wave(conv["grid"], S, 1) == Fraction(24, 148)
+    assert pf.eta_wave(gemm["grid"], S, 1) == Fraction(12, 148)
+    assert Fraction(24, 148) < Fraction(1, 5) and Fraction(12, 148) < Fraction(1, 5)
+    assert abs(conv["share_of_busy_pct"] + gemm["share_of_busy_pct"] - 35) < 0.5
+
+
+def test_split_k_grid_hand_values():
+    """128 x 256 x 65536 is one 128x256 tile; split-K makes the CTAs."""
+    from oracle import plan_forms as pf
+    for split, (num, den) in [(1, (1, 148)), (8, (8, 148)), (32, (32, 148)),
+                              (74, (1, 2)), (148, (1, 1))]:
+        G = pf.grid(128, 256, 128, 256, split)
+        assert G == split
+        assert pf.eta_wave(G, 148, 1) == Fraction(num, den)
+
+
+def test_eta_pad_hand_values():
+    from oracle import plan_forms as pf
+    assert pf.eta_pad(4096, 4096, 4096, 128, 256, 64) == 1
+    assert pf.eta_pad(4097, 4096, 4096, 128, 256, 64) == Fraction(4097, 4224)
+    assert pf.eta_pad(4095, 4096, 4096, 128, 256, 64) == Fraction(4095, 4096)
+    assert pf.eta_pad(4096, 4104, 4096, 128, 256, 64) == Fraction(4104, 4352)
+    assert pf.eta_pad(4096, 4096, 4088, 128, 256, 64) == Fraction(4088, 4096)
+    assert pf.eta_pad(1, 1, 1, 128, 256, 64) == Fraction(1, 128 * 256 * 64)
+
+
+def test_occupancy_worked_example():
+    """230,400 B of shared memory and 155 registers x 256 threads: 40,960
+    registers per CTA, 81,920 for two (over 65,536), one CTA per SM, and
+    still one with no shared memory at all -- registers bind first."""
+    from oracle import plan_forms as pf
+    with open(os.path.join(GOLDEN, "occupancy_grid24.json")) as f:
+        ex = json.load(f)["occupancy_example"]
+    rpc = pf.regs_per_cta(ex["regs_per_thread"], ex["threads_per_cta"])
+    assert rpc == ex["regs_per_cta_stated"]
+    assert 2 * rpc == ex["regs_for_two_ctas_stated"] > ex["regs_per_sm"]
+    b, lim = pf.ctas_per_sm(regs_per_thread=ex["regs_per_thread"], threads=ex["threads_per_cta"],
+                            smem_per_cta=ex["smem_per_cta_bytes"], regs_per_sm=ex["regs_per_sm"],
+                            smem_per_sm=227 * 1024, smem_reserved_per_cta=0)
+    assert (b, lim) == (ex["ctas_per_sm_stated"], ex["binding_first"])
+    b0, lim0 = pf.ctas_per_sm(regs_per_thread=ex["regs_per_thread"], threads=ex["threads_per_cta"],
+                              smem_per_cta=0, regs_per_sm=ex["regs_per_sm"])
+    assert (b0, lim0) == (1, "registers")
+    # shared memory alone also allows exactly one
+    assert (227 * 1024) // ex["smem_per_cta_bytes"] == 1
