@@ -1,0 +1,475 @@
+#!/usr/bin/env python3
+"""BF16 Tensor Core GEMM benchmark on GB300: TFLOP/s = 2MNK / device time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-cpu-baseline] [--all-workloads]
+
+A step is one GEMM C = A . B over one batch of synthetic input (the whole hot
+path: plan, TMA-fed tcgen05 main loop, epilogue, and the split-K combine when
+the workload uses it).  The default workload is the square 4096^3 GEMM with
+bf16 A (row-major), B (column-major) and C, inputs N(0,1)/sqrt(K).
+
+Timing: W untimed warm-up steps, then K steps bracketed by a barrier and
+torch.cuda.synchronize() on both sides, CUDA events on the launching stream
+around the whole region and around each launch.  Operands rotate through
+enough copies that the bytes touched between two uses of one copy exceed L2,
+so every step reads its inputs from HBM.  Under torchrun each rank runs the
+same GEMM on its own GPU (the GEMM does not shard: replicas only); the time
+is the maximum over ranks and the value counts every rank's FLOPs.
+
+Prints one JSON line on rank 0.  ``--impl reference`` times the CPU oracle
+(binary64 triple loop) on the host cores instead, on bounded row samples of
+the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import glob
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s (2MNK/device time) and % of GB300 dense BF16 peak, 1 GPU"
+UNIT = "TFLOP/s"
+
+WORKLOADS = {
+    "square4096": dict(M=4096, N=4096, K=4096, out="bf16", dist="normal", scaled=True, split_k=0,
+                       desc="gemm_bf16 M=N=K=4096, A bf16 row-major, B bf16 column-major, C bf16 row-major, "
+                            "inputs N(0,1)/sqrt(K), fp32 accumulate"),
+    "square256": dict(M=256, N=256, K=256, out="f32", dist="uniform", scaled=False, split_k=0,
+                      desc="gemm_bf16 M=N=K=256, A row-major, B column-major, C fp32, inputs uniform[-1,1]"),
+    "n4095": dict(M=4095, N=4096, K=4096, out="bf16", dist="normal", scaled=True, split_k=0,
+                  desc="gemm_bf16 4095x4096x4096, bf16 row x col -> bf16, N(0,1)/sqrt(K)"),
+    "n4097": dict(M=4097, N=4096, K=4096, out="bf16", dist="normal", scaled=True, split_k=0,
+                  desc="gemm_bf16 4097x4096x4096, bf16 row x col -> bf16, N(0,1)/sqrt(K)"),
+    "k4088": dict(M=4096, N=4096, K=4088, out="bf16", dist="normal", scaled=True, split_k=0,
+                  desc="gemm_bf16 4096x4096x4088, bf16 row x col -> bf16, N(0,1)/sqrt(K)"),
+    "n4104": dict(M=4096, N=4104, K=4096, out="bf16", dist="normal", scaled=True, split_k=0,
+                  desc="gemm_bf16 4096x4104x4096, bf16 row x col -> bf16, N(0,1)/sqrt(K)"),
+    "m3968": dict(M=3968, N=4096, K=4096, out="bf16", dist="normal", scaled=True, split_k=0,
+                  desc="gemm_bf16 3968x4096x4096, bf16 row x col -> bf16, N(0,1)/sqrt(K)"),
+    "large": dict(M=16384, N=8192, K=8192, out="bf16", dist="normal", scaled=True, split_k=0,
+                  desc="gemm_bf16 16384x8192x8192, bf16 row x col -> bf16, N(0,1)/sqrt(K)"),
+    "large_one_cta_per_tile": dict(M=16384, N=8192, K=8192, out="bf16", dist="normal", scaled=True, split_k=0,
+                                   non_persistent=True,
+                                   desc="gemm_bf16 16384x8192x8192, bf16 row x col -> bf16, one CTA per tile"),
+}
+for _s in (1, 8, 32, 74, 148):
+    WORKLOADS[f"splitk{_s}"] = dict(M=128, N=256, K=65536, out="f32", dist="uniform", scaled=True, split_k=_s,
+                                    desc=f"gemm_bf16 128x256x65536, bf16 row x col -> fp32, uniform[-1,1]/sqrt(K), "
+                                         f"split_k={_s}")
+
+KERNEL_NAME = "gemm_bf16_tcgen05_kernel"
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return dict(bf16_burst=float(d["bf16_tflops"]), bf16_sustained=float(d["bf16_tflops_sustained"]),
+                    hbm_gbs=float(d["hbm_gbs"]), source="measured")
+    return dict(bf16_burst=1900.0, bf16_sustained=1700.0, hbm_gbs=6800.0, source="fallback")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "dense_tensor_core_bf16_gb300", "csrc", "*")))
+    files.append(os.path.join(ROOT, "include", "gemm_bf16.h"))
+    for fn in files:
+        with open(fn, "rb") as f:
+            h.update(os.path.basename(fn).encode())
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the main kernel from a committed ncu summary,
+    if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"dram_traffic_{workload}.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ---- clocks sampled during the timed region ------------------------------------------
+
+class ClockSampler:
+    FIELDS = ["timestamp", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str, period_ms: int = 100):
+        self.rows = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", gpu_id, f"--query-gpu={','.join(self.FIELDS)}", "--format=csv,noheader,nounits",
+                 f"-lms={period_ms}"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                self.rows.append((ts, float(parts[1]), float(parts[2]), parts[4:]))
+            except ValueError:
+                continue
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi gave no samples"}
+        inside = [r for r in self.rows if t0 <= r[0] <= t1]
+        note = "samples inside the timed region"
+        if not inside:
+            mid = 0.5 * (t0 + t1)
+            inside = sorted(self.rows, key=lambda r: abs(r[0] - mid))[:3]
+            note = "timed region shorter than the sampling period: nearest samples"
+        names = ["active_mask", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in inside:
+            for n, v in zip(names[1:], r[3][1:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": sorted(reasons), "samples": len(inside), "note": note}
+
+
+# ---- distributed plumbing (host-side only: barrier and max/sum of scalars) ------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(ms_local: float, flops_local: float, group=None):
+    """(max elapsed ms over ranks, total FLOPs over ranks)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized():
+        return ms_local, flops_local
+    dev = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
+    t = torch.tensor([ms_local], dtype=torch.float64, device=dev)
+    f = torch.tensor([flops_local], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    dist.all_reduce(f, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item()), float(f.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---- the GPU arm ---------------------------------------------------------------------
+
+def make_host_operands(w):
+    from dense_tensor_core_bf16_gb300 import inputs
+    seed = inputs.DEFAULT_SEED + 100
+    return inputs.workload_operands(w["M"], w["N"], w["K"], dist=w["dist"], scaled=w["scaled"], seed=seed), seed
+
+
+def run_gpu(args, wname: str, w: dict, cpu_baseline: bool):
+    import numpy as np
+    import torch
+
+    import dense_tensor_core_bf16_gb300 as g
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    M, N, K = w["M"], w["N"], w["K"]
+    out_dtype = torch.bfloat16 if w["out"] == "bf16" else torch.float32
+    (A_h, Bt_h), seed = make_host_operands(w)
+
+    st, plan = g.gemm_plan(M, N, K, g.GEMM_ROW_MAJOR, g.GEMM_COL_MAJOR,
+                           g.GEMM_OUT_BF16 if w["out"] == "bf16" else g.GEMM_OUT_F32, w["split_k"])
+    if st:
+        raise g.GemmError(st, "gemm_plan")
+    if plan.workspace_bytes:
+        st = g.gemm_reserve_workspace(plan.workspace_bytes)
+        if st:
+            raise g.GemmError(st, "gemm_reserve_workspace")
+
+    props = torch.cuda.get_device_properties(local)
+    l2 = getattr(props, "L2_cache_size", 135_528_448) or 135_528_448
+    esize = 2 if w["out"] == "bf16" else 4
+    set_bytes = 2 * M * K + 2 * N * K + esize * M * N
+    copies = max(2, math.ceil(2 * l2 / set_bytes) + 1)
+
+    A0 = torch.from_numpy(A_h.view(np.int16)).cuda().view(torch.bfloat16)
+    B0 = torch.from_numpy(Bt_h.view(np.int16)).cuda().view(torch.bfloat16)
+    sets = []
+    for i in range(copies):
+        a = A0 if i == 0 else A0.clone()
+        b = B0 if i == 0 else B0.clone()
+        c = torch.empty((M, N), dtype=out_dtype, device="cuda")
+        sets.append((a, b.t(), c))
+    kw = dict(split_k=w["split_k"], non_persistent=w.get("non_persistent", False))
+    launches_per_step = 1 + (1 if plan.split_k > 1 else 0)
+
+    def step(i, **extra):
+        a, b, c = sets[i % copies]
+        g.matmul(a, b, out=c, **kw, **extra)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    st, where = g.gemm_get_device_status(None)
+    if st:
+        raise RuntimeError(f"device fault during warm-up: {where:#x}")
+
+    gpu_id = getattr(props, "uuid", None)
+    gpu_id = f"GPU-{gpu_id}" if gpu_id is not None else str(local)
+    sampler = ClockSampler(gpu_id)
+    time.sleep(0.3)
+
+    stream = torch.cuda.current_stream()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)] if plan.split_k > 1 else None
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    e0.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        if mids is not None:
+            step(i, mainloop_done_event=mids[i])
+        else:
+            step(i)
+        ends[i].record(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    t_wall1 = time.time()
+    time.sleep(0.25)
+    sampler.stop()
+    st, where = g.gemm_get_device_status(None)
+    if st:
+        raise RuntimeError(f"device fault in the timed region: {where:#x}")
+
+    total_ms = e0.elapsed_time(e1)
+    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    main_ms = [s.elapsed_time(m) for s, m in zip(starts, mids)] if mids else per_launch_ms
+    combine_ms = [m.elapsed_time(e) for m, e in zip(mids, ends)] if mids else None
+
+    flops = 2.0 * M * N * K
+    max_ms, total_flops = aggregate(total_ms, flops * args.steps)
+    value = total_flops / (max_ms * 1e-3) / 1e12
+
+    peaks = load_peaks()
+    long_region = (t_wall1 - t_wall0) > 1.0
+    peak = peaks["bf16_sustained"] if long_region else peaks["bf16_burst"]
+    peak_kind = ("sustained" if long_region else "burst") + f" bf16, {peaks['source']}"
+    mean_main_ms = statistics.fmean(main_ms)
+    achieved = flops / (mean_main_ms * 1e-3) / 1e12
+    result = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": f"synthetic (seeded SplitMix64, {w['dist']}{'/sqrt(K)' if w['scaled'] else ''}, seed {seed})",
+        "config": {
+            "workload": w["desc"], "M": M, "N": N, "K": K, "out": w["out"],
+            "tile": f"{plan.tile_m}x{plan.tile_n}x{plan.tile_k}", "stages": plan.stages,
+            "split_k": plan.split_k, "persistent": bool(plan.persistent), "grid_G": plan.grid,
+            "launch_ctas": plan.launch_ctas, "num_sms": plan.num_sms, "ctas_per_sm": plan.ctas_per_sm,
+            "occupancy_limiter": g.LIMITERS[plan.occupancy_limiter],
+            "eta_wave": round(plan.eta_wave, 5), "eta_pad": round(plan.eta_pad, 5),
+            "pct_of_peak": round(100.0 * value / world / peak, 2), "peak_tflops": peak, "peak_kind": peak_kind,
+            "l2": f"inputs larger than L2: {copies} rotating operand sets of {set_bytes / 1e6:.1f} MB "
+                  f"({copies * set_bytes / 1e6:.0f} MB) vs L2 {l2 / 1e6:.1f} MB",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "roofline": {
+            "bound": "tensor", "kernel": KERNEL_NAME, "achieved": round(achieved, 3), "peak": peak,
+            "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": recorded_traffic(wname),
+            "algorithmic_flops_per_launch": flops, "mean_launch_ms": round(mean_main_ms, 6),
+            "peak_source": peak_kind,
+        },
+        "gpu_launches": launches_per_step * args.steps,
+    }
+    if combine_ms is not None:
+        comb = statistics.fmean(combine_ms)
+        comb_bytes = plan.split_k * M * ((N + 3) // 4 * 4) * 4 + esize * M * N
+        result["config"]["mainloop_us"] = round(mean_main_ms * 1e3, 3)
+        result["config"]["combine_us"] = round(comb * 1e3, 3)
+        result["config"]["combine_gbs"] = round(comb_bytes / (comb * 1e-3) / 1e9, 1)
+    clocks = sampler.summary(t_wall0, t_wall1)
+    result["clocks"] = clocks
+
+    # end to end through the public API: pinned host operands in, C back out, every step
+    e2e_steps = min(args.steps, 20)
+    hA = torch.from_numpy(A_h.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hB = torch.from_numpy(Bt_h.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hC = torch.empty((M, N), dtype=out_dtype).pin_memory()
+    dA, dB, dC = sets[0][0], sets[0][1].t(), sets[0][2]
+    for _ in range(2):
+        dA.copy_(hA, non_blocking=True)
+        dB.copy_(hB, non_blocking=True)
+        g.matmul(dA, dB.t(), out=dC, **kw)
+        hC.copy_(dC, non_blocking=True)
+    torch.cuda.synchronize()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    f0.record(stream)
+    for _ in range(e2e_steps):
+        dA.copy_(hA, non_blocking=True)
+        dB.copy_(hB, non_blocking=True)
+        g.matmul(dA, dB.t(), out=dC, **kw)
+        hC.copy_(dC, non_blocking=True)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms, e2e_flops = aggregate(f0.elapsed_time(f1), flops * e2e_steps)
+    result["e2e"] = {"value": round(e2e_flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
+                     "h2d_bytes_per_step": int(hA.numel() * 2 + hB.numel() * 2),
+                     "d2h_bytes_per_step": int(hC.numel() * hC.element_size()), "steps": e2e_steps}
+
+    if cpu_baseline and rank == 0 and world == 1:
+        result["cpu_baseline"] = cpu_oracle_baseline(A_h, Bt_h, M, N, K, target_s=args.cpu_seconds)
+    return result, rank
+
+
+# ---- the oracle on the host cores ---------------------------------------------------------
+
+def cpu_oracle_baseline(A_h, Bt_h, M, N, K, target_s: float):
+    """Time the oracle, as it stands, on the first R rows of C (R x N outputs at
+    the workload's K), R sized for about target_s seconds of CPU work."""
+    import oracle
+    oracle.build()
+    cores = oracle.max_threads()
+    r0 = min(M, 4)
+    t = time.perf_counter()
+    oracle.gemm(A_h[:r0], Bt_h, r0, N, K, with_abs=False)
+    dt0 = max(time.perf_counter() - t, 1e-3)
+    rows = int(min(M, max(1, math.floor(r0 * target_s / dt0))))
+    t = time.perf_counter()
+    oracle.gemm(A_h[:rows], Bt_h, rows, N, K, with_abs=False)
+    dt = time.perf_counter() - t
+    return {"value": round(2.0 * rows * N * K / dt / 1e12, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of C ({rows}x{N} outputs, K={K}), binary64 triple loop, "
+                      f"{cores} OpenMP threads, {dt:.1f} s"}
+
+
+def run_reference(args, wname: str, w: dict):
+    """The oracle as the reference arm: each step is a bounded row sample."""
+    import oracle
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None, rank
+    oracle.build()
+    (A_h, Bt_h), seed = make_host_operands(w)
+    M, N, K = w["M"], w["N"], w["K"]
+    cores = oracle.max_threads()
+    budget_s = min(3.0, 150.0 / max(1, args.steps + args.warmup))
+    r0 = min(M, 2)
+    t = time.perf_counter()
+    oracle.gemm(A_h[:r0], Bt_h, r0, N, K, with_abs=False)
+    dt0 = max(time.perf_counter() - t, 1e-4)
+    rows = int(min(M, max(1, math.floor(r0 * budget_s / dt0))))
+    for i in range(args.warmup):
+        s = (i * rows) % max(1, M - rows + 1)
+        oracle.gemm(A_h[s:s + rows], Bt_h, rows, N, K, with_abs=False)
+    t = time.perf_counter()
+    for i in range(args.steps):
+        s = (i * rows) % max(1, M - rows + 1)
+        oracle.gemm(A_h[s:s + rows], Bt_h, rows, N, K, with_abs=False)
+    dt = time.perf_counter() - t
+    value = 2.0 * rows * N * K * args.steps / dt / 1e12
+    sample = (f"each step: {rows} rows of C ({rows}x{N} outputs, K={K}) of the workload, binary64 triple loop, "
+              f"{cores} OpenMP threads")
+    result = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": f"synthetic (seeded SplitMix64, {w['dist']}, seed {seed})",
+        "config": {"workload": w["desc"], "M": M, "N": N, "K": K, "out": w["out"]},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return result, rank
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="square4096")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--all-workloads", action="store_true",
+                    help="run every workload (one JSON line each, no CPU baseline)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        res, rank = run_reference(args, args.workload, WORKLOADS[args.workload])
+        if rank == 0 and res is not None:
+            print(json.dumps(res), flush=True)
+        return 0
+
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    try:
+        names = sorted(WORKLOADS) if args.all_workloads else [args.workload]
+        for name in names:
+            res, rank = run_gpu(args, name, WORKLOADS[name],
+                                cpu_baseline=not args.no_cpu_baseline and not args.all_workloads)
+            if rank == 0:
+                if args.all_workloads:
+                    res["config"]["name"] = name
+                print(json.dumps(res), flush=True)
+    finally:
+        if world > 1 and dist.is_initialized():
+            dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

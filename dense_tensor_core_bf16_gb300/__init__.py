@@ -1,0 +1,258 @@
+"""GB300 BF16 Tensor Core GEMM: Python binding of ``libgemm_bf16.so``.
+
+Argument marshalling only.  Every step of the GEMM runs in the library's CUDA
+kernels; PyTorch provides device memory and streams.  The functions below
+carry the names of the C ABI in ``include/gemm_bf16.h`` and take the same
+arguments (device pointers as integers, the stream as a ``cudaStream_t``
+integer or None); :func:`matmul` wraps them for torch tensors.
+
+Importing the package does not load the library; the first call does, and
+raises :class:`LibraryNotBuilt` if ``_build/libgemm_bf16.so`` is missing --
+there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+from . import _build
+
+__all__ = [
+    "GEMM_ROW_MAJOR", "GEMM_COL_MAJOR", "GEMM_OUT_F32", "GEMM_OUT_BF16", "GemmError", "LibraryNotBuilt",
+    "gemm_device_desc_t", "gemm_kernel_desc_t", "gemm_plan_t", "gemm_options_t",
+    "gemm_bf16", "gemm_bf16_ex", "gemm_plan", "gemm_plan_for_device", "gemm_occupancy",
+    "gemm_device_desc_query", "gemm_kernel_desc", "gemm_reserve_workspace", "gemm_release_workspace",
+    "gemm_get_device_status", "gemm_status_string", "gemm_limiter_string", "matmul", "lib", "header_functions",
+]
+
+GEMM_ROW_MAJOR, GEMM_COL_MAJOR = 0, 1
+GEMM_OUT_F32, GEMM_OUT_BF16 = 0, 1
+STATUS_NAMES = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_VALUE", 2: "GEMM_ERR_MISALIGNED", 3: "GEMM_ERR_NOT_SUPPORTED",
+                4: "GEMM_ERR_NO_DEVICE", 5: "GEMM_ERR_OUT_OF_MEMORY", 6: "GEMM_ERR_LAUNCH",
+                7: "GEMM_ERR_DEVICE_TIMEOUT"}
+LIMITERS = {0: "registers", 1: "smem", 2: "tmem", 3: "threads", 4: "blocks"}
+
+
+class LibraryNotBuilt(ImportError):
+    pass
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, where: str = ""):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}" if where else STATUS_NAMES.get(status, str(status)))
+
+
+class gemm_device_desc_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "num_sms", "smem_per_sm", "smem_optin_per_cta", "smem_reserved_per_cta", "regs_per_sm",
+        "max_threads_per_sm", "max_ctas_per_sm", "tmem_cols_per_sm")]
+
+
+class gemm_kernel_desc_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("regs_per_thread", "threads_per_cta", "smem_per_cta", "tmem_cols_per_cta")]
+
+
+class gemm_plan_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "tile_m", "tile_n", "tile_k", "stages", "threads_per_cta", "split_k", "k_tiles", "k_tiles_per_split",
+        "num_sms", "ctas_per_sm", "occupancy_limiter", "persistent")] + \
+        [(n, ctypes.c_int64) for n in ("tiles", "grid", "launch_ctas", "m_padded", "n_padded", "k_padded")] + \
+        [(n, ctypes.c_double) for n in ("eta_wave", "eta_pad", "flops")] + \
+        [("smem_bytes", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64), ("tmem_cols", ctypes.c_int)]
+
+    def as_dict(self) -> dict:
+        d = {n: getattr(self, n) for n, _ in self._fields_}
+        d["occupancy_limiter"] = LIMITERS.get(d["occupancy_limiter"], "unknown")
+        return d
+
+
+class gemm_options_t(ctypes.Structure):
+    _fields_ = [("split_k", ctypes.c_int), ("non_persistent", ctypes.c_int), ("raster_group_m", ctypes.c_int),
+                ("mainloop_done_event", ctypes.c_void_p), ("timeout_ms", ctypes.c_int),
+                ("debug_skip_load", ctypes.c_int)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises LibraryNotBuilt if it has not been compiled."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_build.LIB_PATH):
+            raise LibraryNotBuilt(
+                f"{_build.LIB_PATH} is missing: build it with __graft_entry__.build() "
+                "(nvcc, sm_103a); there is no non-CUDA fallback")
+        L = ctypes.CDLL(_build.LIB_PATH)
+        i64, i32, vp, P = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.POINTER
+        L.gemm_device_desc_query.argtypes = [i32, P(gemm_device_desc_t)]
+        L.gemm_kernel_desc.argtypes = [P(gemm_kernel_desc_t)]
+        L.gemm_occupancy.argtypes = [P(gemm_kernel_desc_t), P(gemm_device_desc_t), P(i32), P(i32)]
+        L.gemm_plan_for_device.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32, P(gemm_device_desc_t),
+                                           P(gemm_kernel_desc_t), P(gemm_plan_t)]
+        L.gemm_plan.argtypes = [i64, i64, i64, i32, i32, i32, i32, P(gemm_plan_t)]
+        L.gemm_bf16.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, i32, i32, i32, vp]
+        L.gemm_bf16_ex.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, i32, i32, P(gemm_options_t), vp]
+        L.gemm_reserve_workspace.argtypes = [ctypes.c_size_t]
+        L.gemm_release_workspace.argtypes = []
+        L.gemm_release_workspace.restype = None
+        L.gemm_get_device_status.argtypes = [vp, P(ctypes.c_uint)]
+        L.gemm_status_string.argtypes = [i32]
+        L.gemm_status_string.restype = ctypes.c_char_p
+        L.gemm_limiter_string.argtypes = [i32]
+        L.gemm_limiter_string.restype = ctypes.c_char_p
+        for name in ("gemm_device_desc_query", "gemm_kernel_desc", "gemm_occupancy", "gemm_plan_for_device",
+                     "gemm_plan", "gemm_bf16", "gemm_bf16_ex", "gemm_reserve_workspace", "gemm_get_device_status"):
+            getattr(L, name).restype = i32
+        _lib = L
+        return L
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/gemm_bf16.h declares."""
+    path = os.path.join(_build.INCLUDE, "gemm_bf16.h")
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(gemm_\w+)\s*\(", text, flags=re.M)))
+
+
+# ---- the C ABI, one Python function per entry point -------------------------
+
+def gemm_device_desc_query(device: int = 0) -> gemm_device_desc_t:
+    d = gemm_device_desc_t()
+    st = lib().gemm_device_desc_query(device, ctypes.byref(d))
+    if st:
+        raise GemmError(st, "gemm_device_desc_query")
+    return d
+
+
+def gemm_kernel_desc() -> gemm_kernel_desc_t:
+    k = gemm_kernel_desc_t()
+    st = lib().gemm_kernel_desc(ctypes.byref(k))
+    if st:
+        raise GemmError(st, "gemm_kernel_desc")
+    return k
+
+
+def gemm_occupancy(kern: gemm_kernel_desc_t, dev: gemm_device_desc_t):
+    """(status, ctas_per_sm, limiter name)."""
+    b, lim = ctypes.c_int(), ctypes.c_int()
+    st = lib().gemm_occupancy(ctypes.byref(kern), ctypes.byref(dev), ctypes.byref(b), ctypes.byref(lim))
+    return st, b.value, LIMITERS.get(lim.value, "unknown")
+
+
+def gemm_plan_for_device(M, N, K, layout_a, layout_b, out_dtype, split_k, persistent,
+                         dev: gemm_device_desc_t, kern: gemm_kernel_desc_t):
+    """(status, gemm_plan_t)."""
+    plan = gemm_plan_t()
+    st = lib().gemm_plan_for_device(M, N, K, layout_a, layout_b, out_dtype, split_k, persistent,
+                                    ctypes.byref(dev), ctypes.byref(kern), ctypes.byref(plan))
+    return st, plan
+
+
+def gemm_plan(M, N, K, layout_a=GEMM_ROW_MAJOR, layout_b=GEMM_COL_MAJOR, out_dtype=GEMM_OUT_BF16, split_k=0):
+    """(status, gemm_plan_t) on the current CUDA device."""
+    plan = gemm_plan_t()
+    st = lib().gemm_plan(M, N, K, layout_a, layout_b, out_dtype, split_k, ctypes.byref(plan))
+    return st, plan
+
+
+def gemm_bf16(M, N, K, A, lda, B, ldb, C, ldc, layout_a, layout_b, out_dtype, split_k, stream) -> int:
+    """Status code of the C call (pointers and stream as integers)."""
+    return lib().gemm_bf16(M, N, K, A, lda, B, ldb, C, ldc, layout_a, layout_b, out_dtype, split_k, stream)
+
+
+def gemm_bf16_ex(M, N, K, A, lda, B, ldb, C, ldc, layout_a, layout_b, out_dtype,
+                 opts: gemm_options_t | None, stream) -> int:
+    return lib().gemm_bf16_ex(M, N, K, A, lda, B, ldb, C, ldc, layout_a, layout_b, out_dtype,
+                              ctypes.byref(opts) if opts is not None else None, stream)
+
+
+def gemm_reserve_workspace(nbytes: int) -> int:
+    return lib().gemm_reserve_workspace(nbytes)
+
+
+def gemm_release_workspace() -> None:
+    lib().gemm_release_workspace()
+
+
+def gemm_get_device_status(stream=None):
+    """(status, where-bits) after synchronising ``stream``."""
+    w = ctypes.c_uint()
+    st = lib().gemm_get_device_status(stream, ctypes.byref(w))
+    return st, w.value
+
+
+def gemm_status_string(status: int) -> str:
+    return lib().gemm_status_string(status).decode()
+
+
+def gemm_limiter_string(limiter: int) -> str:
+    return lib().gemm_limiter_string(limiter).decode()
+
+
+# ---- torch convenience ---------------------------------------------------------
+
+def _round_up(x: int, m: int) -> int:
+    return max(m, (x + m - 1) // m * m)
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def matmul(A, B, *, out_dtype=None, out=None, split_k: int = 0, non_persistent: bool = False,
+           raster_group_m: int = 0, stream=None, mainloop_done_event=None, timeout_ms: int = 0,
+           debug_skip_load: int = 0):
+    """C = A @ B through ``gemm_bf16_ex``.
+
+    ``A``: (M, K) torch.bfloat16 CUDA tensor, row-major (stride (lda, 1)).
+    ``B``: (K, N) torch.bfloat16 CUDA tensor, column-major (stride (1, ldb)),
+    e.g. ``Bt.t()`` for a contiguous (N, K) ``Bt``.
+    ``out``: optional (M, N) row-major float32 or bfloat16 tensor (stride (ldc, 1)).
+    Raises :class:`GemmError` on a non-zero status.
+    """
+    import torch
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
+        raise TypeError("A and B must be torch.bfloat16")
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K:
+        raise ValueError(f"inner dimensions differ: {K} vs {K2}")
+    if out is None:
+        dt = out_dtype if out_dtype is not None else torch.bfloat16
+        out = torch.empty((M, N), dtype=dt, device=A.device)
+    if out.shape != (M, N):
+        raise ValueError("out has the wrong shape")
+    if M and N and out.stride(1) != 1:
+        raise ValueError("out must be row-major")
+    if M and K and A.stride(1) != 1:
+        raise ValueError("A must be row-major (stride (lda, 1))")
+    if N and K and B.stride(0) != 1:
+        raise ValueError("B must be column-major (stride (1, ldb))")
+    odt = {torch.float32: GEMM_OUT_F32, torch.bfloat16: GEMM_OUT_BF16}.get(out.dtype)
+    if odt is None:
+        raise TypeError("out must be float32 or bfloat16")
+    # a single row (column) has no real leading dimension; report the
+    # smallest aligned one so the alignment rule does not reject it
+    lda = A.stride(0) if M > 1 else _round_up(K, 8)
+    ldb = B.stride(1) if N > 1 else _round_up(K, 8)
+    ldc = out.stride(0) if M > 1 else _round_up(N, 8)
+    opts = gemm_options_t(split_k=split_k, non_persistent=int(non_persistent), raster_group_m=raster_group_m,
+                          mainloop_done_event=(mainloop_done_event.cuda_event if mainloop_done_event is not None
+                                               else None),
+                          timeout_ms=timeout_ms, debug_skip_load=debug_skip_load)
+    st = gemm_bf16_ex(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc,
+                      GEMM_ROW_MAJOR, GEMM_COL_MAJOR, odt, opts, _stream_handle(stream))
+    if st:
+        raise GemmError(st, "gemm_bf16_ex")
+    return out

@@ -1,0 +1,169 @@
+// Host-side planning: argument checks, the closed forms of the launch and
+// the occupancy arithmetic.  No CUDA calls; see gemm_bf16.h for the contract.
+//
+// Closed forms: chapter 10 "Tensor Cores, shapes, and tile alignment",
+// sections "Shape the operation" (FLOPs = 2MNK, G = ceil(M/T_M) ceil(N/T_N),
+// eta_wave = G / (ceil(G/(S b)) S b)), "Padding efficiency"
+// (eta_pad = MNK / (M'N'K')) and "When shape alone can't fix wave
+// efficiency" (split-K multiplies the CTAs).  Occupancy: "Grid 24 is not
+// headroom", section "The question I never asked" (registers per CTA =
+// per-thread count, granted in multiples of 8, times the threads; b is the
+// tightest of registers and shared memory).
+#include "gemm_bf16.h"
+#include "plan_internal.h"
+#include "kernel_config.h"
+
+#include <climits>
+#include <cstring>
+
+namespace gemm {
+
+static int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+gemm_status_t check_problem(int64_t M, int64_t N, int64_t K, gemm_layout_t la, gemm_layout_t lb,
+                            gemm_dtype_t out, int split_k) {
+    if (M < 0 || N < 0 || K < 0 || M > INT_MAX || N > INT_MAX || K > INT_MAX) return GEMM_ERR_INVALID_VALUE;
+    if ((la != GEMM_ROW_MAJOR && la != GEMM_COL_MAJOR) || (lb != GEMM_ROW_MAJOR && lb != GEMM_COL_MAJOR))
+        return GEMM_ERR_INVALID_VALUE;
+    if (out != GEMM_OUT_F32 && out != GEMM_OUT_BF16) return GEMM_ERR_INVALID_VALUE;
+    if (split_k < 0) return GEMM_ERR_INVALID_VALUE;
+    if (la != GEMM_ROW_MAJOR || lb != GEMM_COL_MAJOR) return GEMM_ERR_NOT_SUPPORTED;
+    return GEMM_OK;
+}
+
+int round_regs(int regs_per_thread) { return (regs_per_thread + 7) / 8 * 8; }
+
+gemm_status_t occupancy(const gemm_kernel_desc_t &k, const gemm_device_desc_t &d, int *b_out, int *lim_out) {
+    *b_out = 0;
+    *lim_out = GEMM_LIMIT_BLOCKS;
+    if (k.threads_per_cta <= 0 || k.smem_per_cta < 0 || k.tmem_cols_per_cta < 0 || k.regs_per_thread < 0)
+        return GEMM_ERR_INVALID_VALUE;
+    const int64_t big = INT_MAX;
+    int64_t by_regs = big, by_smem = big, by_tmem = big;
+    if (k.regs_per_thread > 0) by_regs = d.regs_per_sm / ((int64_t)round_regs(k.regs_per_thread) * k.threads_per_cta);
+    const int64_t smem_cost = (int64_t)k.smem_per_cta + d.smem_reserved_per_cta;
+    if (smem_cost > 0) by_smem = d.smem_per_sm / smem_cost;
+    if (k.tmem_cols_per_cta > 0) by_tmem = d.tmem_cols_per_sm / k.tmem_cols_per_cta;
+    int64_t by_threads = d.max_threads_per_sm / k.threads_per_cta;
+    int64_t by_blocks = d.max_ctas_per_sm;
+    const int64_t vals[5] = {by_regs, by_smem, by_tmem, by_threads, by_blocks};
+    const int names[5] = {GEMM_LIMIT_REGISTERS, GEMM_LIMIT_SMEM, GEMM_LIMIT_TMEM, GEMM_LIMIT_THREADS,
+                          GEMM_LIMIT_BLOCKS};
+    int64_t b = vals[0];
+    for (int i = 1; i < 5; ++i) b = b < vals[i] ? b : vals[i];
+    for (int i = 0; i < 5; ++i) {
+        if (vals[i] == b) { *lim_out = names[i]; break; }
+    }
+    if (k.smem_per_cta > d.smem_optin_per_cta) b = 0;
+    *b_out = (int)b;
+    return b > 0 ? GEMM_OK : GEMM_ERR_INVALID_VALUE;
+}
+
+int choose_split(int64_t tiles, int k_tiles, int capacity, int requested) {
+    if (k_tiles <= 0) return 1;
+    int s;
+    if (requested > 0) {
+        s = requested;
+    } else {
+        // Automatic: only when the tiles alone fill under half the resident
+        // slots; then give each slot a slice of K, keeping slices at least
+        // MIN_K_TILES_PER_SPLIT k-tiles long.
+        s = 1;
+        if (tiles * 2 <= capacity) {
+            int64_t by_slots = capacity / tiles;
+            int64_t by_k = k_tiles / MIN_K_TILES_PER_SPLIT;
+            int64_t c = by_slots < by_k ? by_slots : by_k;
+            s = c > 1 ? (int)c : 1;
+        }
+    }
+    if (s > k_tiles) s = k_tiles;
+    return s < 1 ? 1 : s;
+}
+
+gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_layout_t la, gemm_layout_t lb,
+                        gemm_dtype_t out, int split_k, int persistent, const gemm_device_desc_t &dev,
+                        const gemm_kernel_desc_t &kern, gemm_plan_t *plan) {
+    gemm_status_t st = check_problem(M, N, K, la, lb, out, split_k);
+    if (st != GEMM_OK) return st;
+    if (dev.num_sms <= 0) return GEMM_ERR_INVALID_VALUE;
+    std::memset(plan, 0, sizeof *plan);
+    int b = 0, lim = 0;
+    st = occupancy(kern, dev, &b, &lim);
+    if (st != GEMM_OK) return st;
+
+    plan->tile_m = TILE_M;
+    plan->tile_n = TILE_N;
+    plan->tile_k = TILE_K;
+    plan->stages = STAGES;
+    plan->threads_per_cta = kern.threads_per_cta;
+    plan->num_sms = dev.num_sms;
+    plan->ctas_per_sm = b;
+    plan->occupancy_limiter = lim;
+    plan->persistent = persistent ? 1 : 0;
+    plan->tiles = cdiv(M, TILE_M) * cdiv(N, TILE_N);
+    plan->k_tiles = (int)cdiv(K, TILE_K);
+    const int capacity = dev.num_sms * b;
+    plan->split_k = (plan->tiles > 0) ? choose_split(plan->tiles, plan->k_tiles, capacity, split_k) : 1;
+    plan->k_tiles_per_split = plan->k_tiles > 0 ? (int)cdiv(plan->k_tiles, plan->split_k) : 0;
+    plan->grid = plan->tiles * plan->split_k;
+    plan->launch_ctas = persistent ? (plan->grid < capacity ? plan->grid : capacity) : plan->grid;
+    plan->m_padded = cdiv(M, TILE_M) * TILE_M;
+    plan->n_padded = cdiv(N, TILE_N) * TILE_N;
+    plan->k_padded = cdiv(K, TILE_K) * TILE_K;
+    if (plan->grid > 0) {
+        const int64_t waves = cdiv(plan->grid, capacity);
+        plan->eta_wave = (double)plan->grid / ((double)waves * (double)capacity);
+    }
+    if (M > 0 && N > 0 && K > 0) {
+        plan->eta_pad = ((double)M / plan->m_padded) * ((double)N / plan->n_padded) * ((double)K / plan->k_padded);
+    }
+    plan->flops = 2.0 * (double)M * (double)N * (double)K;
+    plan->smem_bytes = SMEM_BYTES;
+    plan->tmem_cols = TMEM_COLS;
+    plan->workspace_bytes = plan->split_k > 1 ? (int64_t)plan->split_k * M * ((N + 3) / 4 * 4) * 4 : 0;
+    return GEMM_OK;
+}
+
+}  // namespace gemm
+
+extern "C" {
+
+gemm_status_t gemm_occupancy(const gemm_kernel_desc_t *kern, const gemm_device_desc_t *dev, int *ctas_per_sm,
+                             int *limiter) {
+    if (!kern || !dev || !ctas_per_sm || !limiter) return GEMM_ERR_INVALID_VALUE;
+    return gemm::occupancy(*kern, *dev, ctas_per_sm, limiter);
+}
+
+gemm_status_t gemm_plan_for_device(int64_t M, int64_t N, int64_t K, gemm_layout_t layout_a, gemm_layout_t layout_b,
+                                   gemm_dtype_t out_dtype, int split_k, int persistent, const gemm_device_desc_t *dev,
+                                   const gemm_kernel_desc_t *kern, gemm_plan_t *plan) {
+    if (!dev || !kern || !plan) return GEMM_ERR_INVALID_VALUE;
+    return gemm::make_plan(M, N, K, layout_a, layout_b, out_dtype, split_k, persistent, *dev, *kern, plan);
+}
+
+const char *gemm_status_string(gemm_status_t s) {
+    switch (s) {
+        case GEMM_OK: return "GEMM_OK";
+        case GEMM_ERR_INVALID_VALUE: return "GEMM_ERR_INVALID_VALUE";
+        case GEMM_ERR_MISALIGNED: return "GEMM_ERR_MISALIGNED";
+        case GEMM_ERR_NOT_SUPPORTED: return "GEMM_ERR_NOT_SUPPORTED";
+        case GEMM_ERR_NO_DEVICE: return "GEMM_ERR_NO_DEVICE";
+        case GEMM_ERR_OUT_OF_MEMORY: return "GEMM_ERR_OUT_OF_MEMORY";
+        case GEMM_ERR_LAUNCH: return "GEMM_ERR_LAUNCH";
+        case GEMM_ERR_DEVICE_TIMEOUT: return "GEMM_ERR_DEVICE_TIMEOUT";
+    }
+    return "GEMM_ERR_UNKNOWN";
+}
+
+const char *gemm_limiter_string(int limiter) {
+    switch (limiter) {
+        case GEMM_LIMIT_REGISTERS: return "registers";
+        case GEMM_LIMIT_SMEM: return "smem";
+        case GEMM_LIMIT_TMEM: return "tmem";
+        case GEMM_LIMIT_THREADS: return "threads";
+        case GEMM_LIMIT_BLOCKS: return "blocks";
+    }
+    return "unknown";
+}
+
+}  // extern "C"

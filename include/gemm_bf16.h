@@ -1,0 +1,230 @@
+/*
+ * gemm_bf16.h -- C ABI of the GB300 (sm_103a) BF16 Tensor Core GEMM library
+ * (libgemm_bf16.so).
+ *
+ * Operation (the pages' "Shape the operation", chapter 10 "Tensor Cores,
+ * shapes, and tile alignment"; the mixed-precision paragraph of "The Tensor
+ * Core" lesson):
+ *
+ *     C[M x N] = A[M x K] . B[K x N]
+ *
+ * with bf16 A and B, products accumulated in fp32 on the Tensor Cores, and C
+ * written as fp32 or as bf16 (round to nearest even).  C is output only: the
+ * "+ C" of D = A x B + C is taken with a zero C (the accumulator starts at
+ * zero), so the previous contents of C are overwritten, never read.
+ *
+ * Conventions shared by every entry point
+ *   - Dimensions are element counts; leading dimensions ("ld") are in
+ *     elements, not bytes.  A row-major X[r][c] lives at X[r*ld + c]; a
+ *     column-major one at X[c*ld + r].
+ *   - Device pointers are raw CUDA device addresses.  The caller owns A, B, C
+ *     and the stream and keeps them alive until the work on the stream has
+ *     finished; the library never frees them.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Every launch is asynchronous on that stream; a return of
+ *     GEMM_OK means the work was enqueued.  Faults found on the device (a
+ *     pipeline wait that ran out of time) are reported by
+ *     gemm_get_device_status().
+ *   - Errors are returned as gemm_status_t; nothing here exits, aborts or
+ *     prints.  Arguments are checked before any CUDA call is made.
+ *
+ * Alignment ("Record pointer alignment, leading dimensions, strides, and all
+ * three contraction dimensions", chapter 10, "Padding efficiency"): the
+ * operands are fed by TMA and stored with 16-byte vector stores, so
+ *   - A, B and C start on a 16-byte boundary;
+ *   - lda and ldb are multiples of 8 (16 bytes of bf16);
+ *   - ldc is a multiple of 8 for bf16 C and of 4 for fp32 C.
+ * M, N and K themselves need no particular multiple: ragged edges are
+ * zero-filled on load and masked on store.  Each of M, N, K must be below
+ * 2^31.
+ */
+#ifndef GEMM_BF16_H
+#define GEMM_BF16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { GEMM_ROW_MAJOR = 0, GEMM_COL_MAJOR = 1 } gemm_layout_t;
+typedef enum { GEMM_OUT_F32 = 0, GEMM_OUT_BF16 = 1 } gemm_dtype_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_VALUE = 1,   /* negative or too large size, bad enum, short ld, NULL */
+    GEMM_ERR_MISALIGNED = 2,      /* a pointer or leading dimension breaks the rules above */
+    GEMM_ERR_NOT_SUPPORTED = 3,   /* a layout pair this build has no kernel for */
+    GEMM_ERR_NO_DEVICE = 4,       /* no usable CUDA device, or not an sm_103 part */
+    GEMM_ERR_OUT_OF_MEMORY = 5,   /* the split-K workspace could not be grown */
+    GEMM_ERR_LAUNCH = 6,          /* a CUDA runtime or driver call failed */
+    GEMM_ERR_DEVICE_TIMEOUT = 7   /* a device-side pipeline wait ran out of time */
+} gemm_status_t;
+
+/* Which resource sets the number of resident CTAs per SM. */
+typedef enum {
+    GEMM_LIMIT_REGISTERS = 0,
+    GEMM_LIMIT_SMEM = 1,
+    GEMM_LIMIT_TMEM = 2,
+    GEMM_LIMIT_THREADS = 3,
+    GEMM_LIMIT_BLOCKS = 4
+} gemm_limiter_t;
+
+/* Facts about one GPU that the plan depends on. */
+typedef struct {
+    int num_sms;                 /* S: streaming multiprocessors */
+    int smem_per_sm;             /* bytes of shared memory per SM */
+    int smem_optin_per_cta;      /* largest dynamic shared memory one CTA may request */
+    int smem_reserved_per_cta;   /* bytes the runtime keeps per resident CTA */
+    int regs_per_sm;             /* 32-bit registers per SM */
+    int max_threads_per_sm;
+    int max_ctas_per_sm;
+    int tmem_cols_per_sm;        /* tensor-memory columns per SM (512 on sm_100-class parts) */
+} gemm_device_desc_t;
+
+/* Resource footprint of one CTA of a kernel. */
+typedef struct {
+    int regs_per_thread;         /* as compiled; 0 = unknown (registers then bind nothing) */
+    int threads_per_cta;
+    int smem_per_cta;            /* dynamic + static shared memory, bytes */
+    int tmem_cols_per_cta;       /* tensor-memory columns allocated by one CTA */
+} gemm_kernel_desc_t;
+
+/*
+ * The launch plan.  Closed forms from chapter 10, "Shape the operation" and
+ * "Padding efficiency":
+ *   grid      G = ceil(M/T_M) ceil(N/T_N) split_k        (split-K adds CTAs,
+ *               "When shape alone can't fix wave efficiency")
+ *   eta_wave    = G / (ceil(G / (S b)) S b)
+ *   eta_pad     = M N K / (M' N' K'),  X' = ceil(X / T_X) T_X
+ * and b, the CTAs per SM, from the tightest resource ("Grid 24 is not
+ * headroom", "The question I never asked"): registers (per-thread count
+ * rounded up to a multiple of 8, times the threads), shared memory (plus the
+ * per-CTA reservation), tensor memory, threads, and the CTA limit.  eta_wave
+ * is reported by that formula for both launch modes; a persistent launch
+ * still runs ceil(G / (S b)) rounds of equal tiles.
+ */
+typedef struct {
+    int tile_m, tile_n, tile_k;  /* T_M x T_N x T_K of one CTA */
+    int stages;                  /* depth of the shared-memory operand ring */
+    int threads_per_cta;
+    int split_k;                 /* splits actually used (after auto choice and clamping) */
+    int k_tiles;                 /* ceil(K / T_K) */
+    int k_tiles_per_split;       /* largest k-tile count of one split */
+    int num_sms;                 /* S */
+    int ctas_per_sm;             /* b */
+    int occupancy_limiter;       /* gemm_limiter_t */
+    int persistent;              /* 1: grid = min(G, S b) CTAs looping over work units */
+    int64_t tiles;               /* ceil(M/T_M) ceil(N/T_N) */
+    int64_t grid;                /* G */
+    int64_t launch_ctas;         /* CTAs actually launched for the main kernel */
+    int64_t m_padded, n_padded, k_padded;  /* M', N', K' */
+    double eta_wave;
+    double eta_pad;
+    double flops;                /* 2 M N K */
+    int64_t smem_bytes;          /* dynamic shared memory per CTA of the main kernel */
+    int64_t workspace_bytes;     /* split-K partial buffer: split_k * M * round_up(N, 4) * 4 */
+    int tmem_cols;               /* tensor-memory columns per CTA */
+} gemm_plan_t;
+
+/* Options of gemm_bf16_ex.  Zero-initialise and set what you need. */
+typedef struct {
+    int split_k;                 /* 0: the plan chooses; 1: off; >1: clamped to [1, k_tiles] */
+    int non_persistent;          /* 1: one CTA per work unit (grid G) instead of a persistent grid */
+    int raster_group_m;          /* m-tiles per raster group for L2 reuse; 0: default (16) */
+    void *mainloop_done_event;   /* cudaEvent_t or NULL: recorded on the stream after the main
+                                    kernel, before the split-K combine kernel */
+    int timeout_ms;              /* per-wait device time limit; 0: default (4000 ms) */
+    int debug_skip_load;         /* test hook; must be 0 in normal use.  k: the producer leaves
+                                    the k-th stage load (1-based, counting from the first load of
+                                    CTA 0) unissued, so its consumer's wait runs out and the call
+                                    ends with GEMM_ERR_DEVICE_TIMEOUT on the device */
+} gemm_options_t;
+
+/* Fill `dev` with the facts of CUDA device `device`. */
+gemm_status_t gemm_device_desc_query(int device, gemm_device_desc_t *dev);
+
+/* The footprint of this library's main kernel.  Registers come from the
+ * compiled kernel when a device is present, else 0. */
+gemm_status_t gemm_kernel_desc(gemm_kernel_desc_t *kern);
+
+/* Resident CTAs per SM for a footprint on a device (host arithmetic only).
+ * Returns INVALID_VALUE for non-positive threads or a footprint that fits
+ * zero times (then *ctas_per_sm is 0). */
+gemm_status_t gemm_occupancy(const gemm_kernel_desc_t *kern, const gemm_device_desc_t *dev,
+                             int *ctas_per_sm, int *limiter);
+
+/* Plan a GEMM for explicit device and kernel facts; host arithmetic only, no
+ * CUDA call.  Same argument rules as gemm_bf16 for the sizes, layouts and
+ * out dtype. */
+gemm_status_t gemm_plan_for_device(int64_t M, int64_t N, int64_t K,
+                                   gemm_layout_t layout_a, gemm_layout_t layout_b,
+                                   gemm_dtype_t out_dtype, int split_k, int persistent,
+                                   const gemm_device_desc_t *dev,
+                                   const gemm_kernel_desc_t *kern, gemm_plan_t *plan);
+
+/* Plan a GEMM on the current CUDA device with this library's kernel. */
+gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K,
+                        gemm_layout_t layout_a, gemm_layout_t layout_b,
+                        gemm_dtype_t out_dtype, int split_k, gemm_plan_t *plan);
+
+/*
+ * C = A . B on `stream`.
+ *   A: M x K bf16, layout_a must be GEMM_ROW_MAJOR (lda >= K).
+ *   B: K x N bf16, layout_b must be GEMM_COL_MAJOR (ldb >= K), i.e. stored as
+ *      N rows of K contiguous values.
+ *   C: M x N row-major (ldc >= N), fp32 or bf16 per out_dtype.
+ *   split_k: 0 = the plan chooses, 1 = off, > 1 = that many K slices
+ *      (clamped to the k-tile count).  With more than one slice the partial
+ *      sums go to an fp32 workspace owned by the library and a second kernel
+ *      adds them in slice order 0, 1, ... and writes C.
+ * Other layouts return GEMM_ERR_NOT_SUPPORTED.  M == 0 or N == 0 is a no-op;
+ * K == 0 writes zeros to C.
+ * The split-K workspace grows on demand with cudaMalloc (a synchronising
+ * call); reserve it beforehand with gemm_reserve_workspace() to keep
+ * allocation out of timed regions and stream captures.
+ * Calls that share the workspace must not overlap in time on different
+ * streams of one device.
+ */
+gemm_status_t gemm_bf16(int64_t M, int64_t N, int64_t K,
+                        const void *A, int64_t lda, const void *B, int64_t ldb,
+                        void *C, int64_t ldc,
+                        gemm_layout_t layout_a, gemm_layout_t layout_b,
+                        gemm_dtype_t out_dtype, int split_k, void *stream);
+
+/* gemm_bf16 with options (launch mode, raster group, timing event, device
+ * time limit).  opts == NULL behaves as gemm_bf16 with split_k = 0. */
+gemm_status_t gemm_bf16_ex(int64_t M, int64_t N, int64_t K,
+                           const void *A, int64_t lda, const void *B, int64_t ldb,
+                           void *C, int64_t ldc,
+                           gemm_layout_t layout_a, gemm_layout_t layout_b,
+                           gemm_dtype_t out_dtype, const gemm_options_t *opts, void *stream);
+
+/* Grow the current device's split-K workspace to at least `bytes`. */
+gemm_status_t gemm_reserve_workspace(size_t bytes);
+
+/* Free the split-K workspaces of every device (waits for each device first). */
+void gemm_release_workspace(void);
+
+/*
+ * Synchronise `stream`, then report and clear the current device's fault
+ * word: GEMM_OK, GEMM_ERR_DEVICE_TIMEOUT (a pipeline wait ran out of time;
+ * if `where` is not NULL it receives the bit set of the waits that gave up:
+ * 1 producer slot wait, 2 MMA operand wait, 4 MMA accumulator wait,
+ * 8 epilogue accumulator wait, 16 end-of-kernel drain), or GEMM_ERR_LAUNCH
+ * if the synchronisation itself failed.
+ */
+gemm_status_t gemm_get_device_status(void *stream, unsigned int *where);
+
+/* A static, human-readable name for a status code. */
+const char *gemm_status_string(gemm_status_t status);
+
+/* Name of a gemm_limiter_t value ("registers", "smem", "tmem", "threads", "blocks"). */
+const char *gemm_limiter_string(int limiter);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_BF16_H */

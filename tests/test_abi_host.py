@@ -1,0 +1,166 @@
+"""The C-ABI library on the host (no GPU needed): it loads, exports what the
+header declares, plans exactly by the pages' closed forms, and rejects bad
+arguments before making any CUDA call."""
+from __future__ import annotations
+
+import ctypes
+import math
+
+import pytest
+
+import dense_tensor_core_bf16_gb300 as g
+from dense_tensor_core_bf16_gb300 import _build
+from oracle import plan_forms as pf
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    _build.build_library()
+    g.lib()
+
+
+GB300 = dict(num_sms=152, smem_per_sm=233472, smem_optin_per_cta=232448, smem_reserved_per_cta=1024,
+             regs_per_sm=65536, max_threads_per_sm=2048, max_ctas_per_sm=32, tmem_cols_per_sm=512)
+
+
+def dev(**over):
+    d = dict(GB300)
+    d.update(over)
+    return g.gemm_device_desc_t(**d)
+
+
+def test_exports_every_declared_function():
+    names = g.header_functions()
+    assert len(names) >= 12
+    L = g.lib()
+    for n in names:
+        assert hasattr(L, n), n
+    for n in names:
+        assert n in g.__all__, f"binding lacks {n}"
+
+
+def test_status_and_limiter_strings():
+    assert g.gemm_status_string(0) == "GEMM_OK"
+    assert g.gemm_status_string(7) == "GEMM_ERR_DEVICE_TIMEOUT"
+    assert [g.gemm_limiter_string(i) for i in range(5)] == ["registers", "smem", "tmem", "threads", "blocks"]
+
+
+def test_occupancy_worked_example_through_the_abi():
+    """230,400 B and 155 registers x 256 threads: one CTA per SM, registers
+    binding first, and still one with no shared memory at all."""
+    d = dev(smem_per_sm=227 * 1024, smem_reserved_per_cta=0, tmem_cols_per_sm=512)
+    k = g.gemm_kernel_desc_t(regs_per_thread=155, threads_per_cta=256, smem_per_cta=230400, tmem_cols_per_cta=0)
+    assert g.gemm_occupancy(k, d) == (0, 1, "registers")
+    k0 = g.gemm_kernel_desc_t(regs_per_thread=155, threads_per_cta=256, smem_per_cta=0, tmem_cols_per_cta=0)
+    assert g.gemm_occupancy(k0, d) == (0, 1, "registers")
+    # 128 registers x 256 threads = 32,768: two fit by registers; smem still allows one
+    k2 = g.gemm_kernel_desc_t(regs_per_thread=128, threads_per_cta=256, smem_per_cta=230400, tmem_cols_per_cta=0)
+    assert g.gemm_occupancy(k2, d) == (0, 1, "smem")
+    k3 = g.gemm_kernel_desc_t(regs_per_thread=32, threads_per_cta=256, smem_per_cta=1000, tmem_cols_per_cta=256)
+    assert g.gemm_occupancy(k3, d) == (0, 2, "tmem")
+    bad = g.gemm_kernel_desc_t(regs_per_thread=32, threads_per_cta=0, smem_per_cta=0, tmem_cols_per_cta=0)
+    assert g.gemm_occupancy(bad, d)[0] == 1
+
+
+def _plan(M, N, K, split=1, persistent=1, d=None, regs=64, out=g.GEMM_OUT_BF16):
+    k = g.gemm_kernel_desc_t(regs_per_thread=regs, threads_per_cta=192, smem_per_cta=197752, tmem_cols_per_cta=512)
+    st, p = g.gemm_plan_for_device(M, N, K, g.GEMM_ROW_MAJOR, g.GEMM_COL_MAJOR, out, split, persistent,
+                                   d or dev(), k)
+    assert st == 0
+    return p
+
+
+WORKLOADS = [(256, 256, 256), (4096, 4096, 4096), (4095, 4096, 4096), (4097, 4096, 4096),
+             (4096, 4096, 4088), (4096, 4104, 4096), (3968, 4096, 4096), (16384, 8192, 8192),
+             (128, 256, 65536), (1, 1, 1), (129, 257, 65)]
+
+
+@pytest.mark.parametrize("S", [148, 152])
+@pytest.mark.parametrize("shape", WORKLOADS)
+def test_plan_matches_oracle_closed_forms(shape, S):
+    M, N, K = shape
+    p = _plan(M, N, K, d=dev(num_sms=S))
+    b, lim = pf.ctas_per_sm(regs_per_thread=64, threads=192, smem_per_cta=197752, regs_per_sm=65536,
+                            smem_per_sm=233472, smem_reserved_per_cta=1024)
+    assert (p.ctas_per_sm, g.LIMITERS[p.occupancy_limiter]) == (b, lim) == (1, "smem")
+    assert (p.tile_m, p.tile_n, p.tile_k) == (128, 256, 64)
+    assert p.tiles == pf.grid(M, N, 128, 256)
+    assert p.grid == pf.grid(M, N, 128, 256, p.split_k)
+    assert p.eta_wave == pytest.approx(float(pf.eta_wave(p.grid, S, b)), rel=1e-15)
+    assert p.eta_pad == pytest.approx(float(pf.eta_pad(M, N, K, 128, 256, 64)), rel=1e-15)
+    assert p.flops == pf.flops(M, N, K)
+    assert (p.m_padded, p.n_padded, p.k_padded) == (pf.padded(M, 128), pf.padded(N, 256), pf.padded(K, 64))
+    assert p.launch_ctas == min(p.grid, S * b)
+    assert p.k_tiles == math.ceil(K / 64)
+
+
+def test_plan_hand_values_148_sms():
+    d = dev(num_sms=148)
+    p = _plan(4096, 4096, 4096, d=d)
+    assert (p.grid, p.launch_ctas) == (512, 148)
+    assert p.eta_wave == pytest.approx(512 / 592, rel=1e-15)
+    p = _plan(4097, 4096, 4096, d=d)
+    assert p.eta_pad == pytest.approx(4097 / 4224, rel=1e-15)
+    p = _plan(4096, 4096, 4096, persistent=0, d=d)
+    assert p.launch_ctas == 512 and p.persistent == 0
+
+
+@pytest.mark.parametrize("split,eta", [(1, 1 / 148), (8, 8 / 148), (32, 32 / 148), (74, 0.5), (148, 1.0)])
+def test_plan_split_k_workload(split, eta):
+    p = _plan(128, 256, 65536, split=split, d=dev(num_sms=148), out=g.GEMM_OUT_F32)
+    assert p.split_k == split and p.grid == split
+    assert p.eta_wave == pytest.approx(eta, rel=1e-15)
+    assert p.eta_pad == 1.0
+    assert p.k_tiles == 1024 and p.k_tiles_per_split == math.ceil(1024 / split)
+    assert p.workspace_bytes == (split * 128 * 256 * 4 if split > 1 else 0)
+
+
+def test_plan_split_k_clamped_and_auto():
+    p = _plan(128, 256, 200, split=50)        # 4 k-tiles: at most 4 slices
+    assert p.split_k == 4
+    p = _plan(128, 256, 65536, split=0)       # auto: one tile, 1024 k-tiles, 152 slots
+    assert p.split_k == 152
+    p = _plan(4096, 4096, 4096, split=0)      # auto: the tiles fill the GPU, no split
+    assert p.split_k == 1
+
+
+def _call(M, N, K, A=16, lda=64, B=16, ldb=64, C=16, ldc=64, la=0, lb=1, out=0, split=1):
+    return g.gemm_bf16(M, N, K, A, lda, B, ldb, C, ldc, la, lb, out, split, None)
+
+
+def test_argument_checks_before_any_cuda_call():
+    # (pointers here are fake; every case must be rejected, or be a no-op, before use)
+    assert _call(-1, 4, 4) == 1
+    assert _call(4, 4, 1 << 31) == 1
+    assert _call(4, 4, 4, la=2) == 1
+    assert _call(4, 4, 4, out=5) == 1
+    assert _call(4, 4, 4, split=-1) == 1
+    assert _call(4, 4, 4, la=1) == 3
+    assert _call(4, 4, 4, lb=0) == 3
+    assert _call(0, 4, 4) == 0            # empty: nothing to do
+    assert _call(4, 0, 4) == 0
+    assert _call(4, 4, 4, C=0) == 1       # NULL C
+    assert _call(4, 64, 4, ldc=32) == 1   # ldc < N
+    assert _call(4, 4, 64, lda=32) == 1   # lda < K
+    assert _call(4, 4, 64, A=0) == 1      # NULL A
+    assert _call(4, 4, 4, A=18) == 2      # A not on 16 bytes
+    assert _call(4, 4, 4, B=24) == 2
+    assert _call(4, 4, 4, C=20) == 2
+    assert _call(4, 4, 60, lda=60) == 2   # 120 bytes: not a multiple of 16
+    assert _call(4, 4, 4, ldc=66) == 2    # fp32: 264 bytes
+    assert _call(4, 4, 4, ldc=68, out=1) == 2   # bf16: 136 bytes
+    opts = g.gemm_options_t(timeout_ms=-1)
+    assert g.gemm_bf16_ex(4, 4, 4, 16, 64, 16, 64, 16, 64, 0, 1, 0, opts, None) == 1
+
+
+def test_plan_argument_checks():
+    k = g.gemm_kernel_desc_t(regs_per_thread=64, threads_per_cta=192, smem_per_cta=197752, tmem_cols_per_cta=512)
+    plan = g.gemm_plan_t()
+    L = g.lib()
+    assert L.gemm_plan_for_device(4, 4, 4, 0, 1, 0, 0, 1, None, ctypes.byref(k), ctypes.byref(plan)) == 1
+    st, _ = g.gemm_plan_for_device(4, 4, 4, 1, 1, 0, 0, 1, dev(), k)
+    assert st == 3
+    too_big = g.gemm_kernel_desc_t(regs_per_thread=64, threads_per_cta=192, smem_per_cta=240000,
+                                   tmem_cols_per_cta=512)
+    st, _ = g.gemm_plan_for_device(4, 4, 4, 0, 1, 0, 0, 1, dev(), too_big)
+    assert st == 1

@@ -1,0 +1,310 @@
+"""GPU parity: the CUDA path through the C ABI against the oracle.
+
+Every case feeds the same seeded bf16 bit patterns to both sides and checks
+the GPU's C element by element (in full where the oracle finishes in seconds,
+on sampled entries at the full workload sizes) against the tolerances in
+tests/_parity.py.
+"""
+from __future__ import annotations
+
+import functools
+import math
+
+import numpy as np
+import pytest
+
+from dense_tensor_core_bf16_gb300 import inputs
+
+from ._parity import check_bf16, check_f32, sample_entries
+
+torch = pytest.importorskip("torch")
+pytestmark = [pytest.mark.gpu, pytest.mark.timeout(900)]
+
+SEED = inputs.DEFAULT_SEED
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import dense_tensor_core_bf16_gb300 as g
+    g.lib()
+    yield
+    st, where = g.gemm_get_device_status(None)
+    assert st == 0, f"device fault word {where:#x}"
+
+
+def _lib():
+    import dense_tensor_core_bf16_gb300 as g
+    return g
+
+
+def to_dev(bits: np.ndarray) -> "torch.Tensor":
+    return torch.from_numpy(np.array(bits, dtype=np.uint16, order="C").view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def _ru(x, m):
+    return max(m, (x + m - 1) // m * m)
+
+
+def to_dev_padded(bits: np.ndarray) -> "torch.Tensor":
+    """rows x cols bf16 on the device, each row padded to a multiple of 8
+    elements (16 bytes) as the ABI's alignment rule asks; returns the view."""
+    rows, cols = bits.shape
+    ld = _ru(cols, 8)
+    buf = np.zeros((rows, ld), dtype=np.uint16)
+    buf[:, :cols] = bits
+    return to_dev(buf)[:, :cols]
+
+
+def from_dev_bf16(t: "torch.Tensor") -> np.ndarray:
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+@functools.lru_cache(maxsize=8)
+def operands(M, N, K, dist, scaled, seed):
+    A, Bt = inputs.workload_operands(M, N, K, dist=dist, scaled=scaled, seed=seed)
+    A.setflags(write=False)
+    Bt.setflags(write=False)
+    return A, Bt
+
+
+def run_gpu(A: np.ndarray, Bt: np.ndarray, M, N, K, out_dtype, **kw):
+    g = _lib()
+    dA, dBt = to_dev_padded(A), to_dev_padded(Bt)
+    ldc = _ru(N, 8)
+    C = torch.empty((M, ldc), dtype=out_dtype, device="cuda")[:, :N]
+    g.matmul(dA, dBt.t(), out=C, **kw)
+    torch.cuda.synchronize()
+    if out_dtype == torch.float32:
+        return C.cpu().numpy()
+    return from_dev_bf16(C)
+
+
+def full_check(oracle, A, Bt, M, N, K, out_dtype, exact=False, **kw):
+    C = run_gpu(A, Bt, M, N, K, out_dtype, **kw)
+    ref, sabs = oracle.gemm(A, Bt, M, N, K)
+    if out_dtype == torch.float32:
+        if exact:
+            assert np.array_equal(C.astype(np.float64), ref), "fp32 output not bit-exact"
+        nbad, worst = check_f32(C, ref, sabs)
+        assert nbad == 0, f"{nbad} fp32 entries outside the bound (worst {worst:.3g} x bound)"
+    else:
+        nbad, neq, ncanc, detail = check_bf16(C, ref, sabs, oracle)
+        if exact:
+            assert neq == 0, f"{neq} bf16 entries differ from RN_bf16(exact)"
+        assert nbad == 0, f"{nbad} bf16 entries outside the tolerance; {detail}"
+        assert ncanc <= max(8, C.size // 10000), f"{ncanc} entries needed the cancellation clause"
+    return C
+
+
+# ---- workload: 256^3, fp32 C (uniform inputs, and the integer bit-exact variant)
+
+def test_square256_uniform_f32(oracle_lib):
+    A, Bt = operands(256, 256, 256, "uniform", False, SEED)
+    full_check(oracle_lib, A, Bt, 256, 256, 256, torch.float32)
+
+
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_square256_small_integers_bit_exact(oracle_lib, out):
+    A, Bt = operands(256, 256, 256, "int4", False, SEED + 1)
+    full_check(oracle_lib, A, Bt, 256, 256, 256, torch.float32 if out == "f32" else torch.bfloat16, exact=True)
+
+
+# ---- shapes the oracle finishes in seconds: several tiles and ragged tails
+
+SMALL_SHAPES = [
+    (128, 256, 64),      # exactly one tile, one k-tile
+    (129, 257, 65),      # one past every tile edge
+    (300, 520, 200),
+    (513, 769, 1000),
+    (255, 511, 136),
+    (1, 1, 8),
+    (64, 40, 8),
+    (384, 1024, 512),    # 3 x 4 tiles, several rounds per CTA when the grid is capped
+]
+
+
+@pytest.mark.parametrize("shape", SMALL_SHAPES)
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_small_shapes_normal(oracle_lib, shape, out):
+    M, N, K = shape
+    A, Bt = operands(M, N, K, "normal", True, SEED + 2)
+    full_check(oracle_lib, A, Bt, M, N, K, torch.float32 if out == "f32" else torch.bfloat16)
+
+
+@pytest.mark.parametrize("shape", [(129, 257, 65), (513, 769, 1000), (384, 1024, 512)])
+def test_small_shapes_integers_exact(oracle_lib, shape):
+    M, N, K = shape
+    A, Bt = operands(M, N, K, "int4", False, SEED + 3)
+    full_check(oracle_lib, A, Bt, M, N, K, torch.float32, exact=True)
+    full_check(oracle_lib, A, Bt, M, N, K, torch.bfloat16, exact=True)
+
+
+@pytest.mark.parametrize("split", [2, 3, 7])
+def test_small_split_k(oracle_lib, split):
+    M, N, K = 200, 300, 1000
+    A, Bt = operands(M, N, K, "normal", True, SEED + 4)
+    full_check(oracle_lib, A, Bt, M, N, K, torch.float32, split_k=split)
+    full_check(oracle_lib, A, Bt, M, N, K, torch.bfloat16, split_k=split)
+    Ai, Bti = operands(M, N, K, "int4", False, SEED + 5)
+    full_check(oracle_lib, Ai, Bti, M, N, K, torch.float32, exact=True, split_k=split)
+
+
+def test_non_persistent_matches_persistent_bitwise(oracle_lib):
+    M, N, K = 640, 1280, 320
+    A, Bt = operands(M, N, K, "normal", True, SEED + 6)
+    C1 = run_gpu(A, Bt, M, N, K, torch.float32)
+    C2 = run_gpu(A, Bt, M, N, K, torch.float32, non_persistent=True)
+    C3 = run_gpu(A, Bt, M, N, K, torch.float32, raster_group_m=1)
+    assert np.array_equal(C1, C2) and np.array_equal(C1, C3)
+    ref, sabs = oracle_lib.gemm(A, Bt, M, N, K)
+    assert check_f32(C1, ref, sabs)[0] == 0
+
+
+# ---- edge cases -------------------------------------------------------------------
+
+def test_padded_leading_dimensions_and_guard_band(oracle_lib):
+    """lda, ldb, ldc larger than the logical sizes; everything outside the
+    M x N block of C (padding columns and guard rows) keeps its sentinel."""
+    g = _lib()
+    M, N, K = 190, 300, 100
+    lda, ldb, ldc = 104, 112, 320
+    A, Bt = operands(M, N, K, "normal", True, SEED + 7)
+    Ap = np.full((M, lda), 0x7FC0, dtype=np.uint16)
+    Ap[:, :K] = A
+    Bp = np.full((N, ldb), 0x7FC0, dtype=np.uint16)
+    Bp[:, :K] = Bt
+    dA, dB = to_dev(Ap), to_dev(Bp)
+    guard = 64
+    Cbuf = torch.full(((M + 2 * guard) * ldc,), -7.0, dtype=torch.float32, device="cuda")
+    Cview = Cbuf[guard * ldc:(guard + M) * ldc].view(M, ldc)
+    st = g.gemm_bf16(M, N, K, dA.data_ptr(), lda, dB.data_ptr(), ldb, Cview.data_ptr(), ldc,
+                     g.GEMM_ROW_MAJOR, g.GEMM_COL_MAJOR, g.GEMM_OUT_F32, 1, torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    host = Cbuf.cpu().numpy()
+    assert np.all(host[:guard * ldc] == -7.0) and np.all(host[(guard + M) * ldc:] == -7.0)
+    body = host[guard * ldc:(guard + M) * ldc].reshape(M, ldc)
+    assert np.all(body[:, N:] == -7.0)
+    ref, sabs = oracle_lib.gemm(A, Bt, M, N, K)
+    assert check_f32(body[:, :N], ref, sabs)[0] == 0
+
+
+def test_empty_and_zero_k(oracle_lib):
+    g = _lib()
+    s = torch.cuda.current_stream().cuda_stream
+    C = torch.full((16, 24), 3.0, device="cuda")
+    A = torch.zeros(16, 8, dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros(24, 8, dtype=torch.bfloat16, device="cuda")
+    # M == 0 and N == 0: no-op
+    assert g.gemm_bf16(0, 24, 8, A.data_ptr(), 8, B.data_ptr(), 8, C.data_ptr(), 24, 0, 1, 0, 1, s) == 0
+    assert g.gemm_bf16(16, 0, 8, A.data_ptr(), 8, B.data_ptr(), 8, C.data_ptr(), 24, 0, 1, 0, 1, s) == 0
+    torch.cuda.synchronize()
+    assert torch.all(C == 3.0)
+    # K == 0: the empty sum
+    assert g.gemm_bf16(16, 24, 0, 0, 8, 0, 8, C.data_ptr(), 24, 0, 1, 0, 1, s) == 0
+    torch.cuda.synchronize()
+    assert torch.all(C == 0.0)
+    Cb = torch.full((16, 24), 3.0, dtype=torch.bfloat16, device="cuda")
+    assert g.gemm_bf16(16, 24, 0, 0, 8, 0, 8, Cb.data_ptr(), 24, 0, 1, 1, 1, s) == 0
+    torch.cuda.synchronize()
+    assert torch.all(Cb == 0.0)
+
+
+def test_argument_errors_on_device():
+    g = _lib()
+    s = torch.cuda.current_stream().cuda_stream
+    A = torch.zeros(64, 64, dtype=torch.bfloat16, device="cuda")
+    C = torch.zeros(64, 64, dtype=torch.float32, device="cuda")
+    p = A.data_ptr()
+    assert g.gemm_bf16(64, 64, 64, p + 2, 64, p, 64, C.data_ptr(), 64, 0, 1, 0, 1, s) == 2   # A off 16 B
+    assert g.gemm_bf16(64, 64, 60, p, 60, p, 64, C.data_ptr(), 64, 0, 1, 0, 1, s) == 2       # lda % 8
+    assert g.gemm_bf16(64, 64, 64, p, 64, p, 64, C.data_ptr(), 66, 0, 1, 0, 1, s) == 2       # ldc*4 % 16
+    assert g.gemm_bf16(64, 64, 64, p, 64, p, 64, C.data_ptr(), 64, 1, 1, 0, 1, s) == 3       # A column-major
+    assert g.gemm_bf16(64, 64, 64, p, 64, p, 64, C.data_ptr(), 64, 0, 0, 0, 1, s) == 3       # B row-major
+    assert g.gemm_bf16(64, 64, 64, p, 32, p, 64, C.data_ptr(), 64, 0, 1, 0, 1, s) == 1       # lda < K
+    assert g.gemm_bf16(-1, 64, 64, p, 64, p, 64, C.data_ptr(), 64, 0, 1, 0, 1, s) == 1
+
+
+def test_plan_on_device_matches_closed_forms():
+    from oracle import plan_forms as pf
+    g = _lib()
+    dev = g.gemm_device_desc_query(0)
+    kern = g.gemm_kernel_desc()
+    assert kern.regs_per_thread > 0
+    st, plan = g.gemm_plan(4096, 4096, 4096)
+    assert st == 0
+    S = dev.num_sms
+    b, _ = pf.ctas_per_sm(regs_per_thread=kern.regs_per_thread, threads=kern.threads_per_cta,
+                          smem_per_cta=kern.smem_per_cta, regs_per_sm=dev.regs_per_sm,
+                          smem_per_sm=dev.smem_per_sm, smem_reserved_per_cta=dev.smem_reserved_per_cta,
+                          max_threads_per_sm=dev.max_threads_per_sm, max_ctas_per_sm=dev.max_ctas_per_sm)
+    assert plan.ctas_per_sm == b == 1 and plan.num_sms == S
+    assert plan.grid == pf.grid(4096, 4096, 128, 256)
+    assert math.isclose(plan.eta_wave, float(pf.eta_wave(plan.grid, S, b)), rel_tol=1e-15)
+
+
+# ---- the full-size workloads, on sampled entries ---------------------------------------
+
+def sampled_check(oracle, A, Bt, M, N, K, C, out, n_random=6000, seed=0):
+    rows, cols = sample_entries(M, N, n_random, seed)
+    ref, sabs = oracle.gemm_entries(A, Bt, M, N, K, rows, cols)
+    got = C[rows, cols]
+    if out == "f32":
+        nbad, worst = check_f32(got, ref, sabs)
+        assert nbad == 0, f"{nbad} sampled fp32 entries outside the bound (worst {worst:.3g})"
+    else:
+        nbad, _, ncanc, detail = check_bf16(got, ref, sabs, oracle)
+        assert nbad == 0, f"{nbad} sampled bf16 entries outside the tolerance; {detail}"
+        assert ncanc <= max(8, got.size // 1000), f"{ncanc} entries needed the cancellation clause"
+
+
+def test_square4096_bf16_sampled(oracle_lib):
+    M = N = K = 4096
+    A, Bt = operands(M, N, K, "normal", True, SEED + 10)
+    C = run_gpu(A, Bt, M, N, K, torch.bfloat16)
+    sampled_check(oracle_lib, A, Bt, M, N, K, C, "bf16")
+
+
+@pytest.mark.parametrize("shape", [(4095, 4096, 4096), (4097, 4096, 4096), (4096, 4096, 4088),
+                                   (4096, 4104, 4096), (3968, 4096, 4096)])
+def test_neighbour_shapes_bf16_sampled(oracle_lib, shape):
+    M, N, K = shape
+    A, Bt = operands(M, N, K, "normal", True, SEED + 11)
+    C = run_gpu(A, Bt, M, N, K, torch.bfloat16)
+    sampled_check(oracle_lib, A, Bt, M, N, K, C, "bf16")
+
+
+def test_splitk_128x256x65536_all_splits(oracle_lib):
+    """Every split of the split-K workload against the full oracle; each split
+    is deterministic run to run."""
+    M, N, K = 128, 256, 65536
+    A, Bt = operands(M, N, K, "uniform", True, SEED + 12)
+    ref, sabs = oracle_lib.gemm(A, Bt, M, N, K)
+    g = _lib()
+    dA, dBt = to_dev(A), to_dev(Bt)
+    for split in (1, 8, 32, 74, 148):
+        C1 = g.matmul(dA, dBt.t(), out_dtype=torch.float32, split_k=split).cpu().numpy()
+        C2 = g.matmul(dA, dBt.t(), out_dtype=torch.float32, split_k=split).cpu().numpy()
+        assert np.array_equal(C1, C2), f"split {split} not deterministic"
+        nbad, worst = check_f32(C1, ref, sabs)
+        assert nbad == 0, f"split {split}: {nbad} entries outside the bound (worst {worst:.3g})"
+    # the integer variant is exact for every split
+    Ai, Bti = operands(M, N, 4096, "int4", False, SEED + 13)
+    refi, _ = oracle_lib.gemm(Ai, Bti, M, N, 4096)
+    dAi, dBti = to_dev(Ai), to_dev(Bti)
+    for split in (1, 8, 32, 64):
+        Ci = g.matmul(dAi, dBti.t(), out_dtype=torch.float32, split_k=split).cpu().numpy()
+        assert np.array_equal(Ci.astype(np.float64), refi), f"split {split} not exact on integers"
+
+
+def test_large_16384x8192x8192_persistent_and_one_cta_per_tile(oracle_lib):
+    M, N, K = 16384, 8192, 8192
+    A, Bt = operands(M, N, K, "normal", True, SEED + 14)
+    g = _lib()
+    dA, dBt = to_dev(A), to_dev(Bt)
+    C1 = g.matmul(dA, dBt.t(), out_dtype=torch.bfloat16)
+    C2 = g.matmul(dA, dBt.t(), out_dtype=torch.bfloat16, non_persistent=True)
+    assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))
+    del dA, dBt, C2
+    sampled_check(oracle_lib, A, Bt, M, N, K, from_dev_bf16(C1), "bf16", n_random=4000)
