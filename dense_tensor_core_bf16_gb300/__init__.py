@@ -25,6 +25,7 @@ __all__ = [
     "gemm_bf16", "gemm_bf16_ex", "gemm_plan", "gemm_plan_for_device", "gemm_occupancy",
     "gemm_device_desc_query", "gemm_kernel_desc", "gemm_reserve_workspace", "gemm_release_workspace",
     "gemm_get_device_status", "gemm_status_string", "gemm_limiter_string", "matmul", "lib", "header_functions",
+    "gemm_bf16_splitk_noalloc", "GEMM_NOALLOC_SCRATCH_FLOATS",
 ]
 
 GEMM_ROW_MAJOR, GEMM_COL_MAJOR = 0, 1
@@ -99,6 +100,8 @@ def lib() -> ctypes.CDLL:
         L.gemm_plan.argtypes = [i64, i64, i64, i32, i32, i32, i32, P(gemm_plan_t)]
         L.gemm_bf16.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, i32, i32, i32, vp]
         L.gemm_bf16_ex.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, i32, i32, P(gemm_options_t), vp]
+        L.gemm_bf16_splitk_noalloc.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, i32, i32, i32, vp]
+        L.gemm_bf16_splitk_noalloc.restype = i32
         L.gemm_reserve_workspace.argtypes = [ctypes.c_size_t]
         L.gemm_release_workspace.argtypes = []
         L.gemm_release_workspace.restype = None
@@ -172,6 +175,19 @@ def gemm_bf16_ex(M, N, K, A, lda, B, ldb, C, ldc, layout_a, layout_b, out_dtype,
                  opts: gemm_options_t | None, stream) -> int:
     return lib().gemm_bf16_ex(M, N, K, A, lda, B, ldb, C, ldc, layout_a, layout_b, out_dtype,
                               ctypes.byref(opts) if opts is not None else None, stream)
+
+
+# Capacity of the fixed split-K scratch of gemm_bf16_splitk_noalloc, in floats
+# (GEMM_NOALLOC_SCRATCH_FLOATS in the header: 16 MiB of fp32).
+GEMM_NOALLOC_SCRATCH_FLOATS = 16 * 1024 * 1024 // 4
+
+
+def gemm_bf16_splitk_noalloc(M, N, K, A, lda, B, ldb, C, ldc, layout_a, layout_b, out_dtype, split_k, stream) -> int:
+    """Status code of the C call: gemm_bf16 for callers that must not allocate
+    device memory; split-K partials go to a fixed 16 MiB array in the library
+    (split * M * round_up(N, 4) must fit in it)."""
+    return lib().gemm_bf16_splitk_noalloc(M, N, K, A, lda, B, ldb, C, ldc, layout_a, layout_b, out_dtype,
+                                          split_k, stream)
 
 
 def gemm_reserve_workspace(nbytes: int) -> int:

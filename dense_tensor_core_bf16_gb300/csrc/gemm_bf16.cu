@@ -704,3 +704,142 @@ gemm_status_t gemm_get_device_status(void *stream, unsigned int *where) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------- split-K without device allocation
+//
+// gemm_bf16_splitk_noalloc (contract in gemm_bf16.h): the same kernels as
+// gemm_bf16, with the split-K partial sums in a fixed array compiled into the
+// library instead of the cudaMalloc'd workspace.
+
+namespace gemm {
+
+// Host code must not use this name as a device address: on the host it is only
+// a stand-in.  The device address comes from cudaGetSymbolAddress, per device.
+static __device__ __align__(256) float g_noalloc_scratch[GEMM_NOALLOC_SCRATCH_FLOATS];
+
+namespace {
+
+std::mutex g_noalloc_mutex;
+float *g_noalloc_scratch_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on `device` (which must be current),
+// looked up once per device.
+gemm_status_t noalloc_scratch(int device, float **out) {
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_scratch_addr[device]) {
+        void *addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+        g_noalloc_scratch_addr[device] = static_cast<float *>(addr);
+    }
+    *out = g_noalloc_scratch_addr[device];
+    return GEMM_OK;
+}
+
+}  // namespace
+}  // namespace gemm
+
+extern "C" gemm_status_t gemm_bf16_splitk_noalloc(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
+                                                  const void *B, int64_t ldb, void *C, int64_t ldc,
+                                                  gemm_layout_t layout_a, gemm_layout_t layout_b,
+                                                  gemm_dtype_t out_dtype, int split_k, void *stream) {
+    gemm_status_t st = check_problem(M, N, K, layout_a, layout_b, out_dtype, split_k);
+    if (st != GEMM_OK) return st;
+    if (M == 0 || N == 0) return GEMM_OK;
+    const int esize = out_dtype == GEMM_OUT_BF16 ? 2 : 4;
+    if (!C || ldc < N) return GEMM_ERR_INVALID_VALUE;
+    if (reinterpret_cast<uintptr_t>(C) % 16 != 0 || (ldc * esize) % 16 != 0) return GEMM_ERR_MISALIGNED;
+    if (K > 0) {
+        if (!A || !B || lda < K || ldb < K) return GEMM_ERR_INVALID_VALUE;
+        if (reinterpret_cast<uintptr_t>(A) % 16 != 0 || reinterpret_cast<uintptr_t>(B) % 16 != 0 || lda % 8 != 0 ||
+            ldb % 8 != 0)
+            return GEMM_ERR_MISALIGNED;
+    }
+
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_NO_DEVICE;
+    }
+    DeviceState *ds = nullptr;
+    st = device_state(device, &ds);
+    if (st != GEMM_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    if (K == 0) return launch_fill_zero(M, N, C, ldc, esize, ds->desc.num_sms, s);
+
+    gemm_plan_t plan;
+    st = make_plan(M, N, K, layout_a, layout_b, out_dtype, split_k, 1, ds->desc, main_kernel_desc(ds->regs_per_thread),
+                   &plan);
+    if (st != GEMM_OK) return st;
+    const int64_t ldp = (N + 3) / 4 * 4;
+    float *scratch = nullptr;
+    if (plan.split_k > 1) {
+        const int64_t per_split = M * ldp;   // < 2^62: M, N < 2^31
+        if (per_split > static_cast<int64_t>(GEMM_NOALLOC_SCRATCH_FLOATS) ||
+            plan.split_k > static_cast<int64_t>(GEMM_NOALLOC_SCRATCH_FLOATS) / per_split)
+            return GEMM_ERR_INVALID_VALUE;
+        st = noalloc_scratch(device, &scratch);
+        if (st != GEMM_OK) return st;
+    }
+
+    CUtensorMap tmap_a, tmap_b;
+    st = encode_operand(&tmap_a, A, K, M, lda, TILE_M);
+    if (st != GEMM_OK) return st;
+    st = encode_operand(&tmap_b, B, K, N, ldb, TILE_N);
+    if (st != GEMM_OK) return st;
+
+    KernelParams p{};
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.tiles_m = static_cast<int>((M + TILE_M - 1) / TILE_M);
+    p.tiles_n = static_cast<int>((N + TILE_N - 1) / TILE_N);
+    p.k_tiles = plan.k_tiles;
+    p.split_k = plan.split_k;
+    p.group_m = DEFAULT_RASTER_GROUP_M;
+    p.num_units = plan.grid;
+    if (plan.split_k > 1) {
+        p.out = scratch;
+        p.ld_out = ldp;
+        p.split_stride = M * ldp;
+        p.out_bf16 = 0;
+    } else {
+        p.out = C;
+        p.ld_out = ldc;
+        p.split_stride = 0;
+        p.out_bf16 = out_dtype == GEMM_OUT_BF16 ? 1 : 0;
+    }
+    p.timeout_ns = static_cast<unsigned long long>(DEFAULT_TIMEOUT_MS) * 1000000ull;
+    p.skip_load = 0;
+
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(plan.launch_ctas));
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = s;
+    if (cudaLaunchKernelEx(&cfg, gemm_bf16_tcgen05_kernel, tmap_a, tmap_b, p) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    if (plan.split_k > 1) {
+        const long long total = M * ((N + 3) / 4);
+        long long blocks = (total + 255) / 256;
+        const long long cap = 4LL * ds->desc.num_sms;
+        if (blocks > cap) blocks = cap;
+        cudaLaunchConfig_t cc{};
+        cc.gridDim = dim3(static_cast<unsigned>(blocks));
+        cc.blockDim = dim3(256);
+        cc.stream = s;
+        if (cudaLaunchKernelEx(&cc, splitk_combine_kernel, static_cast<const float *>(scratch),
+                               static_cast<long long>(ldp), static_cast<long long>(M * ldp), plan.split_k,
+                               static_cast<int>(M), static_cast<int>(N), C, static_cast<long long>(ldc),
+                               out_dtype == GEMM_OUT_BF16 ? 1 : 0) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+    }
+    return GEMM_OK;
+}

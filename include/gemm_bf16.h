@@ -193,6 +193,46 @@ gemm_status_t gemm_bf16(int64_t M, int64_t N, int64_t K,
                         gemm_layout_t layout_a, gemm_layout_t layout_b,
                         gemm_dtype_t out_dtype, int split_k, void *stream);
 
+/*
+ * gemm_bf16_splitk_noalloc -- gemm_bf16 for callers that must not allocate
+ * device memory.  The pages have no counterpart to this entry point; it is
+ * the library's own.
+ *
+ * Who needs it: gemm_bf16 grows its split-K workspace with cudaMalloc the
+ * first time a large enough split is asked for.  Some callers cannot allow
+ * that -- a process whose device memory is handed out entirely by its own
+ * pool allocator (a raw cudaMalloc would fail, or carve memory out from under
+ * the pool), a long-running service that keeps a fixed memory footprint and
+ * must never meet an out-of-memory error in the middle of its work, or a
+ * latency-critical loop that cannot absorb cudaMalloc's implicit
+ * synchronisation of the whole device.  This entry point keeps the fp32
+ * partial sums in a fixed array compiled into the library instead
+ * (GEMM_NOALLOC_SCRATCH_BYTES = 16 MiB), which every GPU that loads the
+ * library holds until the process exits.  It calls no cudaMalloc, cudaFree
+ * or other allocating routine.
+ *
+ * Arguments, layouts, alignment rules and results are those of gemm_bf16.
+ * The split actually used (split_k, or the plan's choice when split_k is 0)
+ * must satisfy  split * M * round_up(N, 4) <= GEMM_NOALLOC_SCRATCH_FLOATS;
+ * otherwise the call returns GEMM_ERR_INVALID_VALUE and launches nothing.
+ * split_k = 1 uses no scratch at all.
+ *
+ * The first call on a device looks up the array's address on that device
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Every call shares the one array, and the array keeps whatever the last
+ * call left in it.  Nothing needs clearing: each partial sum a call reads was
+ * written earlier by the same call.  Calls whose work can overlap on the GPU
+ * (other streams, other host threads) race on the array and must be
+ * serialised by the caller.
+ */
+#define GEMM_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+#define GEMM_NOALLOC_SCRATCH_FLOATS (GEMM_NOALLOC_SCRATCH_BYTES / 4u)
+gemm_status_t gemm_bf16_splitk_noalloc(int64_t M, int64_t N, int64_t K,
+                                       const void *A, int64_t lda, const void *B, int64_t ldb,
+                                       void *C, int64_t ldc,
+                                       gemm_layout_t layout_a, gemm_layout_t layout_b,
+                                       gemm_dtype_t out_dtype, int split_k, void *stream);
+
 /* gemm_bf16 with options (launch mode, raster group, timing event, device
  * time limit).  opts == NULL behaves as gemm_bf16 with split_k = 0. */
 gemm_status_t gemm_bf16_ex(int64_t M, int64_t N, int64_t K,
