@@ -70,7 +70,7 @@ for _s in (1, 8, 32, 74, 148):
                                     desc=f"gemm_bf16 128x256x65536, bf16 row x col -> fp32, uniform[-1,1]/sqrt(K), "
                                          f"split_k={_s}")
 
-KERNEL_NAME = "gemm_bf16_tcgen05_kernel"
+KERNEL_NAME = "gemm_bf16_kernel"
 
 
 def log(*a):
@@ -220,7 +220,7 @@ def run_gpu(args, wname: str, w: dict, cpu_baseline: bool):
     (A_h, Bt_h), seed = make_host_operands(w)
 
     st, plan = g.gemm_plan(M, N, K, g.GEMM_ROW_MAJOR, g.GEMM_COL_MAJOR,
-                           g.GEMM_OUT_BF16 if w["out"] == "bf16" else g.GEMM_OUT_F32, w["split_k"])
+                           g.GEMM_OUT_BF16 if w["out"] == "bf16" else g.GEMM_OUT_F32, w["split_k"], args.variant)
     if st:
         raise g.GemmError(st, "gemm_plan")
     if plan.workspace_bytes:
@@ -242,7 +242,7 @@ def run_gpu(args, wname: str, w: dict, cpu_baseline: bool):
         b = B0 if i == 0 else B0.clone()
         c = torch.empty((M, N), dtype=out_dtype, device="cuda")
         sets.append((a, b.t(), c))
-    kw = dict(split_k=w["split_k"], non_persistent=w.get("non_persistent", False))
+    kw = dict(split_k=w["split_k"], non_persistent=w.get("non_persistent", False), kernel_variant=args.variant)
     launches_per_step = 1 + (1 if plan.split_k > 1 else 0)
 
     def step(i, **extra):
@@ -309,9 +309,11 @@ def run_gpu(args, wname: str, w: dict, cpu_baseline: bool):
         "data": f"synthetic (seeded SplitMix64, {w['dist']}{'/sqrt(K)' if w['scaled'] else ''}, seed {seed})",
         "config": {
             "workload": w["desc"], "M": M, "N": N, "K": K, "out": w["out"],
+            "kernel_variant": g.KERNEL_VARIANTS[plan.kernel_variant], "cluster_size": plan.cluster_size,
             "tile": f"{plan.tile_m}x{plan.tile_n}x{plan.tile_k}", "stages": plan.stages,
             "split_k": plan.split_k, "persistent": bool(plan.persistent), "grid_G": plan.grid,
-            "launch_ctas": plan.launch_ctas, "num_sms": plan.num_sms, "ctas_per_sm": plan.ctas_per_sm,
+            "launch_ctas": plan.launch_ctas, "resident_ctas": plan.resident_ctas, "num_sms": plan.num_sms,
+            "ctas_per_sm": plan.ctas_per_sm,
             "occupancy_limiter": g.LIMITERS[plan.occupancy_limiter],
             "eta_wave": round(plan.eta_wave, 5), "eta_pad": round(plan.eta_pad, 5),
             "pct_of_peak": round(100.0 * value / world / peak, 2), "peak_tflops": peak, "peak_kind": peak_kind,
@@ -320,7 +322,8 @@ def run_gpu(args, wname: str, w: dict, cpu_baseline: bool):
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
         "roofline": {
-            "bound": "tensor", "kernel": KERNEL_NAME, "achieved": round(achieved, 3), "peak": peak,
+            "bound": "tensor", "kernel": f"{KERNEL_NAME}<{plan.cluster_size},{plan.tile_n}>",
+            "achieved": round(achieved, 3), "peak": peak,
             "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": recorded_traffic(wname),
             "algorithmic_flops_per_launch": flops, "mean_launch_ms": round(mean_main_ms, 6),
             "peak_source": peak_kind,
@@ -438,6 +441,8 @@ def main(argv=None):
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="square4096")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--variant", type=int, default=0, choices=[0, 1, 2, 3],
+                    help="kernel variant: 0 auto, 1 one-SM 128x256, 2 two-SM 256x256, 3 two-SM 256x128")
     ap.add_argument("--all-workloads", action="store_true",
                     help="run every workload (one JSON line each, no CPU baseline)")
     args = ap.parse_args(argv)

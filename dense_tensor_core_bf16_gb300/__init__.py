@@ -30,6 +30,8 @@ __all__ = [
 
 GEMM_ROW_MAJOR, GEMM_COL_MAJOR = 0, 1
 GEMM_OUT_F32, GEMM_OUT_BF16 = 0, 1
+GEMM_KERNEL_AUTO, GEMM_KERNEL_1SM_128x256, GEMM_KERNEL_2SM_256x256, GEMM_KERNEL_2SM_256x128 = 0, 1, 2, 3
+KERNEL_VARIANTS = {1: "1sm_128x256", 2: "2sm_256x256", 3: "2sm_256x128"}
 STATUS_NAMES = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_VALUE", 2: "GEMM_ERR_MISALIGNED", 3: "GEMM_ERR_NOT_SUPPORTED",
                 4: "GEMM_ERR_NO_DEVICE", 5: "GEMM_ERR_OUT_OF_MEMORY", 6: "GEMM_ERR_LAUNCH",
                 7: "GEMM_ERR_DEVICE_TIMEOUT"}
@@ -53,7 +55,8 @@ class gemm_device_desc_t(ctypes.Structure):
 
 
 class gemm_kernel_desc_t(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_int) for n in ("regs_per_thread", "threads_per_cta", "smem_per_cta", "tmem_cols_per_cta")]
+    _fields_ = [(n, ctypes.c_int) for n in ("regs_per_thread", "threads_per_cta", "smem_per_cta", "tmem_cols_per_cta",
+                                             "cluster_size", "max_active_clusters")]
 
 
 class gemm_plan_t(ctypes.Structure):
@@ -62,7 +65,8 @@ class gemm_plan_t(ctypes.Structure):
         "num_sms", "ctas_per_sm", "occupancy_limiter", "persistent")] + \
         [(n, ctypes.c_int64) for n in ("tiles", "grid", "launch_ctas", "m_padded", "n_padded", "k_padded")] + \
         [(n, ctypes.c_double) for n in ("eta_wave", "eta_pad", "flops")] + \
-        [("smem_bytes", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64), ("tmem_cols", ctypes.c_int)]
+        [("smem_bytes", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64), ("tmem_cols", ctypes.c_int),
+         ("kernel_variant", ctypes.c_int), ("cluster_size", ctypes.c_int), ("resident_ctas", ctypes.c_int64)]
 
     def as_dict(self) -> dict:
         d = {n: getattr(self, n) for n, _ in self._fields_}
@@ -73,7 +77,7 @@ class gemm_plan_t(ctypes.Structure):
 class gemm_options_t(ctypes.Structure):
     _fields_ = [("split_k", ctypes.c_int), ("non_persistent", ctypes.c_int), ("raster_group_m", ctypes.c_int),
                 ("mainloop_done_event", ctypes.c_void_p), ("timeout_ms", ctypes.c_int),
-                ("debug_skip_load", ctypes.c_int)]
+                ("debug_skip_load", ctypes.c_int), ("kernel_variant", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -93,11 +97,11 @@ def lib() -> ctypes.CDLL:
         L = ctypes.CDLL(_build.LIB_PATH)
         i64, i32, vp, P = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.POINTER
         L.gemm_device_desc_query.argtypes = [i32, P(gemm_device_desc_t)]
-        L.gemm_kernel_desc.argtypes = [P(gemm_kernel_desc_t)]
+        L.gemm_kernel_desc.argtypes = [i32, P(gemm_kernel_desc_t)]
         L.gemm_occupancy.argtypes = [P(gemm_kernel_desc_t), P(gemm_device_desc_t), P(i32), P(i32)]
-        L.gemm_plan_for_device.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32, P(gemm_device_desc_t),
+        L.gemm_plan_for_device.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32, i32, P(gemm_device_desc_t),
                                            P(gemm_kernel_desc_t), P(gemm_plan_t)]
-        L.gemm_plan.argtypes = [i64, i64, i64, i32, i32, i32, i32, P(gemm_plan_t)]
+        L.gemm_plan.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32, P(gemm_plan_t)]
         L.gemm_bf16.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, i32, i32, i32, vp]
         L.gemm_bf16_ex.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, i32, i32, P(gemm_options_t), vp]
         L.gemm_bf16_splitk_noalloc.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, i32, i32, i32, vp]
@@ -135,9 +139,9 @@ def gemm_device_desc_query(device: int = 0) -> gemm_device_desc_t:
     return d
 
 
-def gemm_kernel_desc() -> gemm_kernel_desc_t:
+def gemm_kernel_desc(kernel_variant: int = 0) -> gemm_kernel_desc_t:
     k = gemm_kernel_desc_t()
-    st = lib().gemm_kernel_desc(ctypes.byref(k))
+    st = lib().gemm_kernel_desc(kernel_variant, ctypes.byref(k))
     if st:
         raise GemmError(st, "gemm_kernel_desc")
     return k
@@ -150,19 +154,20 @@ def gemm_occupancy(kern: gemm_kernel_desc_t, dev: gemm_device_desc_t):
     return st, b.value, LIMITERS.get(lim.value, "unknown")
 
 
-def gemm_plan_for_device(M, N, K, layout_a, layout_b, out_dtype, split_k, persistent,
+def gemm_plan_for_device(M, N, K, layout_a, layout_b, out_dtype, split_k, persistent, kernel_variant,
                          dev: gemm_device_desc_t, kern: gemm_kernel_desc_t):
     """(status, gemm_plan_t)."""
     plan = gemm_plan_t()
-    st = lib().gemm_plan_for_device(M, N, K, layout_a, layout_b, out_dtype, split_k, persistent,
+    st = lib().gemm_plan_for_device(M, N, K, layout_a, layout_b, out_dtype, split_k, persistent, kernel_variant,
                                     ctypes.byref(dev), ctypes.byref(kern), ctypes.byref(plan))
     return st, plan
 
 
-def gemm_plan(M, N, K, layout_a=GEMM_ROW_MAJOR, layout_b=GEMM_COL_MAJOR, out_dtype=GEMM_OUT_BF16, split_k=0):
+def gemm_plan(M, N, K, layout_a=GEMM_ROW_MAJOR, layout_b=GEMM_COL_MAJOR, out_dtype=GEMM_OUT_BF16, split_k=0,
+              kernel_variant=0):
     """(status, gemm_plan_t) on the current CUDA device."""
     plan = gemm_plan_t()
-    st = lib().gemm_plan(M, N, K, layout_a, layout_b, out_dtype, split_k, ctypes.byref(plan))
+    st = lib().gemm_plan(M, N, K, layout_a, layout_b, out_dtype, split_k, kernel_variant, ctypes.byref(plan))
     return st, plan
 
 
@@ -228,7 +233,7 @@ def _stream_handle(stream):
 
 def matmul(A, B, *, out_dtype=None, out=None, split_k: int = 0, non_persistent: bool = False,
            raster_group_m: int = 0, stream=None, mainloop_done_event=None, timeout_ms: int = 0,
-           debug_skip_load: int = 0):
+           debug_skip_load: int = 0, kernel_variant: int = 0):
     """C = A @ B through ``gemm_bf16_ex``.
 
     ``A``: (M, K) torch.bfloat16 CUDA tensor, row-major (stride (lda, 1)).
@@ -266,7 +271,7 @@ def matmul(A, B, *, out_dtype=None, out=None, split_k: int = 0, non_persistent: 
     opts = gemm_options_t(split_k=split_k, non_persistent=int(non_persistent), raster_group_m=raster_group_m,
                           mainloop_done_event=(mainloop_done_event.cuda_event if mainloop_done_event is not None
                                                else None),
-                          timeout_ms=timeout_ms, debug_skip_load=debug_skip_load)
+                          timeout_ms=timeout_ms, debug_skip_load=debug_skip_load, kernel_variant=kernel_variant)
     st = gemm_bf16_ex(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc,
                       GEMM_ROW_MAJOR, GEMM_COL_MAJOR, odt, opts, _stream_handle(stream))
     if st:

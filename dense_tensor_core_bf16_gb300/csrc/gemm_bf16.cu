@@ -55,22 +55,20 @@ struct KernelParams {
     int skip_load;               // test hook (0 = off)
 };
 
-// Barrier indices in shared memory.
-constexpr int BAR_FULL = 0;                          // [STAGES] operands landed
-constexpr int BAR_EMPTY = STAGES;                    // [STAGES] slot free again
-constexpr int BAR_ACC_FULL = 2 * STAGES;             // [ACC_BUFS] accumulator complete
-constexpr int BAR_ACC_EMPTY = 2 * STAGES + ACC_BUFS; // [ACC_BUFS] accumulator drained
-constexpr int BAR_DRAIN = 2 * STAGES + 2 * ACC_BUFS; // all MMAs of this CTA done
-
 // Wait for the phase of `bar` with parity `parity`.  Gives up after
 // `timeout_ns` (recording `site` in the fault word and raising the CTA's abort
 // flag), or -- when `honor_abort` -- as soon as another role has given up.
+// CLUSTER_SCOPE: acquire at cluster scope (barriers the peer CTA signals).
+template <bool CLUSTER_SCOPE>
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                            unsigned long long timeout_ns, unsigned site, bool honor_abort) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    auto try_wait = [&]() {
+        return CLUSTER_SCOPE ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
+    };
+    if (try_wait()) return true;
     const uint64_t t0 = ptx::globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (try_wait()) return true;
         if ((i & 31u) == 0) {
             if (honor_abort && *abort_flag) return false;
             if (ptx::globaltimer_ns() - t0 > timeout_ns) {
@@ -90,7 +88,7 @@ struct Unit {
 };
 
 // Work unit u -> tile and K slice.  Tiles are visited in groups of group_m
-// tile-rows, column by column inside a group, so that the CTAs resident at
+// tile-rows, column by column inside a group, so that the tiles in flight at
 // one time share A rows and B columns in L2.  Slices split the k-tiles as
 // evenly as possible: the first (k_tiles mod split_k) slices get one more.
 __device__ __forceinline__ Unit decode_unit(long long u, const KernelParams &p) {
@@ -153,16 +151,40 @@ __device__ __forceinline__ void store_row_chunk(const KernelParams &p, const Uni
     }
 }
 
+// The GEMM kernel, one instantiation per variant (see kernel_config.h).
+//   CG = 1: one CTA per 128 x BN tile.
+//   CG = 2: a cluster of two CTAs per 256 x BN tile.  Both CTAs' producers
+//     load their own A rows and half of B into their own rings and complete
+//     on the leader's (rank 0) full barriers; the leader's MMA thread issues
+//     cta_group::2 MMAs that read both CTAs' shared memory and write both
+//     CTAs' tensor memory, and its commits arrive on the barriers of both
+//     CTAs; each CTA's epilogue drains its own 128 rows and tells the leader
+//     when its half of an accumulator is free.
+template <int CG, int BN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    gemm_bf16_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                             const KernelParams p) {
+    gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                     const KernelParams p) {
+    constexpr VariantInfo V = make_variant(CG, BN);
+    constexpr int STAGES = V.stages;
+    constexpr int BAR_FULL = 0;                           // [STAGES] operands landed (leader's count both CTAs)
+    constexpr int BAR_EMPTY = STAGES;                     // [STAGES] slot free again
+    constexpr int BAR_ACC_FULL = 2 * STAGES;              // [ACC_BUFS] accumulator complete
+    constexpr int BAR_ACC_EMPTY = 2 * STAGES + ACC_BUFS;  // [ACC_BUFS] accumulator drained (leader's)
+    constexpr int BAR_DRAIN = 2 * STAGES + 2 * ACC_BUFS;  // all MMAs of this CTA done
+    constexpr int NUM_BARRIERS = 2 * STAGES + 2 * ACC_BUFS + 1;
+    constexpr uint32_t IDESC = ptx::idesc_bf16_f32(CTA_ROWS * CG, BN);
+    constexpr uint32_t TX_BYTES = CG * V.stage;           // bytes both CTAs land per stage
+    constexpr bool PAIR = CG == 2;
+
     extern __shared__ uint8_t smem_raw[];
-    // Operand tiles must start on the 1024-byte swizzle-atom boundary.
+    // Operand tiles must start on the 1024-byte swizzle-atom boundary.  The
+    // layout is identical in both CTAs of a pair: the pair MMA reads the peer's
+    // operands at the leader's offsets.
     const uint32_t raw_addr = ptx::smem_addr(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
     const uint32_t sA = ptx::smem_addr(smem);                      // STAGES A tiles
-    const uint32_t sB = sA + STAGES * A_STAGE_BYTES;               // STAGES B tiles
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+    const uint32_t sB = sA + STAGES * V.a_stage;                   // STAGES B tiles
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * V.stage);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NUM_BARRIERS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     const uint32_t bar0 = ptx::smem_addr(bars);
@@ -170,15 +192,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+    const long long first_unit = blockIdx.x / CG;
+    const long long unit_stride = gridDim.x / CG;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(bar(BAR_FULL + s), 1);    // producer's arrive + TMA bytes
+            ptx::mbar_init(bar(BAR_FULL + s), 1);    // leader's producer arrive + both CTAs' bytes
             ptx::mbar_init(bar(BAR_EMPTY + s), 1);   // MMA commit
         }
         for (int b = 0; b < ACC_BUFS; ++b) {
             ptx::mbar_init(bar(BAR_ACC_FULL + b), 1);              // MMA commit
-            ptx::mbar_init(bar(BAR_ACC_EMPTY + b), EPI_THREADS);   // every epilogue thread
+            ptx::mbar_init(bar(BAR_ACC_EMPTY + b), EPI_WARPS * CG); // one lane per epilogue warp of each CTA
         }
         ptx::mbar_init(bar(BAR_DRAIN), 1);
         *abort_flag = 0;
@@ -189,11 +215,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::prefetch_tensormap(&tmap_b);
     }
     if (warp == 1) {
-        ptx::tmem_alloc(ptx::smem_addr(tmem_slot), TMEM_COLS);
-        ptx::tmem_relinquish_alloc_permit();
+        if constexpr (PAIR) {
+            ptx::tmem_alloc_pair(ptx::smem_addr(tmem_slot), V.tmem_cols);
+            ptx::tmem_relinquish_alloc_permit_pair();
+        } else {
+            ptx::tmem_alloc(ptx::smem_addr(tmem_slot), V.tmem_cols);
+            ptx::tmem_relinquish_alloc_permit();
+        }
     }
     ptx::tc_fence_before_sync();
-    __syncthreads();
+    if constexpr (PAIR) {
+        ptx::cluster_sync();   // both CTAs' barriers initialised and TMEM allocated
+    } else {
+        __syncthreads();
+    }
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
 
@@ -202,12 +237,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) {
             uint32_t it = 0, issued = 0;
             bool ok = true;
-            for (long long u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+            for (long long u = first_unit; u < p.num_units && ok; u += unit_stride) {
                 const Unit w = decode_unit(u, p);
+                const int row_a = w.tm * V.tile_m + static_cast<int>(rank) * CTA_ROWS;
+                const int row_b = w.tn * BN + static_cast<int>(rank) * V.b_rows;
                 for (int kb = 0; kb < w.kb_count; ++kb, ++it) {
                     const uint32_t s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1u;
-                    if (!wait_phase(bar(BAR_EMPTY + s), ph ^ 1u, abort_flag, p.timeout_ns, SITE_PRODUCER, true)) {
+                    if (!wait_phase<PAIR>(bar(BAR_EMPTY + s), ph ^ 1u, abort_flag, p.timeout_ns, SITE_PRODUCER,
+                                          true)) {
                         ok = false;
                         break;
                     }
@@ -215,79 +253,109 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (p.skip_load != 0 && blockIdx.x == 0 && issued == static_cast<uint32_t>(p.skip_load)) {
                         continue;   // test hook: this slot is never filled
                     }
-                    ptx::mbar_arrive_expect_tx(bar(BAR_FULL + s), STAGE_BYTES);
+                    if (leader) ptx::mbar_arrive_expect_tx(bar(BAR_FULL + s), TX_BYTES);
                     const int kc = (w.kb_begin + kb) * TILE_K;
-                    ptx::tma_load_2d(sA + s * A_STAGE_BYTES, &tmap_a, bar(BAR_FULL + s), kc, w.tm * TILE_M);
-                    ptx::tma_load_2d(sB + s * B_STAGE_BYTES, &tmap_b, bar(BAR_FULL + s), kc, w.tn * TILE_N);
+                    if constexpr (PAIR) {
+                        const uint32_t full_leader = ptx::mapa_shared(bar(BAR_FULL + s), 0);
+                        ptx::tma_load_2d_pair(sA + s * V.a_stage, &tmap_a, full_leader, kc, row_a);
+                        ptx::tma_load_2d_pair(sB + s * V.b_stage, &tmap_b, full_leader, kc, row_b);
+                    } else {
+                        ptx::tma_load_2d(sA + s * V.a_stage, &tmap_a, bar(BAR_FULL + s), kc, row_a);
+                        ptx::tma_load_2d(sB + s * V.b_stage, &tmap_b, bar(BAR_FULL + s), kc, row_b);
+                    }
                 }
             }
-            // No copy may still be writing this CTA's shared memory when it
-            // exits: wait (bounded) for the last STAGES loads.  Earlier ones
-            // were consumed by the MMA warp before their slots were reused.
-            const uint32_t first = it > static_cast<uint32_t>(STAGES) ? it - STAGES : 0u;
-            for (uint32_t j = first; j < it; ++j) {
-                wait_phase(bar(BAR_FULL + j % STAGES), (j / STAGES) & 1u, abort_flag, p.timeout_ns, SITE_DRAIN, false);
+            // No copy may still be writing a CTA's shared memory when it exits:
+            // the leader waits (bounded) for the last STAGES stages, whose full
+            // barriers count both CTAs' bytes; the peer cannot pass the final
+            // cluster barrier before the leader does.  Earlier stages were
+            // consumed by the MMA thread before their slots were reused.
+            if (leader) {
+                const uint32_t first = it > static_cast<uint32_t>(STAGES) ? it - STAGES : 0u;
+                for (uint32_t j = first; j < it; ++j) {
+                    wait_phase<PAIR>(bar(BAR_FULL + j % STAGES), (j / STAGES) & 1u, abort_flag, p.timeout_ns,
+                                     SITE_DRAIN, false);
+                }
             }
         }
     } else if (warp == 1) {
-        // ---------------- MMA issuer: one thread drives the Tensor Core ------
-        if (lane == 0) {
-            constexpr uint32_t IDESC = ptx::idesc_bf16_f32(TILE_M, TILE_N);
+        // ---------------- MMA issuer: one thread of the leader CTA ------------
+        if (lane == 0 && leader) {
             uint32_t it = 0, tc = 0;
             bool ok = true;
-            for (long long u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++tc) {
+            for (long long u = first_unit; u < p.num_units && ok; u += unit_stride, ++tc) {
                 const Unit w = decode_unit(u, p);
                 const uint32_t buf = tc & 1u;
                 const uint32_t use = tc >> 1;
-                if (!wait_phase(bar(BAR_ACC_EMPTY + buf), (use & 1u) ^ 1u, abort_flag, p.timeout_ns, SITE_MMA_ACC,
-                                true)) {
+                if (!wait_phase<PAIR>(bar(BAR_ACC_EMPTY + buf), (use & 1u) ^ 1u, abort_flag, p.timeout_ns,
+                                      SITE_MMA_ACC, true)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + buf * TILE_N;
+                const uint32_t d_tmem = tmem_base + buf * BN;
                 for (int kb = 0; kb < w.kb_count; ++kb, ++it) {
                     const uint32_t s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1u;
-                    if (!wait_phase(bar(BAR_FULL + s), ph, abort_flag, p.timeout_ns, SITE_MMA_OPERANDS, true)) {
+                    if (!wait_phase<PAIR>(bar(BAR_FULL + s), ph, abort_flag, p.timeout_ns, SITE_MMA_OPERANDS, true)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after_sync();
-                    const uint64_t a_desc = ptx::smem_desc_kmajor_sw128(sA + s * A_STAGE_BYTES);
-                    const uint64_t b_desc = ptx::smem_desc_kmajor_sw128(sB + s * B_STAGE_BYTES);
+                    const uint64_t a_desc = ptx::smem_desc_kmajor_sw128(sA + s * V.a_stage);
+                    const uint64_t b_desc = ptx::smem_desc_kmajor_sw128(sB + s * V.b_stage);
 #pragma unroll
                     for (int k = 0; k < TILE_K / MMA_K; ++k) {
                         // next 16 elements of K: +32 bytes inside the swizzled
                         // 128-byte row, i.e. +2 in the address>>4 field
-                        ptx::mma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, IDESC, (kb | k) != 0 ? 1u : 0u);
+                        const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
+                        if constexpr (PAIR) {
+                            ptx::mma_bf16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, IDESC, acc);
+                        } else {
+                            ptx::mma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, IDESC, acc);
+                        }
                     }
-                    ptx::mma_commit(bar(BAR_EMPTY + s));   // slot reusable once these MMAs have read it
+                    // slot reusable (in every CTA) once these MMAs have read it
+                    if constexpr (PAIR) {
+                        ptx::mma_commit_pair_multicast(bar(BAR_EMPTY + s), 0x3);
+                    } else {
+                        ptx::mma_commit(bar(BAR_EMPTY + s));
+                    }
                 }
                 if (!ok) break;
-                ptx::mma_commit(bar(BAR_ACC_FULL + buf));  // accumulator complete
+                // accumulator complete (in every CTA)
+                if constexpr (PAIR) {
+                    ptx::mma_commit_pair_multicast(bar(BAR_ACC_FULL + buf), 0x3);
+                } else {
+                    ptx::mma_commit(bar(BAR_ACC_FULL + buf));
+                }
             }
             // Every MMA issued here must finish before TMEM is released.
-            ptx::mma_commit(bar(BAR_DRAIN));
-            wait_phase(bar(BAR_DRAIN), 0, abort_flag, p.timeout_ns, SITE_DRAIN, false);
+            if constexpr (PAIR) {
+                ptx::mma_commit_pair(bar(BAR_DRAIN));
+            } else {
+                ptx::mma_commit(bar(BAR_DRAIN));
+            }
+            wait_phase<PAIR>(bar(BAR_DRAIN), 0, abort_flag, p.timeout_ns, SITE_DRAIN, false);
         }
     } else {
         // ---------------- epilogue: TMEM -> registers -> global ---------------
         const int quarter = warp & 3;            // TMEM lanes this warp may read: 32*quarter ..
-        const int row_in_tile = quarter * 32 + lane;
+        const int row_in_cta = quarter * 32 + lane;
         uint32_t tc = 0;
-        for (long long u = blockIdx.x; u < p.num_units; u += gridDim.x, ++tc) {
+        for (long long u = first_unit; u < p.num_units; u += unit_stride, ++tc) {
             const Unit w = decode_unit(u, p);
             const uint32_t buf = tc & 1u;
             const uint32_t use = tc >> 1;
-            const bool ok = wait_phase(bar(BAR_ACC_FULL + buf), use & 1u, abort_flag, p.timeout_ns, SITE_EPI_ACC, true);
+            const bool ok =
+                wait_phase<PAIR>(bar(BAR_ACC_FULL + buf), use & 1u, abort_flag, p.timeout_ns, SITE_EPI_ACC, true);
             if (!__all_sync(0xffffffffu, ok)) break;
             ptx::tc_fence_after_sync();
-            const int row = w.tm * TILE_M + row_in_tile;
-            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * TILE_N;
-            const int col_base = w.tn * TILE_N;
+            const int row = w.tm * V.tile_m + static_cast<int>(rank) * CTA_ROWS + row_in_cta;
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * BN;
+            const int col_base = w.tn * BN;
 #pragma unroll 1
-            for (int c = 0; c < TILE_N / 32; ++c) {
+            for (int c = 0; c < BN / 32; ++c) {
                 const int col0 = col_base + c * 32;
                 if (col0 >= p.N) break;          // same for the whole warp
                 uint32_t r[32];
@@ -297,15 +365,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (row < p.M) store_row_chunk(p, w, row, col0, r);
             }
             ptx::tc_fence_before_sync();
-            ptx::mbar_arrive(bar(BAR_ACC_EMPTY + buf));
+            __syncwarp();
+            if (lane == 0) {
+                if constexpr (PAIR) {
+                    ptx::mbar_arrive_cluster(ptx::mapa_shared(bar(BAR_ACC_EMPTY + buf), 0));
+                } else {
+                    ptx::mbar_arrive(bar(BAR_ACC_EMPTY + buf));
+                }
+            }
         }
     }
 
-    __syncthreads();
+    __syncwarp();
+    ptx::tc_fence_before_sync();
+    if constexpr (PAIR) {
+        ptx::cluster_sync();   // no CTA leaves while its peer may still touch its memory
+    } else {
+        __syncthreads();
+    }
     if (warp == 1) {
         __syncwarp();
         ptx::tc_fence_after_sync();
-        ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+        if constexpr (PAIR) {
+            ptx::tmem_dealloc_pair(tmem_base, V.tmem_cols);
+        } else {
+            ptx::tmem_dealloc(tmem_base, V.tmem_cols);
+        }
     }
 }
 
@@ -375,10 +460,25 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
+using KernelFn = void (*)(CUtensorMap, CUtensorMap, KernelParams);
+
+KernelFn kernel_fn(int variant) {
+    switch (variant) {
+        case VARIANT_2SM_256x256: return gemm_bf16_kernel<2, 256>;
+        case VARIANT_2SM_256x128: return gemm_bf16_kernel<2, 128>;
+        default: return gemm_bf16_kernel<1, 256>;
+    }
+}
+
+struct VariantState {
+    int regs_per_thread = 0;
+    int max_active_clusters = 0;   // 0 for single-CTA variants
+};
+
 struct DeviceState {
     bool ready = false;
     gemm_device_desc_t desc{};
-    int regs_per_thread = 0;
+    VariantState var[VARIANT_COUNT];
     float *workspace = nullptr;
     size_t workspace_bytes = 0;
 };
@@ -407,6 +507,40 @@ gemm_status_t query_desc(int device, gemm_device_desc_t *d) {
     return GEMM_OK;
 }
 
+cudaLaunchAttribute cluster_attr(int cluster_size) {
+    cudaLaunchAttribute a{};
+    a.id = cudaLaunchAttributeClusterDimension;
+    a.val.clusterDim.x = static_cast<unsigned>(cluster_size);
+    a.val.clusterDim.y = 1;
+    a.val.clusterDim.z = 1;
+    return a;
+}
+
+gemm_status_t init_variant(int variant, int num_sms, VariantState &vs) {
+    const VariantInfo vi = variant_info(variant);
+    KernelFn fn = kernel_fn(variant);
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, vi.smem) != cudaSuccess)
+        return GEMM_ERR_LAUNCH;
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return GEMM_ERR_LAUNCH;
+    vs.regs_per_thread = fa.numRegs;
+    vs.max_active_clusters = 0;
+    if (vi.cta_group > 1) {
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(static_cast<unsigned>(num_sms / vi.cta_group * vi.cta_group));
+        cfg.blockDim = dim3(NUM_THREADS);
+        cfg.dynamicSmemBytes = vi.smem;
+        cudaLaunchAttribute attr = cluster_attr(vi.cta_group);
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void *>(fn), &cfg) != cudaSuccess || n <= 0)
+            return GEMM_ERR_LAUNCH;
+        vs.max_active_clusters = n;
+    }
+    return GEMM_OK;
+}
+
 // Per-device one-time set-up, under g_mutex.
 gemm_status_t device_state(int device, DeviceState **out) {
     if (device < 0 || device >= kMaxDevices) return GEMM_ERR_NO_DEVICE;
@@ -420,12 +554,13 @@ gemm_status_t device_state(int device, DeviceState **out) {
         if (major != 10 || minor != 3) return GEMM_ERR_NO_DEVICE;   // built for sm_103a only
         gemm_status_t st = query_desc(device, &ds.desc);
         if (st != GEMM_OK) return st;
-        if (cudaFuncSetAttribute(gemm_bf16_tcgen05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SMEM_BYTES) != cudaSuccess)
-            return GEMM_ERR_LAUNCH;
-        cudaFuncAttributes fa{};
-        if (cudaFuncGetAttributes(&fa, gemm_bf16_tcgen05_kernel) != cudaSuccess) return GEMM_ERR_LAUNCH;
-        ds.regs_per_thread = fa.numRegs;
+        for (int v = 1; v < VARIANT_COUNT; ++v) {
+            st = init_variant(v, ds.desc.num_sms, ds.var[v]);
+            if (st != GEMM_OK) {
+                cudaGetLastError();
+                return st;
+            }
+        }
         if (!g_encode_tiled) {
             void *fn = nullptr;
             cudaDriverEntryPointQueryResult qr{};
@@ -441,12 +576,15 @@ gemm_status_t device_state(int device, DeviceState **out) {
     return GEMM_OK;
 }
 
-gemm_kernel_desc_t main_kernel_desc(int regs_per_thread) {
+gemm_kernel_desc_t kernel_desc(int variant, const VariantState &vs) {
+    const VariantInfo vi = variant_info(variant);
     gemm_kernel_desc_t k{};
-    k.regs_per_thread = regs_per_thread;
+    k.regs_per_thread = vs.regs_per_thread;
     k.threads_per_cta = NUM_THREADS;
-    k.smem_per_cta = SMEM_BYTES;
-    k.tmem_cols_per_cta = TMEM_COLS;
+    k.smem_per_cta = vi.smem;
+    k.tmem_cols_per_cta = vi.tmem_cols;
+    k.cluster_size = vi.cta_group;
+    k.max_active_clusters = vs.max_active_clusters;
     return k;
 }
 
@@ -462,7 +600,7 @@ gemm_status_t encode_operand(CUtensorMap *map, const void *ptr, int64_t k, int64
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_LAUNCH;
 }
 
-gemm_status_t ensure_workspace(int device, DeviceState &ds, size_t bytes) {
+gemm_status_t ensure_workspace(DeviceState &ds, size_t bytes) {
     std::lock_guard<std::mutex> lock(g_mutex);
     if (ds.workspace_bytes >= bytes) return GEMM_OK;
     if (ds.workspace) {
@@ -471,7 +609,6 @@ gemm_status_t ensure_workspace(int device, DeviceState &ds, size_t bytes) {
         ds.workspace = nullptr;
         ds.workspace_bytes = 0;
     }
-    (void)device;
     void *p = nullptr;
     if (cudaMalloc(&p, bytes) != cudaSuccess) {
         cudaGetLastError();
@@ -497,59 +634,9 @@ gemm_status_t launch_fill_zero(int64_t M, int64_t N, void *C, int64_t ldc, int e
                : GEMM_ERR_LAUNCH;
 }
 
-}  // namespace
-
-}  // namespace gemm
-
-using namespace gemm;
-
-extern "C" {
-
-gemm_status_t gemm_device_desc_query(int device, gemm_device_desc_t *dev) {
-    if (!dev) return GEMM_ERR_INVALID_VALUE;
-    std::memset(dev, 0, sizeof *dev);
-    return query_desc(device, dev);
-}
-
-gemm_status_t gemm_kernel_desc(gemm_kernel_desc_t *kern) {
-    if (!kern) return GEMM_ERR_INVALID_VALUE;
-    int regs = 0;
-    int device = 0;
-    if (cudaGetDevice(&device) == cudaSuccess) {
-        DeviceState *ds = nullptr;
-        if (device_state(device, &ds) == GEMM_OK) regs = ds->regs_per_thread;
-    }
-    cudaGetLastError();
-    *kern = main_kernel_desc(regs);
-    return GEMM_OK;
-}
-
-gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, gemm_layout_t layout_a, gemm_layout_t layout_b,
-                        gemm_dtype_t out_dtype, int split_k, gemm_plan_t *plan) {
-    if (!plan) return GEMM_ERR_INVALID_VALUE;
-    gemm_status_t st = check_problem(M, N, K, layout_a, layout_b, out_dtype, split_k);
-    if (st != GEMM_OK) return st;
-    int device = 0;
-    if (cudaGetDevice(&device) != cudaSuccess) {
-        cudaGetLastError();
-        return GEMM_ERR_NO_DEVICE;
-    }
-    DeviceState *ds = nullptr;
-    st = device_state(device, &ds);
-    if (st != GEMM_OK) return st;
-    return make_plan(M, N, K, layout_a, layout_b, out_dtype, split_k, 1, ds->desc, main_kernel_desc(ds->regs_per_thread),
-                     plan);
-}
-
-gemm_status_t gemm_bf16_ex(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
-                           void *C, int64_t ldc, gemm_layout_t layout_a, gemm_layout_t layout_b,
-                           gemm_dtype_t out_dtype, const gemm_options_t *opts, void *stream) {
-    gemm_options_t o{};
-    if (opts) o = *opts;
-    gemm_status_t st = check_problem(M, N, K, layout_a, layout_b, out_dtype, o.split_k);
-    if (st != GEMM_OK) return st;
-    if (o.timeout_ms < 0 || o.raster_group_m < 0 || o.debug_skip_load < 0) return GEMM_ERR_INVALID_VALUE;
-    if (M == 0 || N == 0) return GEMM_OK;
+// Checks shared by every GEMM entry point; no CUDA calls.
+gemm_status_t check_operands(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
+                             const void *C, int64_t ldc, gemm_dtype_t out_dtype) {
     const int esize = out_dtype == GEMM_OUT_BF16 ? 2 : 4;
     if (!C || ldc < N) return GEMM_ERR_INVALID_VALUE;
     if (reinterpret_cast<uintptr_t>(C) % 16 != 0 || (ldc * esize) % 16 != 0) return GEMM_ERR_MISALIGNED;
@@ -559,47 +646,60 @@ gemm_status_t gemm_bf16_ex(int64_t M, int64_t N, int64_t K, const void *A, int64
             ldb % 8 != 0)
             return GEMM_ERR_MISALIGNED;
     }
+    return GEMM_OK;
+}
 
-    int device = 0;
-    if (cudaGetDevice(&device) != cudaSuccess) {
-        cudaGetLastError();
-        return GEMM_ERR_NO_DEVICE;
-    }
-    DeviceState *ds = nullptr;
-    st = device_state(device, &ds);
-    if (st != GEMM_OK) return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
+// Where the split-K partial sums of one call go.
+struct PartialBuffer {
+    bool fixed;          // true: the caller-provided array below, never grown
+    float *ptr;
+    int64_t floats;      // capacity when fixed
+};
 
-    if (K == 0) return launch_fill_zero(M, N, C, ldc, esize, ds->desc.num_sms, s);
-
+// Plan and enqueue one GEMM whose arguments have passed check_problem and
+// check_operands, with M, N, K > 0.
+gemm_status_t launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
+                          void *C, int64_t ldc, gemm_layout_t layout_a, gemm_layout_t layout_b,
+                          gemm_dtype_t out_dtype, const gemm_options_t &o, cudaStream_t s, DeviceState &ds,
+                          const PartialBuffer &pb) {
+    const int variant = resolve_variant(o.kernel_variant);
+    const VariantInfo vi = variant_info(variant);
     gemm_plan_t plan;
-    st = make_plan(M, N, K, layout_a, layout_b, out_dtype, o.split_k, o.non_persistent ? 0 : 1, ds->desc,
-                   main_kernel_desc(ds->regs_per_thread), &plan);
+    gemm_status_t st = make_plan(M, N, K, layout_a, layout_b, out_dtype, o.split_k, o.non_persistent ? 0 : 1, variant,
+                                 ds.desc, kernel_desc(variant, ds.var[variant]), &plan);
     if (st != GEMM_OK) return st;
     const int64_t ldp = (N + 3) / 4 * 4;
+    float *partials = nullptr;
     if (plan.split_k > 1) {
-        st = ensure_workspace(device, *ds, static_cast<size_t>(plan.workspace_bytes));
-        if (st != GEMM_OK) return st;
+        if (pb.fixed) {
+            const int64_t per_split = M * ldp;   // < 2^62: M, N < 2^31
+            if (per_split > pb.floats || plan.split_k > pb.floats / per_split) return GEMM_ERR_INVALID_VALUE;
+            partials = pb.ptr;
+        } else {
+            st = ensure_workspace(ds, static_cast<size_t>(plan.workspace_bytes));
+            if (st != GEMM_OK) return st;
+            partials = ds.workspace;
+        }
     }
 
     CUtensorMap tmap_a, tmap_b;
-    st = encode_operand(&tmap_a, A, K, M, lda, TILE_M);
+    st = encode_operand(&tmap_a, A, K, M, lda, CTA_ROWS);
     if (st != GEMM_OK) return st;
-    st = encode_operand(&tmap_b, B, K, N, ldb, TILE_N);
+    st = encode_operand(&tmap_b, B, K, N, ldb, vi.b_rows);
     if (st != GEMM_OK) return st;
 
     KernelParams p{};
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
-    p.tiles_m = static_cast<int>((M + TILE_M - 1) / TILE_M);
-    p.tiles_n = static_cast<int>((N + TILE_N - 1) / TILE_N);
+    p.tiles_m = static_cast<int>((M + vi.tile_m - 1) / vi.tile_m);
+    p.tiles_n = static_cast<int>((N + vi.bn - 1) / vi.bn);
     p.k_tiles = plan.k_tiles;
     p.split_k = plan.split_k;
     p.group_m = o.raster_group_m > 0 ? o.raster_group_m : DEFAULT_RASTER_GROUP_M;
-    p.num_units = plan.grid;
+    p.num_units = plan.tiles * plan.split_k;
     if (plan.split_k > 1) {
-        p.out = ds->workspace;
+        p.out = partials;
         p.ld_out = ldp;
         p.split_stride = M * ldp;
         p.out_bf16 = 0;
@@ -616,9 +716,14 @@ gemm_status_t gemm_bf16_ex(int64_t M, int64_t N, int64_t K, const void *A, int64
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(plan.launch_ctas));
     cfg.blockDim = dim3(NUM_THREADS);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.dynamicSmemBytes = vi.smem;
     cfg.stream = s;
-    if (cudaLaunchKernelEx(&cfg, gemm_bf16_tcgen05_kernel, tmap_a, tmap_b, p) != cudaSuccess) {
+    cudaLaunchAttribute attr = cluster_attr(vi.cta_group);
+    if (vi.cta_group > 1) {
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+    }
+    if (cudaLaunchKernelEx(&cfg, kernel_fn(variant), tmap_a, tmap_b, p) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
     }
@@ -627,13 +732,13 @@ gemm_status_t gemm_bf16_ex(int64_t M, int64_t N, int64_t K, const void *A, int64
     if (plan.split_k > 1) {
         const long long total = M * ((N + 3) / 4);
         long long blocks = (total + 255) / 256;
-        const long long cap = 4LL * ds->desc.num_sms;
+        const long long cap = 4LL * ds.desc.num_sms;
         if (blocks > cap) blocks = cap;
         cudaLaunchConfig_t cc{};
         cc.gridDim = dim3(static_cast<unsigned>(blocks));
         cc.blockDim = dim3(256);
         cc.stream = s;
-        if (cudaLaunchKernelEx(&cc, splitk_combine_kernel, static_cast<const float *>(ds->workspace),
+        if (cudaLaunchKernelEx(&cc, splitk_combine_kernel, static_cast<const float *>(partials),
                                static_cast<long long>(ldp), static_cast<long long>(M * ldp), plan.split_k,
                                static_cast<int>(M), static_cast<int>(N), C, static_cast<long long>(ldc),
                                out_dtype == GEMM_OUT_BF16 ? 1 : 0) != cudaSuccess) {
@@ -642,6 +747,78 @@ gemm_status_t gemm_bf16_ex(int64_t M, int64_t N, int64_t K, const void *A, int64
         }
     }
     return GEMM_OK;
+}
+
+gemm_status_t current_device(int *device, DeviceState **ds) {
+    if (cudaGetDevice(device) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_NO_DEVICE;
+    }
+    return device_state(*device, ds);
+}
+
+}  // namespace
+
+}  // namespace gemm
+
+using namespace gemm;
+
+extern "C" {
+
+gemm_status_t gemm_device_desc_query(int device, gemm_device_desc_t *dev) {
+    if (!dev) return GEMM_ERR_INVALID_VALUE;
+    std::memset(dev, 0, sizeof *dev);
+    return query_desc(device, dev);
+}
+
+gemm_status_t gemm_kernel_desc(int kernel_variant, gemm_kernel_desc_t *kern) {
+    if (!kern || kernel_variant < 0 || kernel_variant >= VARIANT_COUNT) return GEMM_ERR_INVALID_VALUE;
+    const int v = resolve_variant(kernel_variant);
+    VariantState vs;
+    int device = 0;
+    DeviceState *ds = nullptr;
+    if (current_device(&device, &ds) == GEMM_OK) vs = ds->var[v];
+    cudaGetLastError();
+    *kern = kernel_desc(v, vs);
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, gemm_layout_t layout_a, gemm_layout_t layout_b,
+                        gemm_dtype_t out_dtype, int split_k, int kernel_variant, gemm_plan_t *plan) {
+    if (!plan) return GEMM_ERR_INVALID_VALUE;
+    gemm_status_t st = check_problem(M, N, K, layout_a, layout_b, out_dtype, split_k);
+    if (st != GEMM_OK) return st;
+    if (kernel_variant < 0 || kernel_variant >= VARIANT_COUNT) return GEMM_ERR_INVALID_VALUE;
+    int device = 0;
+    DeviceState *ds = nullptr;
+    st = current_device(&device, &ds);
+    if (st != GEMM_OK) return st;
+    const int v = resolve_variant(kernel_variant);
+    return make_plan(M, N, K, layout_a, layout_b, out_dtype, split_k, 1, v, ds->desc, kernel_desc(v, ds->var[v]), plan);
+}
+
+gemm_status_t gemm_bf16_ex(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
+                           void *C, int64_t ldc, gemm_layout_t layout_a, gemm_layout_t layout_b,
+                           gemm_dtype_t out_dtype, const gemm_options_t *opts, void *stream) {
+    gemm_options_t o{};
+    if (opts) o = *opts;
+    gemm_status_t st = check_problem(M, N, K, layout_a, layout_b, out_dtype, o.split_k);
+    if (st != GEMM_OK) return st;
+    if (o.timeout_ms < 0 || o.raster_group_m < 0 || o.debug_skip_load < 0 || o.kernel_variant < 0 ||
+        o.kernel_variant >= VARIANT_COUNT)
+        return GEMM_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0) return GEMM_OK;
+    st = check_operands(M, N, K, A, lda, B, ldb, C, ldc, out_dtype);
+    if (st != GEMM_OK) return st;
+
+    int device = 0;
+    DeviceState *ds = nullptr;
+    st = current_device(&device, &ds);
+    if (st != GEMM_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) return launch_fill_zero(M, N, C, ldc, out_dtype == GEMM_OUT_BF16 ? 2 : 4, ds->desc.num_sms, s);
+    return launch_gemm(M, N, K, A, lda, B, ldb, C, ldc, layout_a, layout_b, out_dtype, o, s, *ds,
+                       PartialBuffer{false, nullptr, 0});
 }
 
 gemm_status_t gemm_bf16(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
@@ -654,14 +831,10 @@ gemm_status_t gemm_bf16(int64_t M, int64_t N, int64_t K, const void *A, int64_t 
 
 gemm_status_t gemm_reserve_workspace(size_t bytes) {
     int device = 0;
-    if (cudaGetDevice(&device) != cudaSuccess) {
-        cudaGetLastError();
-        return GEMM_ERR_NO_DEVICE;
-    }
     DeviceState *ds = nullptr;
-    gemm_status_t st = device_state(device, &ds);
+    gemm_status_t st = current_device(&device, &ds);
     if (st != GEMM_OK) return st;
-    return ensure_workspace(device, *ds, bytes);
+    return ensure_workspace(*ds, bytes);
 }
 
 void gemm_release_workspace(void) {
@@ -748,98 +921,21 @@ extern "C" gemm_status_t gemm_bf16_splitk_noalloc(int64_t M, int64_t N, int64_t 
     gemm_status_t st = check_problem(M, N, K, layout_a, layout_b, out_dtype, split_k);
     if (st != GEMM_OK) return st;
     if (M == 0 || N == 0) return GEMM_OK;
-    const int esize = out_dtype == GEMM_OUT_BF16 ? 2 : 4;
-    if (!C || ldc < N) return GEMM_ERR_INVALID_VALUE;
-    if (reinterpret_cast<uintptr_t>(C) % 16 != 0 || (ldc * esize) % 16 != 0) return GEMM_ERR_MISALIGNED;
-    if (K > 0) {
-        if (!A || !B || lda < K || ldb < K) return GEMM_ERR_INVALID_VALUE;
-        if (reinterpret_cast<uintptr_t>(A) % 16 != 0 || reinterpret_cast<uintptr_t>(B) % 16 != 0 || lda % 8 != 0 ||
-            ldb % 8 != 0)
-            return GEMM_ERR_MISALIGNED;
-    }
+    st = check_operands(M, N, K, A, lda, B, ldb, C, ldc, out_dtype);
+    if (st != GEMM_OK) return st;
 
     int device = 0;
-    if (cudaGetDevice(&device) != cudaSuccess) {
-        cudaGetLastError();
-        return GEMM_ERR_NO_DEVICE;
-    }
     DeviceState *ds = nullptr;
-    st = device_state(device, &ds);
+    st = current_device(&device, &ds);
     if (st != GEMM_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) return launch_fill_zero(M, N, C, ldc, out_dtype == GEMM_OUT_BF16 ? 2 : 4, ds->desc.num_sms, s);
 
-    if (K == 0) return launch_fill_zero(M, N, C, ldc, esize, ds->desc.num_sms, s);
-
-    gemm_plan_t plan;
-    st = make_plan(M, N, K, layout_a, layout_b, out_dtype, split_k, 1, ds->desc, main_kernel_desc(ds->regs_per_thread),
-                   &plan);
-    if (st != GEMM_OK) return st;
-    const int64_t ldp = (N + 3) / 4 * 4;
     float *scratch = nullptr;
-    if (plan.split_k > 1) {
-        const int64_t per_split = M * ldp;   // < 2^62: M, N < 2^31
-        if (per_split > static_cast<int64_t>(GEMM_NOALLOC_SCRATCH_FLOATS) ||
-            plan.split_k > static_cast<int64_t>(GEMM_NOALLOC_SCRATCH_FLOATS) / per_split)
-            return GEMM_ERR_INVALID_VALUE;
-        st = noalloc_scratch(device, &scratch);
-        if (st != GEMM_OK) return st;
-    }
-
-    CUtensorMap tmap_a, tmap_b;
-    st = encode_operand(&tmap_a, A, K, M, lda, TILE_M);
+    st = noalloc_scratch(device, &scratch);
     if (st != GEMM_OK) return st;
-    st = encode_operand(&tmap_b, B, K, N, ldb, TILE_N);
-    if (st != GEMM_OK) return st;
-
-    KernelParams p{};
-    p.M = static_cast<int>(M);
-    p.N = static_cast<int>(N);
-    p.K = static_cast<int>(K);
-    p.tiles_m = static_cast<int>((M + TILE_M - 1) / TILE_M);
-    p.tiles_n = static_cast<int>((N + TILE_N - 1) / TILE_N);
-    p.k_tiles = plan.k_tiles;
-    p.split_k = plan.split_k;
-    p.group_m = DEFAULT_RASTER_GROUP_M;
-    p.num_units = plan.grid;
-    if (plan.split_k > 1) {
-        p.out = scratch;
-        p.ld_out = ldp;
-        p.split_stride = M * ldp;
-        p.out_bf16 = 0;
-    } else {
-        p.out = C;
-        p.ld_out = ldc;
-        p.split_stride = 0;
-        p.out_bf16 = out_dtype == GEMM_OUT_BF16 ? 1 : 0;
-    }
-    p.timeout_ns = static_cast<unsigned long long>(DEFAULT_TIMEOUT_MS) * 1000000ull;
-    p.skip_load = 0;
-
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(static_cast<unsigned>(plan.launch_ctas));
-    cfg.blockDim = dim3(NUM_THREADS);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
-    cfg.stream = s;
-    if (cudaLaunchKernelEx(&cfg, gemm_bf16_tcgen05_kernel, tmap_a, tmap_b, p) != cudaSuccess) {
-        cudaGetLastError();
-        return GEMM_ERR_LAUNCH;
-    }
-    if (plan.split_k > 1) {
-        const long long total = M * ((N + 3) / 4);
-        long long blocks = (total + 255) / 256;
-        const long long cap = 4LL * ds->desc.num_sms;
-        if (blocks > cap) blocks = cap;
-        cudaLaunchConfig_t cc{};
-        cc.gridDim = dim3(static_cast<unsigned>(blocks));
-        cc.blockDim = dim3(256);
-        cc.stream = s;
-        if (cudaLaunchKernelEx(&cc, splitk_combine_kernel, static_cast<const float *>(scratch),
-                               static_cast<long long>(ldp), static_cast<long long>(M * ldp), plan.split_k,
-                               static_cast<int>(M), static_cast<int>(N), C, static_cast<long long>(ldc),
-                               out_dtype == GEMM_OUT_BF16 ? 1 : 0) != cudaSuccess) {
-            cudaGetLastError();
-            return GEMM_ERR_LAUNCH;
-        }
-    }
-    return GEMM_OK;
+    gemm_options_t o{};
+    o.split_k = split_k;
+    return launch_gemm(M, N, K, A, lda, B, ldb, C, ldc, layout_a, layout_b, out_dtype, o, s, *ds,
+                       PartialBuffer{true, scratch, static_cast<int64_t>(GEMM_NOALLOC_SCRATCH_FLOATS)});
 }

@@ -1,29 +1,81 @@
-// Compile-time shape of the main GEMM kernel, shared by the planner and the
-// CUDA sources.  One CTA computes a TILE_M x TILE_N block of C; operands
-// arrive in TILE_K-wide k-tiles through a STAGES-deep shared-memory ring.
+// Compile-time shapes of the GEMM kernel variants, shared by the planner (host
+// C++) and the CUDA sources.
+//
+// A variant is (CTA group, BN):
+//   * CTA group 1: one CTA computes a 128 x BN block of C with
+//     tcgen05.mma.cta_group::1 (M = 128);
+//   * CTA group 2: a cluster of two CTAs on a pair of SMs computes a
+//     256 x BN block with tcgen05.mma.cta_group::2 (M = 256): each CTA stages
+//     its own 128 rows of A and BN/2 rows of B, and holds its 128 rows of the
+//     accumulator in its own tensor memory.
+// Operands arrive in TILE_K-wide k-tiles (64 bf16 = 128 bytes, one swizzle
+// span) through a ring of as many stages as the shared memory holds.
 #pragma once
+
+#if defined(__CUDACC__)
+#define GEMM_HD __host__ __device__
+#else
+#define GEMM_HD
+#endif
 
 namespace gemm {
 
-constexpr int TILE_M = 128;              // rows of C per CTA (= MMA M, one TMEM lane per row)
-constexpr int TILE_N = 256;              // columns of C per CTA (= MMA N)
-constexpr int TILE_K = 64;               // bf16 elements per k-tile row: 128 bytes, one swizzle span
-constexpr int MMA_K = 16;                // K of one kind::f16 tcgen05.mma
-constexpr int STAGES = 4;                // operand ring depth
-constexpr int ACC_BUFS = 2;              // accumulators in TMEM (epilogue overlaps the next tile)
-constexpr int TMEM_COLS = ACC_BUFS * TILE_N;   // fp32 accumulator: one column per element of a row
-
-constexpr int NUM_WARPS = 6;             // 0: TMA producer, 1: MMA issuer, 2..5: epilogue
+constexpr int TILE_K = 64;
+constexpr int MMA_K = 16;                 // K of one kind::f16 tcgen05.mma
+constexpr int CTA_ROWS = 128;             // rows of C per CTA = TMEM lanes
+constexpr int ACC_BUFS = 2;               // accumulators in TMEM (epilogue overlaps the next tile)
+constexpr int NUM_WARPS = 6;              // 0: TMA producer, 1: TMEM owner + MMA issuer, 2..5: epilogue
 constexpr int NUM_THREADS = NUM_WARPS * 32;
-constexpr int EPI_THREADS = 128;
+constexpr int EPI_WARPS = 4;
+constexpr int NUM_BARRIERS_FIXED = 2 * ACC_BUFS + 1;   // + 2 per stage
+constexpr int SMEM_LIMIT = 232448;        // opt-in dynamic shared memory per CTA on sm_100-class parts
+constexpr int MAX_STAGES = 8;
 
-constexpr int A_STAGE_BYTES = TILE_M * TILE_K * 2;
-constexpr int B_STAGE_BYTES = TILE_N * TILE_K * 2;
-constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-constexpr int NUM_BARRIERS = 2 * STAGES + 2 * ACC_BUFS + 1;
-// ring + barriers + TMEM address slot + abort flag, plus 1 KiB to align the
-// ring to the 1024-byte swizzle atom
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARRIERS * 8 + 16;
+enum Variant : int {
+    VARIANT_AUTO = 0,
+    VARIANT_1SM_128x256 = 1,
+    VARIANT_2SM_256x256 = 2,
+    VARIANT_2SM_256x128 = 3,
+    VARIANT_COUNT = 4
+};
+
+GEMM_HD constexpr int pow2_at_least(int x, int p = 32) { return p >= x ? p : pow2_at_least(x, p * 2); }
+
+struct VariantInfo {
+    int cta_group;   // CTAs cooperating on one tile (cluster size)
+    int bn;          // columns of C per tile
+    int tile_m;      // rows of C per tile (128 * cta_group)
+    int b_rows;      // rows of B (N direction) each CTA stages
+    int a_stage;     // bytes of A per stage per CTA
+    int b_stage;     // bytes of B per stage per CTA
+    int stage;       // a_stage + b_stage
+    int stages;      // ring depth
+    int smem;        // dynamic shared memory per CTA
+    int tmem_cols;   // tensor-memory columns per CTA (power of two >= 32)
+};
+
+GEMM_HD constexpr VariantInfo make_variant(int cg, int bn) {
+    const int a = CTA_ROWS * TILE_K * 2;
+    const int b = (bn / cg) * TILE_K * 2;
+    const int st = a + b;
+    const int fixed = 1024 + (NUM_BARRIERS_FIXED + 2 * MAX_STAGES) * 8 + 16;
+    int stages = (SMEM_LIMIT - fixed) / st;
+    if (stages > MAX_STAGES) stages = MAX_STAGES;
+    return VariantInfo{cg, bn, CTA_ROWS * cg, bn / cg, a, b, st, stages,
+                       1024 + stages * st + (NUM_BARRIERS_FIXED + 2 * stages) * 8 + 16,
+                       pow2_at_least(ACC_BUFS * bn)};
+}
+
+GEMM_HD constexpr VariantInfo variant_info(int v) {
+    return v == VARIANT_2SM_256x256 ? make_variant(2, 256)
+         : v == VARIANT_2SM_256x128 ? make_variant(2, 128)
+                                    : make_variant(1, 256);
+}
+
+static_assert(variant_info(VARIANT_1SM_128x256).stages == 4, "1-SM 128x256: four 48 KiB stages");
+static_assert(variant_info(VARIANT_2SM_256x256).stages == 7, "2-SM 256x256: seven 32 KiB stages");
+static_assert(variant_info(VARIANT_2SM_256x256).smem <= SMEM_LIMIT, "fits");
+static_assert(variant_info(VARIANT_2SM_256x128).smem <= SMEM_LIMIT, "fits");
 
 constexpr int DEFAULT_RASTER_GROUP_M = 16;
 constexpr int DEFAULT_TIMEOUT_MS = 4000;

@@ -80,46 +80,65 @@ int choose_split(int64_t tiles, int k_tiles, int capacity, int requested) {
     return s < 1 ? 1 : s;
 }
 
+int resolve_variant(int requested) {
+    if (requested == VARIANT_AUTO) return VARIANT_2SM_256x256;
+    return requested;
+}
+
 gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_layout_t la, gemm_layout_t lb,
-                        gemm_dtype_t out, int split_k, int persistent, const gemm_device_desc_t &dev,
-                        const gemm_kernel_desc_t &kern, gemm_plan_t *plan) {
+                        gemm_dtype_t out, int split_k, int persistent, int variant,
+                        const gemm_device_desc_t &dev, const gemm_kernel_desc_t &kern, gemm_plan_t *plan) {
     gemm_status_t st = check_problem(M, N, K, la, lb, out, split_k);
     if (st != GEMM_OK) return st;
+    if (variant < 0 || variant >= VARIANT_COUNT) return GEMM_ERR_INVALID_VALUE;
     if (dev.num_sms <= 0) return GEMM_ERR_INVALID_VALUE;
+    const int v = resolve_variant(variant);
+    const VariantInfo vi = variant_info(v);
+    const int cs = kern.cluster_size > 0 ? kern.cluster_size : 1;
+    if (cs != vi.cta_group) return GEMM_ERR_INVALID_VALUE;
     std::memset(plan, 0, sizeof *plan);
     int b = 0, lim = 0;
     st = occupancy(kern, dev, &b, &lim);
     if (st != GEMM_OK) return st;
 
-    plan->tile_m = TILE_M;
-    plan->tile_n = TILE_N;
+    // CTAs resident at once: S b, rounded down to whole clusters, or the
+    // device's own count of resident clusters when it is known.
+    int64_t clusters = (int64_t)dev.num_sms * b / cs;
+    if (kern.max_active_clusters > 0 && kern.max_active_clusters < clusters) clusters = kern.max_active_clusters;
+    if (clusters <= 0) return GEMM_ERR_INVALID_VALUE;
+    const int64_t resident = clusters * cs;
+
+    plan->kernel_variant = v;
+    plan->cluster_size = cs;
+    plan->resident_ctas = resident;
+    plan->tile_m = vi.tile_m;
+    plan->tile_n = vi.bn;
     plan->tile_k = TILE_K;
-    plan->stages = STAGES;
+    plan->stages = vi.stages;
     plan->threads_per_cta = kern.threads_per_cta;
     plan->num_sms = dev.num_sms;
     plan->ctas_per_sm = b;
     plan->occupancy_limiter = lim;
     plan->persistent = persistent ? 1 : 0;
-    plan->tiles = cdiv(M, TILE_M) * cdiv(N, TILE_N);
+    plan->tiles = cdiv(M, vi.tile_m) * cdiv(N, vi.bn);
     plan->k_tiles = (int)cdiv(K, TILE_K);
-    const int capacity = dev.num_sms * b;
-    plan->split_k = (plan->tiles > 0) ? choose_split(plan->tiles, plan->k_tiles, capacity, split_k) : 1;
+    plan->split_k = (plan->tiles > 0) ? choose_split(plan->tiles, plan->k_tiles, (int)clusters, split_k) : 1;
     plan->k_tiles_per_split = plan->k_tiles > 0 ? (int)cdiv(plan->k_tiles, plan->split_k) : 0;
-    plan->grid = plan->tiles * plan->split_k;
-    plan->launch_ctas = persistent ? (plan->grid < capacity ? plan->grid : capacity) : plan->grid;
-    plan->m_padded = cdiv(M, TILE_M) * TILE_M;
-    plan->n_padded = cdiv(N, TILE_N) * TILE_N;
+    plan->grid = plan->tiles * plan->split_k * cs;
+    plan->launch_ctas = persistent ? (plan->grid < resident ? plan->grid : resident) : plan->grid;
+    plan->m_padded = cdiv(M, vi.tile_m) * vi.tile_m;
+    plan->n_padded = cdiv(N, vi.bn) * vi.bn;
     plan->k_padded = cdiv(K, TILE_K) * TILE_K;
     if (plan->grid > 0) {
-        const int64_t waves = cdiv(plan->grid, capacity);
-        plan->eta_wave = (double)plan->grid / ((double)waves * (double)capacity);
+        const int64_t waves = cdiv(plan->grid, resident);
+        plan->eta_wave = (double)plan->grid / ((double)waves * (double)resident);
     }
     if (M > 0 && N > 0 && K > 0) {
         plan->eta_pad = ((double)M / plan->m_padded) * ((double)N / plan->n_padded) * ((double)K / plan->k_padded);
     }
     plan->flops = 2.0 * (double)M * (double)N * (double)K;
-    plan->smem_bytes = SMEM_BYTES;
-    plan->tmem_cols = TMEM_COLS;
+    plan->smem_bytes = vi.smem;
+    plan->tmem_cols = vi.tmem_cols;
     plan->workspace_bytes = plan->split_k > 1 ? (int64_t)plan->split_k * M * ((N + 3) / 4 * 4) * 4 : 0;
     return GEMM_OK;
 }
@@ -135,10 +154,11 @@ gemm_status_t gemm_occupancy(const gemm_kernel_desc_t *kern, const gemm_device_d
 }
 
 gemm_status_t gemm_plan_for_device(int64_t M, int64_t N, int64_t K, gemm_layout_t layout_a, gemm_layout_t layout_b,
-                                   gemm_dtype_t out_dtype, int split_k, int persistent, const gemm_device_desc_t *dev,
-                                   const gemm_kernel_desc_t *kern, gemm_plan_t *plan) {
+                                   gemm_dtype_t out_dtype, int split_k, int persistent, int kernel_variant,
+                                   const gemm_device_desc_t *dev, const gemm_kernel_desc_t *kern, gemm_plan_t *plan) {
     if (!dev || !kern || !plan) return GEMM_ERR_INVALID_VALUE;
-    return gemm::make_plan(M, N, K, layout_a, layout_b, out_dtype, split_k, persistent, *dev, *kern, plan);
+    return gemm::make_plan(M, N, K, layout_a, layout_b, out_dtype, split_k, persistent, kernel_variant, *dev, *kern,
+                           plan);
 }
 
 const char *gemm_status_string(gemm_status_t s) {

@@ -62,6 +62,20 @@ typedef enum {
     GEMM_ERR_DEVICE_TIMEOUT = 7   /* a device-side pipeline wait ran out of time */
 } gemm_status_t;
 
+/* Kernel variants.  A tile is the block of C one work unit produces.
+ *   1SM_128x256: one CTA per tile, tcgen05.mma.cta_group::1 with M = 128.
+ *   2SM_256x256, 2SM_256x128: a cluster of two CTAs on a pair of SMs per
+ *     tile, tcgen05.mma.cta_group::2 with M = 256; each CTA stages its own
+ *     128 rows of A and half of the tile's columns of B, and holds its 128
+ *     rows of the accumulator.
+ * GEMM_KERNEL_AUTO lets the plan choose. */
+typedef enum {
+    GEMM_KERNEL_AUTO = 0,
+    GEMM_KERNEL_1SM_128x256 = 1,
+    GEMM_KERNEL_2SM_256x256 = 2,
+    GEMM_KERNEL_2SM_256x128 = 3
+} gemm_kernel_variant_t;
+
 /* Which resource sets the number of resident CTAs per SM. */
 typedef enum {
     GEMM_LIMIT_REGISTERS = 0,
@@ -89,6 +103,9 @@ typedef struct {
     int threads_per_cta;
     int smem_per_cta;            /* dynamic + static shared memory, bytes */
     int tmem_cols_per_cta;       /* tensor-memory columns allocated by one CTA */
+    int cluster_size;            /* CTAs per cluster (1 or 2) */
+    int max_active_clusters;     /* clusters resident at once on the device; 0 = unknown
+                                    (then floor(S b / cluster_size)) */
 } gemm_kernel_desc_t;
 
 /*
@@ -104,9 +121,11 @@ typedef struct {
  * per-CTA reservation), tensor memory, threads, and the CTA limit.  eta_wave
  * is reported by that formula for both launch modes; a persistent launch
  * still runs ceil(G / (S b)) rounds of equal tiles.
+ * For two-CTA tiles, G counts CTAs (two per tile and split) and S b is the
+ * number of CTAs resident at once: resident clusters times two.
  */
 typedef struct {
-    int tile_m, tile_n, tile_k;  /* T_M x T_N x T_K of one CTA */
+    int tile_m, tile_n, tile_k;  /* T_M x T_N x T_K of one tile */
     int stages;                  /* depth of the shared-memory operand ring */
     int threads_per_cta;
     int split_k;                 /* splits actually used (after auto choice and clamping) */
@@ -126,6 +145,9 @@ typedef struct {
     int64_t smem_bytes;          /* dynamic shared memory per CTA of the main kernel */
     int64_t workspace_bytes;     /* split-K partial buffer: split_k * M * round_up(N, 4) * 4 */
     int tmem_cols;               /* tensor-memory columns per CTA */
+    int kernel_variant;          /* gemm_kernel_variant_t actually used */
+    int cluster_size;            /* CTAs per tile */
+    int64_t resident_ctas;       /* S b: CTAs resident at once */
 } gemm_plan_t;
 
 /* Options of gemm_bf16_ex.  Zero-initialise and set what you need. */
@@ -140,14 +162,16 @@ typedef struct {
                                     the k-th stage load (1-based, counting from the first load of
                                     CTA 0) unissued, so its consumer's wait runs out and the call
                                     ends with GEMM_ERR_DEVICE_TIMEOUT on the device */
+    int kernel_variant;          /* gemm_kernel_variant_t; 0 = the plan chooses */
 } gemm_options_t;
 
 /* Fill `dev` with the facts of CUDA device `device`. */
 gemm_status_t gemm_device_desc_query(int device, gemm_device_desc_t *dev);
 
-/* The footprint of this library's main kernel.  Registers come from the
- * compiled kernel when a device is present, else 0. */
-gemm_status_t gemm_kernel_desc(gemm_kernel_desc_t *kern);
+/* The footprint of one kernel variant (GEMM_KERNEL_AUTO: the variant the
+ * plan chooses by default).  Registers and resident clusters come from the
+ * compiled kernel on the current device when there is one, else 0. */
+gemm_status_t gemm_kernel_desc(int kernel_variant, gemm_kernel_desc_t *kern);
 
 /* Resident CTAs per SM for a footprint on a device (host arithmetic only).
  * Returns INVALID_VALUE for non-positive threads or a footprint that fits
@@ -157,17 +181,19 @@ gemm_status_t gemm_occupancy(const gemm_kernel_desc_t *kern, const gemm_device_d
 
 /* Plan a GEMM for explicit device and kernel facts; host arithmetic only, no
  * CUDA call.  Same argument rules as gemm_bf16 for the sizes, layouts and
- * out dtype. */
+ * out dtype.  `kern` describes the footprint of `kernel_variant` (an explicit
+ * variant; GEMM_KERNEL_AUTO resolves to the default variant). */
 gemm_status_t gemm_plan_for_device(int64_t M, int64_t N, int64_t K,
                                    gemm_layout_t layout_a, gemm_layout_t layout_b,
                                    gemm_dtype_t out_dtype, int split_k, int persistent,
-                                   const gemm_device_desc_t *dev,
+                                   int kernel_variant, const gemm_device_desc_t *dev,
                                    const gemm_kernel_desc_t *kern, gemm_plan_t *plan);
 
-/* Plan a GEMM on the current CUDA device with this library's kernel. */
+/* Plan a GEMM on the current CUDA device with one of this library's kernel
+ * variants (GEMM_KERNEL_AUTO: the one gemm_bf16 would use). */
 gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K,
                         gemm_layout_t layout_a, gemm_layout_t layout_b,
-                        gemm_dtype_t out_dtype, int split_k, gemm_plan_t *plan);
+                        gemm_dtype_t out_dtype, int split_k, int kernel_variant, gemm_plan_t *plan);
 
 /*
  * C = A . B on `stream`.

@@ -62,10 +62,17 @@ def test_occupancy_worked_example_through_the_abi():
     assert g.gemm_occupancy(bad, d)[0] == 1
 
 
-def _plan(M, N, K, split=1, persistent=1, d=None, regs=64, out=g.GEMM_OUT_BF16):
-    k = g.gemm_kernel_desc_t(regs_per_thread=regs, threads_per_cta=192, smem_per_cta=197752, tmem_cols_per_cta=512)
-    st, p = g.gemm_plan_for_device(M, N, K, g.GEMM_ROW_MAJOR, g.GEMM_COL_MAJOR, out, split, persistent,
-                                   d or dev(), k)
+def kern(variant, regs=64, max_active_clusters=0):
+    """The library's own footprint of a variant, with a register count."""
+    k = g.gemm_kernel_desc(variant)
+    k.regs_per_thread = regs
+    k.max_active_clusters = max_active_clusters
+    return k
+
+
+def _plan(M, N, K, split=1, persistent=1, d=None, regs=64, out=g.GEMM_OUT_BF16, variant=1, mac=0):
+    st, p = g.gemm_plan_for_device(M, N, K, g.GEMM_ROW_MAJOR, g.GEMM_COL_MAJOR, out, split, persistent, variant,
+                                   d or dev(), kern(variant, regs, mac))
     assert st == 0
     return p
 
@@ -73,24 +80,43 @@ def _plan(M, N, K, split=1, persistent=1, d=None, regs=64, out=g.GEMM_OUT_BF16):
 WORKLOADS = [(256, 256, 256), (4096, 4096, 4096), (4095, 4096, 4096), (4097, 4096, 4096),
              (4096, 4096, 4088), (4096, 4104, 4096), (3968, 4096, 4096), (16384, 8192, 8192),
              (128, 256, 65536), (1, 1, 1), (129, 257, 65)]
+TILES = {1: (128, 256, 1), 2: (256, 256, 2), 3: (256, 128, 2)}
 
 
-@pytest.mark.parametrize("S", [148, 152])
+def test_kernel_desc_without_a_device():
+    for v, (tm, tn, cs) in TILES.items():
+        k = g.gemm_kernel_desc(v)
+        assert k.threads_per_cta == 192 and k.cluster_size == cs
+        assert 0 < k.smem_per_cta <= 232448
+        assert k.tmem_cols_per_cta == (512 if tn == 256 else 256)
+
+
+@pytest.mark.parametrize("variant", [1, 2, 3])
+@pytest.mark.parametrize("S,mac", [(148, 0), (152, 0), (152, 72)])
 @pytest.mark.parametrize("shape", WORKLOADS)
-def test_plan_matches_oracle_closed_forms(shape, S):
+def test_plan_matches_oracle_closed_forms(shape, S, mac, variant):
+    """The plan against the oracle's closed forms; S b is the number of CTAs
+    resident at once (for two-CTA tiles: resident clusters times two)."""
     M, N, K = shape
-    p = _plan(M, N, K, d=dev(num_sms=S))
-    b, lim = pf.ctas_per_sm(regs_per_thread=64, threads=192, smem_per_cta=197752, regs_per_sm=65536,
+    tm, tn, cs = TILES[variant]
+    k = kern(variant, 64, mac)
+    p = _plan(M, N, K, d=dev(num_sms=S), variant=variant, mac=mac)
+    b, lim = pf.ctas_per_sm(regs_per_thread=64, threads=192, smem_per_cta=k.smem_per_cta, regs_per_sm=65536,
                             smem_per_sm=233472, smem_reserved_per_cta=1024)
     assert (p.ctas_per_sm, g.LIMITERS[p.occupancy_limiter]) == (b, lim) == (1, "smem")
-    assert (p.tile_m, p.tile_n, p.tile_k) == (128, 256, 64)
-    assert p.tiles == pf.grid(M, N, 128, 256)
-    assert p.grid == pf.grid(M, N, 128, 256, p.split_k)
-    assert p.eta_wave == pytest.approx(float(pf.eta_wave(p.grid, S, b)), rel=1e-15)
-    assert p.eta_pad == pytest.approx(float(pf.eta_pad(M, N, K, 128, 256, 64)), rel=1e-15)
+    clusters = S * b // cs
+    if mac:
+        clusters = min(clusters, mac)
+    R = clusters * cs
+    assert p.resident_ctas == R and p.cluster_size == cs and p.kernel_variant == variant
+    assert (p.tile_m, p.tile_n, p.tile_k) == (tm, tn, 64)
+    assert p.tiles == pf.grid(M, N, tm, tn)
+    assert p.grid == pf.grid(M, N, tm, tn, p.split_k) * cs
+    assert p.eta_wave == pytest.approx(float(pf.eta_wave(p.grid, R, 1)), rel=1e-15)
+    assert p.eta_pad == pytest.approx(float(pf.eta_pad(M, N, K, tm, tn, 64)), rel=1e-15)
     assert p.flops == pf.flops(M, N, K)
-    assert (p.m_padded, p.n_padded, p.k_padded) == (pf.padded(M, 128), pf.padded(N, 256), pf.padded(K, 64))
-    assert p.launch_ctas == min(p.grid, S * b)
+    assert (p.m_padded, p.n_padded, p.k_padded) == (pf.padded(M, tm), pf.padded(N, tn), pf.padded(K, 64))
+    assert p.launch_ctas == min(p.grid, R)
     assert p.k_tiles == math.ceil(K / 64)
 
 
@@ -103,6 +129,23 @@ def test_plan_hand_values_148_sms():
     assert p.eta_pad == pytest.approx(4097 / 4224, rel=1e-15)
     p = _plan(4096, 4096, 4096, persistent=0, d=d)
     assert p.launch_ctas == 512 and p.persistent == 0
+
+
+def test_plan_hand_values_pair_tiles_152_sms():
+    """256x256 pair tiles: 16 x 16 = 256 tiles, 512 CTAs on 152 resident CTAs
+    = 4 rounds (608 slots).  256x128: 512 tiles, 1024 CTAs, 7 rounds (1064)."""
+    p = _plan(4096, 4096, 4096, variant=2)
+    assert (p.tiles, p.grid, p.resident_ctas, p.launch_ctas) == (256, 512, 152, 152)
+    assert p.eta_wave == pytest.approx(512 / 608, rel=1e-15)
+    p = _plan(4096, 4096, 4096, variant=3)
+    assert (p.tiles, p.grid) == (512, 1024)
+    assert p.eta_wave == pytest.approx(1024 / 1064, rel=1e-15)
+    # 72 resident pairs (some SMs without a partner): 144 CTAs, 4 rounds of 144
+    p = _plan(4096, 4096, 4096, variant=2, mac=72)
+    assert p.resident_ctas == 144 and p.eta_wave == pytest.approx(512 / 576, rel=1e-15)
+    p = _plan(16384, 8192, 8192, variant=2)
+    assert (p.tiles, p.grid) == (2048, 4096)
+    assert p.eta_wave == pytest.approx(4096 / (27 * 152), rel=1e-15)
 
 
 @pytest.mark.parametrize("split,eta", [(1, 1 / 148), (8, 8 / 148), (32, 32 / 148), (74, 0.5), (148, 1.0)])
@@ -120,8 +163,17 @@ def test_plan_split_k_clamped_and_auto():
     assert p.split_k == 4
     p = _plan(128, 256, 65536, split=0)       # auto: one tile, 1024 k-tiles, 152 slots
     assert p.split_k == 152
+    p = _plan(128, 256, 65536, split=0, variant=2)   # pairs: 76 slots
+    assert p.split_k == 76 and p.grid == 152
     p = _plan(4096, 4096, 4096, split=0)      # auto: the tiles fill the GPU, no split
     assert p.split_k == 1
+
+
+def test_plan_auto_variant_is_the_pair_kernel():
+    st, p = g.gemm_plan_for_device(4096, 4096, 4096, 0, 1, 1, 0, 1, 0, dev(), kern(2))
+    assert st == 0 and p.kernel_variant == 2
+    st, _ = g.gemm_plan_for_device(4096, 4096, 4096, 0, 1, 1, 0, 1, 0, dev(), kern(1))
+    assert st == 1     # a footprint that does not match the variant
 
 
 def _call(M, N, K, A=16, lda=64, B=16, ldb=64, C=16, ldc=64, la=0, lb=1, out=0, split=1):
@@ -151,16 +203,20 @@ def test_argument_checks_before_any_cuda_call():
     assert _call(4, 4, 4, ldc=68, out=1) == 2   # bf16: 136 bytes
     opts = g.gemm_options_t(timeout_ms=-1)
     assert g.gemm_bf16_ex(4, 4, 4, 16, 64, 16, 64, 16, 64, 0, 1, 0, opts, None) == 1
+    opts = g.gemm_options_t(kernel_variant=9)
+    assert g.gemm_bf16_ex(4, 4, 4, 16, 64, 16, 64, 16, 64, 0, 1, 0, opts, None) == 1
 
 
 def test_plan_argument_checks():
-    k = g.gemm_kernel_desc_t(regs_per_thread=64, threads_per_cta=192, smem_per_cta=197752, tmem_cols_per_cta=512)
+    k = kern(1)
     plan = g.gemm_plan_t()
     L = g.lib()
-    assert L.gemm_plan_for_device(4, 4, 4, 0, 1, 0, 0, 1, None, ctypes.byref(k), ctypes.byref(plan)) == 1
-    st, _ = g.gemm_plan_for_device(4, 4, 4, 1, 1, 0, 0, 1, dev(), k)
+    assert L.gemm_plan_for_device(4, 4, 4, 0, 1, 0, 0, 1, 1, None, ctypes.byref(k), ctypes.byref(plan)) == 1
+    st, _ = g.gemm_plan_for_device(4, 4, 4, 1, 1, 0, 0, 1, 1, dev(), k)
     assert st == 3
-    too_big = g.gemm_kernel_desc_t(regs_per_thread=64, threads_per_cta=192, smem_per_cta=240000,
-                                   tmem_cols_per_cta=512)
-    st, _ = g.gemm_plan_for_device(4, 4, 4, 0, 1, 0, 0, 1, dev(), too_big)
+    st, _ = g.gemm_plan_for_device(4, 4, 4, 0, 1, 0, 0, 1, 7, dev(), k)
+    assert st == 1
+    too_big = kern(1)
+    too_big.smem_per_cta = 240000
+    st, _ = g.gemm_plan_for_device(4, 4, 4, 0, 1, 0, 0, 1, 1, dev(), too_big)
     assert st == 1

@@ -125,41 +125,60 @@ SMALL_SHAPES = [
 ]
 
 
+VARIANTS = [1, 2, 3]   # 1-SM 128x256, 2-SM 256x256, 2-SM 256x128
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("shape", SMALL_SHAPES)
 @pytest.mark.parametrize("out", ["f32", "bf16"])
-def test_small_shapes_normal(oracle_lib, shape, out):
+def test_small_shapes_normal(oracle_lib, shape, out, variant):
     M, N, K = shape
     A, Bt = operands(M, N, K, "normal", True, SEED + 2)
-    full_check(oracle_lib, A, Bt, M, N, K, torch.float32 if out == "f32" else torch.bfloat16)
+    full_check(oracle_lib, A, Bt, M, N, K, torch.float32 if out == "f32" else torch.bfloat16,
+               kernel_variant=variant)
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("shape", [(129, 257, 65), (513, 769, 1000), (384, 1024, 512)])
-def test_small_shapes_integers_exact(oracle_lib, shape):
+def test_small_shapes_integers_exact(oracle_lib, shape, variant):
     M, N, K = shape
     A, Bt = operands(M, N, K, "int4", False, SEED + 3)
-    full_check(oracle_lib, A, Bt, M, N, K, torch.float32, exact=True)
-    full_check(oracle_lib, A, Bt, M, N, K, torch.bfloat16, exact=True)
+    full_check(oracle_lib, A, Bt, M, N, K, torch.float32, exact=True, kernel_variant=variant)
+    full_check(oracle_lib, A, Bt, M, N, K, torch.bfloat16, exact=True, kernel_variant=variant)
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("split", [2, 3, 7])
-def test_small_split_k(oracle_lib, split):
+def test_small_split_k(oracle_lib, split, variant):
     M, N, K = 200, 300, 1000
     A, Bt = operands(M, N, K, "normal", True, SEED + 4)
-    full_check(oracle_lib, A, Bt, M, N, K, torch.float32, split_k=split)
-    full_check(oracle_lib, A, Bt, M, N, K, torch.bfloat16, split_k=split)
+    full_check(oracle_lib, A, Bt, M, N, K, torch.float32, split_k=split, kernel_variant=variant)
+    full_check(oracle_lib, A, Bt, M, N, K, torch.bfloat16, split_k=split, kernel_variant=variant)
     Ai, Bti = operands(M, N, K, "int4", False, SEED + 5)
-    full_check(oracle_lib, Ai, Bti, M, N, K, torch.float32, exact=True, split_k=split)
+    full_check(oracle_lib, Ai, Bti, M, N, K, torch.float32, exact=True, split_k=split, kernel_variant=variant)
 
 
-def test_non_persistent_matches_persistent_bitwise(oracle_lib):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_non_persistent_matches_persistent_bitwise(oracle_lib, variant):
     M, N, K = 640, 1280, 320
     A, Bt = operands(M, N, K, "normal", True, SEED + 6)
-    C1 = run_gpu(A, Bt, M, N, K, torch.float32)
-    C2 = run_gpu(A, Bt, M, N, K, torch.float32, non_persistent=True)
-    C3 = run_gpu(A, Bt, M, N, K, torch.float32, raster_group_m=1)
+    C1 = run_gpu(A, Bt, M, N, K, torch.float32, kernel_variant=variant)
+    C2 = run_gpu(A, Bt, M, N, K, torch.float32, non_persistent=True, kernel_variant=variant)
+    C3 = run_gpu(A, Bt, M, N, K, torch.float32, raster_group_m=1, kernel_variant=variant)
     assert np.array_equal(C1, C2) and np.array_equal(C1, C3)
     ref, sabs = oracle_lib.gemm(A, Bt, M, N, K)
     assert check_f32(C1, ref, sabs)[0] == 0
+
+
+def test_variants_agree_bitwise_on_integers(oracle_lib):
+    """Every variant gives the exact product on small-integer inputs, so all
+    three agree bit for bit."""
+    M, N, K = 700, 900, 777
+    A, Bt = operands(M, N, K, "int4", False, SEED + 9)
+    outs = [run_gpu(A, Bt, M, N, K, torch.float32, kernel_variant=v) for v in VARIANTS]
+    ref, _ = oracle_lib.gemm(A, Bt, M, N, K)
+    for C in outs:
+        assert np.array_equal(C.astype(np.float64), ref)
 
 
 # ---- edge cases -------------------------------------------------------------------
@@ -226,13 +245,14 @@ def test_argument_errors_on_device():
     assert g.gemm_bf16(-1, 64, 64, p, 64, p, 64, C.data_ptr(), 64, 0, 1, 0, 1, s) == 1
 
 
-def test_plan_on_device_matches_closed_forms():
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_plan_on_device_matches_closed_forms(variant):
     from oracle import plan_forms as pf
     g = _lib()
     dev = g.gemm_device_desc_query(0)
-    kern = g.gemm_kernel_desc()
+    kern = g.gemm_kernel_desc(variant)
     assert kern.regs_per_thread > 0
-    st, plan = g.gemm_plan(4096, 4096, 4096)
+    st, plan = g.gemm_plan(4096, 4096, 4096, kernel_variant=variant)
     assert st == 0
     S = dev.num_sms
     b, _ = pf.ctas_per_sm(regs_per_thread=kern.regs_per_thread, threads=kern.threads_per_cta,
@@ -240,8 +260,11 @@ def test_plan_on_device_matches_closed_forms():
                           smem_per_sm=dev.smem_per_sm, smem_reserved_per_cta=dev.smem_reserved_per_cta,
                           max_threads_per_sm=dev.max_threads_per_sm, max_ctas_per_sm=dev.max_ctas_per_sm)
     assert plan.ctas_per_sm == b == 1 and plan.num_sms == S
-    assert plan.grid == pf.grid(4096, 4096, 128, 256)
-    assert math.isclose(plan.eta_wave, float(pf.eta_wave(plan.grid, S, b)), rel_tol=1e-15)
+    cs = kern.cluster_size
+    R = (min(kern.max_active_clusters, S * b // cs) if cs > 1 else S * b) * cs
+    assert plan.resident_ctas == R
+    assert plan.grid == pf.grid(4096, 4096, plan.tile_m, plan.tile_n) * cs
+    assert math.isclose(plan.eta_wave, float(pf.eta_wave(plan.grid, R, 1)), rel_tol=1e-15)
 
 
 # ---- the full-size workloads, on sampled entries ---------------------------------------
@@ -259,20 +282,22 @@ def sampled_check(oracle, A, Bt, M, N, K, C, out, n_random=6000, seed=0):
         assert ncanc <= max(8, got.size // 1000), f"{ncanc} entries needed the cancellation clause"
 
 
-def test_square4096_bf16_sampled(oracle_lib):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_square4096_bf16_sampled(oracle_lib, variant):
     M = N = K = 4096
     A, Bt = operands(M, N, K, "normal", True, SEED + 10)
-    C = run_gpu(A, Bt, M, N, K, torch.bfloat16)
+    C = run_gpu(A, Bt, M, N, K, torch.bfloat16, kernel_variant=variant)
     sampled_check(oracle_lib, A, Bt, M, N, K, C, "bf16")
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("shape", [(4095, 4096, 4096), (4097, 4096, 4096), (4096, 4096, 4088),
                                    (4096, 4104, 4096), (3968, 4096, 4096)])
-def test_neighbour_shapes_bf16_sampled(oracle_lib, shape):
+def test_neighbour_shapes_bf16_sampled(oracle_lib, shape, variant):
     M, N, K = shape
     A, Bt = operands(M, N, K, "normal", True, SEED + 11)
-    C = run_gpu(A, Bt, M, N, K, torch.bfloat16)
-    sampled_check(oracle_lib, A, Bt, M, N, K, C, "bf16")
+    C = run_gpu(A, Bt, M, N, K, torch.bfloat16, kernel_variant=variant)
+    sampled_check(oracle_lib, A, Bt, M, N, K, C, "bf16", seed=variant)
 
 
 def test_splitk_128x256x65536_all_splits(oracle_lib):
@@ -284,11 +309,13 @@ def test_splitk_128x256x65536_all_splits(oracle_lib):
     g = _lib()
     dA, dBt = to_dev(A), to_dev(Bt)
     for split in (1, 8, 32, 74, 148):
-        C1 = g.matmul(dA, dBt.t(), out_dtype=torch.float32, split_k=split).cpu().numpy()
-        C2 = g.matmul(dA, dBt.t(), out_dtype=torch.float32, split_k=split).cpu().numpy()
-        assert np.array_equal(C1, C2), f"split {split} not deterministic"
-        nbad, worst = check_f32(C1, ref, sabs)
-        assert nbad == 0, f"split {split}: {nbad} entries outside the bound (worst {worst:.3g})"
+        for variant in VARIANTS:
+            C1 = g.matmul(dA, dBt.t(), out_dtype=torch.float32, split_k=split, kernel_variant=variant)
+            C2 = g.matmul(dA, dBt.t(), out_dtype=torch.float32, split_k=split, kernel_variant=variant)
+            C1, C2 = C1.cpu().numpy(), C2.cpu().numpy()
+            assert np.array_equal(C1, C2), f"split {split} variant {variant} not deterministic"
+            nbad, worst = check_f32(C1, ref, sabs)
+            assert nbad == 0, f"split {split} variant {variant}: {nbad} entries outside the bound ({worst:.3g})"
     # the integer variant is exact for every split
     Ai, Bti = operands(M, N, 4096, "int4", False, SEED + 13)
     refi, _ = oracle_lib.gemm(Ai, Bti, M, N, 4096)
@@ -303,8 +330,10 @@ def test_large_16384x8192x8192_persistent_and_one_cta_per_tile(oracle_lib):
     A, Bt = operands(M, N, K, "normal", True, SEED + 14)
     g = _lib()
     dA, dBt = to_dev(A), to_dev(Bt)
-    C1 = g.matmul(dA, dBt.t(), out_dtype=torch.bfloat16)
-    C2 = g.matmul(dA, dBt.t(), out_dtype=torch.bfloat16, non_persistent=True)
-    assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))
-    del dA, dBt, C2
-    sampled_check(oracle_lib, A, Bt, M, N, K, from_dev_bf16(C1), "bf16", n_random=4000)
+    for variant in VARIANTS:
+        C1 = g.matmul(dA, dBt.t(), out_dtype=torch.bfloat16, kernel_variant=variant)
+        C2 = g.matmul(dA, dBt.t(), out_dtype=torch.bfloat16, non_persistent=True, kernel_variant=variant)
+        assert torch.equal(C1.view(torch.int16), C2.view(torch.int16)), f"variant {variant}"
+        del C2
+        sampled_check(oracle_lib, A, Bt, M, N, K, from_dev_bf16(C1), "bf16", n_random=3000, seed=variant)
+        del C1
