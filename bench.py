@@ -219,8 +219,12 @@ def run_gpu(args, wname: str, w: dict, cpu_baseline: bool):
     out_dtype = torch.bfloat16 if w["out"] == "bf16" else torch.float32
     (A_h, Bt_h), seed = make_host_operands(w)
 
+    kw = dict(split_k=w["split_k"], non_persistent=w.get("non_persistent", False), kernel_variant=args.variant,
+              no_stream_k=args.no_stream_k)
     st, plan = g.gemm_plan(M, N, K, g.GEMM_ROW_MAJOR, g.GEMM_COL_MAJOR,
-                           g.GEMM_OUT_BF16 if w["out"] == "bf16" else g.GEMM_OUT_F32, w["split_k"], args.variant)
+                           g.GEMM_OUT_BF16 if w["out"] == "bf16" else g.GEMM_OUT_F32,
+                           g.options(split_k=kw["split_k"], non_persistent=int(kw["non_persistent"]),
+                                     kernel_variant=kw["kernel_variant"], no_stream_k=int(kw["no_stream_k"])))
     if st:
         raise g.GemmError(st, "gemm_plan")
     if plan.workspace_bytes:
@@ -242,7 +246,6 @@ def run_gpu(args, wname: str, w: dict, cpu_baseline: bool):
         b = B0 if i == 0 else B0.clone()
         c = torch.empty((M, N), dtype=out_dtype, device="cuda")
         sets.append((a, b.t(), c))
-    kw = dict(split_k=w["split_k"], non_persistent=w.get("non_persistent", False), kernel_variant=args.variant)
     launches_per_step = 1 + (1 if plan.split_k > 1 else 0)
 
     def step(i, **extra):
@@ -316,6 +319,8 @@ def run_gpu(args, wname: str, w: dict, cpu_baseline: bool):
             "ctas_per_sm": plan.ctas_per_sm,
             "occupancy_limiter": g.LIMITERS[plan.occupancy_limiter],
             "eta_wave": round(plan.eta_wave, 5), "eta_pad": round(plan.eta_pad, 5),
+            "stream_k_tiles": plan.stream_k_tiles, "dp_tiles": plan.dp_tiles,
+            "eta_stream_k": round(plan.eta_stream_k, 5),
             "pct_of_peak": round(100.0 * value / world / peak, 2), "peak_tflops": peak, "peak_kind": peak_kind,
             "l2": f"inputs larger than L2: {copies} rotating operand sets of {set_bytes / 1e6:.1f} MB "
                   f"({copies * set_bytes / 1e6:.0f} MB) vs L2 {l2 / 1e6:.1f} MB",
@@ -441,6 +446,7 @@ def main(argv=None):
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="square4096")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-stream-k", action="store_true", help="never spread a tail of tiles over the clusters")
     ap.add_argument("--variant", type=int, default=0, choices=[0, 1, 2, 3],
                     help="kernel variant: 0 auto, 1 one-SM 128x256, 2 two-SM 256x256, 3 two-SM 256x128")
     ap.add_argument("--all-workloads", action="store_true",

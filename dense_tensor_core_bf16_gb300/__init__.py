@@ -25,7 +25,7 @@ __all__ = [
     "gemm_bf16", "gemm_bf16_ex", "gemm_plan", "gemm_plan_for_device", "gemm_occupancy",
     "gemm_device_desc_query", "gemm_kernel_desc", "gemm_reserve_workspace", "gemm_release_workspace",
     "gemm_get_device_status", "gemm_status_string", "gemm_limiter_string", "matmul", "lib", "header_functions",
-    "gemm_bf16_splitk_noalloc", "GEMM_NOALLOC_SCRATCH_FLOATS",
+    "gemm_bf16_splitk_noalloc", "GEMM_NOALLOC_SCRATCH_FLOATS", "options",
 ]
 
 GEMM_ROW_MAJOR, GEMM_COL_MAJOR = 0, 1
@@ -66,7 +66,8 @@ class gemm_plan_t(ctypes.Structure):
         [(n, ctypes.c_int64) for n in ("tiles", "grid", "launch_ctas", "m_padded", "n_padded", "k_padded")] + \
         [(n, ctypes.c_double) for n in ("eta_wave", "eta_pad", "flops")] + \
         [("smem_bytes", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64), ("tmem_cols", ctypes.c_int),
-         ("kernel_variant", ctypes.c_int), ("cluster_size", ctypes.c_int), ("resident_ctas", ctypes.c_int64)]
+         ("kernel_variant", ctypes.c_int), ("cluster_size", ctypes.c_int), ("resident_ctas", ctypes.c_int64),
+         ("stream_k_tiles", ctypes.c_int64), ("dp_tiles", ctypes.c_int64), ("eta_stream_k", ctypes.c_double)]
 
     def as_dict(self) -> dict:
         d = {n: getattr(self, n) for n, _ in self._fields_}
@@ -77,7 +78,7 @@ class gemm_plan_t(ctypes.Structure):
 class gemm_options_t(ctypes.Structure):
     _fields_ = [("split_k", ctypes.c_int), ("non_persistent", ctypes.c_int), ("raster_group_m", ctypes.c_int),
                 ("mainloop_done_event", ctypes.c_void_p), ("timeout_ms", ctypes.c_int),
-                ("debug_skip_load", ctypes.c_int), ("kernel_variant", ctypes.c_int)]
+                ("debug_skip_load", ctypes.c_int), ("kernel_variant", ctypes.c_int), ("no_stream_k", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -99,9 +100,9 @@ def lib() -> ctypes.CDLL:
         L.gemm_device_desc_query.argtypes = [i32, P(gemm_device_desc_t)]
         L.gemm_kernel_desc.argtypes = [i32, P(gemm_kernel_desc_t)]
         L.gemm_occupancy.argtypes = [P(gemm_kernel_desc_t), P(gemm_device_desc_t), P(i32), P(i32)]
-        L.gemm_plan_for_device.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32, i32, P(gemm_device_desc_t),
+        L.gemm_plan_for_device.argtypes = [i64, i64, i64, i32, i32, i32, P(gemm_options_t), P(gemm_device_desc_t),
                                            P(gemm_kernel_desc_t), P(gemm_plan_t)]
-        L.gemm_plan.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32, P(gemm_plan_t)]
+        L.gemm_plan.argtypes = [i64, i64, i64, i32, i32, i32, P(gemm_options_t), P(gemm_plan_t)]
         L.gemm_bf16.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, i32, i32, i32, vp]
         L.gemm_bf16_ex.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, i32, i32, P(gemm_options_t), vp]
         L.gemm_bf16_splitk_noalloc.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, i32, i32, i32, vp]
@@ -154,20 +155,27 @@ def gemm_occupancy(kern: gemm_kernel_desc_t, dev: gemm_device_desc_t):
     return st, b.value, LIMITERS.get(lim.value, "unknown")
 
 
-def gemm_plan_for_device(M, N, K, layout_a, layout_b, out_dtype, split_k, persistent, kernel_variant,
+def options(**kw) -> gemm_options_t:
+    """A gemm_options_t from keyword arguments (fields of the C struct)."""
+    return gemm_options_t(**kw)
+
+
+def gemm_plan_for_device(M, N, K, layout_a, layout_b, out_dtype, opts: gemm_options_t | None,
                          dev: gemm_device_desc_t, kern: gemm_kernel_desc_t):
     """(status, gemm_plan_t)."""
     plan = gemm_plan_t()
-    st = lib().gemm_plan_for_device(M, N, K, layout_a, layout_b, out_dtype, split_k, persistent, kernel_variant,
+    st = lib().gemm_plan_for_device(M, N, K, layout_a, layout_b, out_dtype,
+                                    ctypes.byref(opts) if opts is not None else None,
                                     ctypes.byref(dev), ctypes.byref(kern), ctypes.byref(plan))
     return st, plan
 
 
-def gemm_plan(M, N, K, layout_a=GEMM_ROW_MAJOR, layout_b=GEMM_COL_MAJOR, out_dtype=GEMM_OUT_BF16, split_k=0,
-              kernel_variant=0):
-    """(status, gemm_plan_t) on the current CUDA device."""
+def gemm_plan(M, N, K, layout_a=GEMM_ROW_MAJOR, layout_b=GEMM_COL_MAJOR, out_dtype=GEMM_OUT_BF16,
+              opts: gemm_options_t | None = None):
+    """(status, gemm_plan_t) on the current CUDA device, as gemm_bf16_ex would run it."""
     plan = gemm_plan_t()
-    st = lib().gemm_plan(M, N, K, layout_a, layout_b, out_dtype, split_k, kernel_variant, ctypes.byref(plan))
+    st = lib().gemm_plan(M, N, K, layout_a, layout_b, out_dtype,
+                         ctypes.byref(opts) if opts is not None else None, ctypes.byref(plan))
     return st, plan
 
 
@@ -233,7 +241,7 @@ def _stream_handle(stream):
 
 def matmul(A, B, *, out_dtype=None, out=None, split_k: int = 0, non_persistent: bool = False,
            raster_group_m: int = 0, stream=None, mainloop_done_event=None, timeout_ms: int = 0,
-           debug_skip_load: int = 0, kernel_variant: int = 0):
+           debug_skip_load: int = 0, kernel_variant: int = 0, no_stream_k: bool = False):
     """C = A @ B through ``gemm_bf16_ex``.
 
     ``A``: (M, K) torch.bfloat16 CUDA tensor, row-major (stride (lda, 1)).
@@ -271,7 +279,8 @@ def matmul(A, B, *, out_dtype=None, out=None, split_k: int = 0, non_persistent: 
     opts = gemm_options_t(split_k=split_k, non_persistent=int(non_persistent), raster_group_m=raster_group_m,
                           mainloop_done_event=(mainloop_done_event.cuda_event if mainloop_done_event is not None
                                                else None),
-                          timeout_ms=timeout_ms, debug_skip_load=debug_skip_load, kernel_variant=kernel_variant)
+                          timeout_ms=timeout_ms, debug_skip_load=debug_skip_load, kernel_variant=kernel_variant,
+                          no_stream_k=int(no_stream_k))
     st = gemm_bf16_ex(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc,
                       GEMM_ROW_MAJOR, GEMM_COL_MAJOR, odt, opts, _stream_handle(stream))
     if st:

@@ -38,7 +38,14 @@ namespace gemm {
 // Bit set of the pipeline waits that ran out of time (see gemm_get_device_status).
 __device__ unsigned int g_fault_word;
 
-enum : unsigned { SITE_PRODUCER = 1u, SITE_MMA_OPERANDS = 2u, SITE_MMA_ACC = 4u, SITE_EPI_ACC = 8u, SITE_DRAIN = 16u };
+enum : unsigned {
+    SITE_PRODUCER = 1u,
+    SITE_MMA_OPERANDS = 2u,
+    SITE_MMA_ACC = 4u,
+    SITE_EPI_ACC = 8u,
+    SITE_DRAIN = 16u,
+    SITE_FIXUP = 32u
+};
 
 struct KernelParams {
     int M, N, K;
@@ -53,6 +60,16 @@ struct KernelParams {
     int out_bf16;                // 1: bf16 stores, 0: fp32 stores
     unsigned long long timeout_ns;
     int skip_load;               // test hook (0 = off)
+    // Stream-K tail (sk_tiles > 0; split_k is then 1): tiles [0, dp_tiles) are
+    // computed whole, round robin over the clusters; the k-iterations of tiles
+    // [dp_tiles, tiles) are spread evenly over the clusters, which run them first.
+    int num_clusters;            // clusters launched (gridDim.x / CTA group)
+    int dp_tiles;
+    int sk_tiles;
+    long long sk_iters;          // sk_tiles * k_tiles
+    float *sk_partials;          // [num_clusters][tile rows][BN] fp32 partial tiles
+    unsigned int *sk_flags;      // [num_clusters][CTA group][4 epilogue warps]
+    unsigned int epoch;          // value the flags of this launch carry (never 0)
 };
 
 // Wait for the phase of `bar` with parity `parity`.  Gives up after
@@ -80,11 +97,18 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
     }
 }
 
+enum : int { KIND_FULL = 0, KIND_PARTIAL = 1, KIND_OWNER = 2 };
+
 struct Unit {
     int tm, tn;         // tile coordinates (in tiles)
     int split;          // K slice
     int kb_begin;       // first k-tile of the slice
     int kb_count;       // k-tiles in the slice (>= 1)
+    int kind;           // KIND_FULL: store C (or the split-K slice); stream-K only:
+                        // KIND_PARTIAL: a segment not starting at k = 0, stored to this
+                        // cluster's partial slot; KIND_OWNER: the k = 0 segment of a tile
+                        // whose later segments other clusters computed
+    int sk_tile;        // index of the tile in the stream-K region (stream-K units)
 };
 
 // Work unit u -> tile and K slice.  Tiles are visited in groups of group_m
@@ -106,8 +130,70 @@ __device__ __forceinline__ Unit decode_unit(long long u, const KernelParams &p) 
     const int rem = p.k_tiles - base * p.split_k;
     w.kb_count = base + (w.split < rem ? 1 : 0);
     w.kb_begin = w.split * base + min(w.split, rem);
+    w.kind = KIND_FULL;
+    w.sk_tile = -1;
     return w;
 }
+
+// Tile index -> tile coordinates, grouped raster (see decode_unit).
+__device__ __forceinline__ void tile_coords(long long tile, const KernelParams &p, int &tm, int &tn) {
+    const long long per_group = static_cast<long long>(p.group_m) * p.tiles_n;
+    const int group = static_cast<int>(tile / per_group);
+    const int first_m = group * p.group_m;
+    const int gsize = min(p.tiles_m - first_m, p.group_m);
+    const int r = static_cast<int>(tile - static_cast<long long>(group) * per_group);
+    tm = first_m + r % gsize;
+    tn = r / gsize;
+}
+
+// First stream-K iteration of cluster c: the sk_iters iterations are dealt out
+// in contiguous ranges, the first (sk_iters mod clusters) ranges one longer.
+__device__ __forceinline__ long long sk_range_start(const KernelParams &p, long long c) {
+    const long long base = p.sk_iters / p.num_clusters;
+    const long long rem = p.sk_iters - base * p.num_clusters;
+    return c * base + min(c, rem);
+}
+
+// The work of one cluster, in the order every role of its CTAs walks it:
+// its stream-K range (cut at tile boundaries), then its whole tiles.
+struct Schedule {
+    long long it, it_end;   // stream-K iterations still to do
+    long long u;            // next whole-tile (or split-K) unit
+    long long cluster;
+
+    __device__ __forceinline__ Schedule(const KernelParams &p, long long c) : u(c), cluster(c) {
+        if (p.sk_tiles > 0) {
+            it = sk_range_start(p, c);
+            it_end = sk_range_start(p, c + 1);
+        } else {
+            it = it_end = 0;
+        }
+    }
+
+    __device__ __forceinline__ bool next(const KernelParams &p, Unit &w) {
+        if (it < it_end) {
+            const long long t = it / p.k_tiles;
+            const int k0 = static_cast<int>(it - t * p.k_tiles);
+            const long long left = it_end - it;
+            const int k1 = static_cast<int>(min(static_cast<long long>(p.k_tiles), k0 + left));
+            tile_coords(p.dp_tiles + t, p, w.tm, w.tn);
+            w.split = 0;
+            w.kb_begin = k0;
+            w.kb_count = k1 - k0;
+            w.kind = k0 > 0 ? KIND_PARTIAL : (k1 < p.k_tiles ? KIND_OWNER : KIND_FULL);
+            w.sk_tile = static_cast<int>(t);
+            it += k1 - k0;
+            return true;
+        }
+        const long long units = p.sk_tiles > 0 ? p.dp_tiles : p.num_units;
+        if (u < units) {
+            w = decode_unit(u, p);
+            u += p.num_clusters;
+            return true;
+        }
+        return false;
+    }
+};
 
 __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_bits, uint32_t hi_bits) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(lo_bits), __uint_as_float(hi_bits));
@@ -146,6 +232,35 @@ __device__ __forceinline__ void store_row_chunk(const KernelParams &p, const Uni
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 if (col0 + j < p.N) dst[j] = __uint_as_float(r[j]);
+            }
+        }
+    }
+}
+
+// Stream-K flags: a release store of the launch's epoch after a partial is
+// written, and a bounded acquire spin for it on the reader's side.
+__device__ __forceinline__ void publish_flag(unsigned int *flag, unsigned int epoch) {
+    __threadfence();
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(epoch) : "memory");
+}
+
+__device__ __forceinline__ bool wait_flag(const unsigned int *flag, unsigned int epoch, volatile int *abort_flag,
+                                          unsigned long long timeout_ns) {
+    auto seen = [&]() {
+        unsigned int v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+        return v == epoch;
+    };
+    if (seen()) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (seen()) return true;
+        if ((i & 31u) == 0) {
+            if (*abort_flag) return false;
+            if (ptx::globaltimer_ns() - t0 > timeout_ns) {
+                *abort_flag = 1;
+                atomicOr(&g_fault_word, SITE_FIXUP);
+                return false;
             }
         }
     }
@@ -194,8 +309,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int lane = threadIdx.x & 31;
     const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;
     const bool leader = rank == 0;
-    const long long first_unit = blockIdx.x / CG;
-    const long long unit_stride = gridDim.x / CG;
+    const long long cluster = blockIdx.x / CG;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -237,8 +351,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) {
             uint32_t it = 0, issued = 0;
             bool ok = true;
-            for (long long u = first_unit; u < p.num_units && ok; u += unit_stride) {
-                const Unit w = decode_unit(u, p);
+            Schedule sched(p, cluster);
+            Unit w;
+            while (ok && sched.next(p, w)) {
                 const int row_a = w.tm * V.tile_m + static_cast<int>(rank) * CTA_ROWS;
                 const int row_b = w.tn * BN + static_cast<int>(rank) * V.b_rows;
                 for (int kb = 0; kb < w.kb_count; ++kb, ++it) {
@@ -283,8 +398,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0 && leader) {
             uint32_t it = 0, tc = 0;
             bool ok = true;
-            for (long long u = first_unit; u < p.num_units && ok; u += unit_stride, ++tc) {
-                const Unit w = decode_unit(u, p);
+            Schedule sched(p, cluster);
+            Unit w;
+            for (; ok && sched.next(p, w); ++tc) {
                 const uint32_t buf = tc & 1u;
                 const uint32_t use = tc >> 1;
                 if (!wait_phase<PAIR>(bar(BAR_ACC_EMPTY + buf), (use & 1u) ^ 1u, abort_flag, p.timeout_ns,
@@ -343,26 +459,109 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int quarter = warp & 3;            // TMEM lanes this warp may read: 32*quarter ..
         const int row_in_cta = quarter * 32 + lane;
         uint32_t tc = 0;
-        for (long long u = first_unit; u < p.num_units; u += unit_stride, ++tc) {
-            const Unit w = decode_unit(u, p);
+        Schedule sched(p, cluster);
+        Unit w;
+        for (; sched.next(p, w); ++tc) {
             const uint32_t buf = tc & 1u;
             const uint32_t use = tc >> 1;
             const bool ok =
                 wait_phase<PAIR>(bar(BAR_ACC_FULL + buf), use & 1u, abort_flag, p.timeout_ns, SITE_EPI_ACC, true);
             if (!__all_sync(0xffffffffu, ok)) break;
             ptx::tc_fence_after_sync();
-            const int row = w.tm * V.tile_m + static_cast<int>(rank) * CTA_ROWS + row_in_cta;
+            const int row_in_tile = static_cast<int>(rank) * CTA_ROWS + row_in_cta;
+            const int row = w.tm * V.tile_m + row_in_tile;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * BN;
             const int col_base = w.tn * BN;
+            const int flag_idx = static_cast<int>(rank) * EPI_WARPS + quarter;   // within a slot
+            // Stream-K owner: the other segments of this tile are the first
+            // units of the next clusters whose ranges start inside the tile;
+            // wait until each has published its partial for these 32 rows.
+            long long contrib_end = cluster + 1;
+            if (w.kind == KIND_OWNER) {
+                const long long tile_end = static_cast<long long>(w.sk_tile + 1) * p.k_tiles;
+                while (contrib_end < p.num_clusters && sk_range_start(p, contrib_end) < tile_end) ++contrib_end;
+                bool got = true;
+                for (long long c2 = cluster + 1; c2 < contrib_end && got; ++c2) {
+                    if (sk_range_start(p, c2 + 1) == sk_range_start(p, c2)) continue;   // empty range: no partial
+                    got = wait_flag(p.sk_flags + c2 * (CG * EPI_WARPS) + flag_idx, p.epoch, abort_flag,
+                                    p.timeout_ns);
+                }
+            }
+            // A partial slot holds a tile in warp-major order: for each
+            // (CTA, warp quarter, 32-column chunk, float4 v), the 32 lanes' float4s
+            // are consecutive, so every warp access moves 512 contiguous bytes.
+            // Lane l of the warp at (rank, quarter) owns row quarter*32 + l.
+            const long long slot_floats = static_cast<long long>(V.tile_m) * BN;
+            const int warp_chunk0 = (static_cast<int>(rank) * EPI_WARPS + quarter) * (BN / 32);
+            auto slot_ptr = [&](long long slot, int chunk) {
+                return reinterpret_cast<float4 *>(p.sk_partials + slot * slot_floats) +
+                       (static_cast<long long>(warp_chunk0 + chunk) * 8) * 32 + lane;
+            };
+            // stream-K owner: partial sums of the first contributor, one chunk ahead
+            float4 pre[8];
+            auto prefetch = [&](int chunk) {
+                const float4 *src = slot_ptr(cluster + 1, chunk);
+#pragma unroll
+                for (int v = 0; v < 8; ++v) pre[v] = __ldcg(src + v * 32);
+            };
+            const bool owner_fast = w.kind == KIND_OWNER && contrib_end == cluster + 2;   // the common case
+            if (owner_fast) prefetch(0);
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 const int col0 = col_base + c * 32;
-                if (col0 >= p.N) break;          // same for the whole warp
+                if (w.kind != KIND_PARTIAL && col0 >= p.N) break;   // same for the whole warp
                 uint32_t r[32];
                 __syncwarp();
                 ptx::tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r);
                 ptx::tmem_wait_ld();
+                if (w.kind == KIND_PARTIAL) {
+                    // the whole tile-row chunk, in range or not: the owner reads it back
+                    float4 *dst = slot_ptr(cluster, c);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        __stcg(dst + v * 32, make_float4(__uint_as_float(r[4 * v + 0]), __uint_as_float(r[4 * v + 1]),
+                                                         __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
+                    }
+                    continue;
+                }
+                if (w.kind == KIND_OWNER) {
+                    // add the later segments in k order
+                    if (owner_fast) {
+                        float4 q[8];
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) q[v] = pre[v];
+                        if (c + 1 < BN / 32 && col0 + 32 < p.N) prefetch(c + 1);
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            r[4 * v + 0] = __float_as_uint(__uint_as_float(r[4 * v + 0]) + q[v].x);
+                            r[4 * v + 1] = __float_as_uint(__uint_as_float(r[4 * v + 1]) + q[v].y);
+                            r[4 * v + 2] = __float_as_uint(__uint_as_float(r[4 * v + 2]) + q[v].z);
+                            r[4 * v + 3] = __float_as_uint(__uint_as_float(r[4 * v + 3]) + q[v].w);
+                        }
+                    } else {
+                        for (long long c2 = cluster + 1; c2 < contrib_end; ++c2) {
+                            if (sk_range_start(p, c2 + 1) == sk_range_start(p, c2)) continue;
+                            const float4 *src = slot_ptr(c2, c);
+                            float4 q[8];
+#pragma unroll
+                            for (int v = 0; v < 8; ++v) q[v] = __ldcg(src + v * 32);
+#pragma unroll
+                            for (int v = 0; v < 8; ++v) {
+                                r[4 * v + 0] = __float_as_uint(__uint_as_float(r[4 * v + 0]) + q[v].x);
+                                r[4 * v + 1] = __float_as_uint(__uint_as_float(r[4 * v + 1]) + q[v].y);
+                                r[4 * v + 2] = __float_as_uint(__uint_as_float(r[4 * v + 2]) + q[v].z);
+                                r[4 * v + 3] = __float_as_uint(__uint_as_float(r[4 * v + 3]) + q[v].w);
+                            }
+                        }
+                    }
+                }
                 if (row < p.M) store_row_chunk(p, w, row, col0, r);
+            }
+            if (w.kind == KIND_PARTIAL) {
+                // publish: every lane's stores, then one release of the flag
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) publish_flag(p.sk_flags + cluster * (CG * EPI_WARPS) + flag_idx, p.epoch);
             }
             ptx::tc_fence_before_sync();
             __syncwarp();
@@ -475,12 +674,16 @@ struct VariantState {
     int max_active_clusters = 0;   // 0 for single-CTA variants
 };
 
+constexpr int kMaxFlagSlots = 1024;   // clusters x CTAs x epilogue warps, bounds the stream-K flags
+
 struct DeviceState {
     bool ready = false;
     gemm_device_desc_t desc{};
     VariantState var[VARIANT_COUNT];
     float *workspace = nullptr;
     size_t workspace_bytes = 0;
+    unsigned int *sk_flags = nullptr;   // zeroed once; each launch writes its own epoch
+    unsigned int epoch = 0;
 };
 
 std::mutex g_mutex;
@@ -619,6 +822,30 @@ gemm_status_t ensure_workspace(DeviceState &ds, size_t bytes) {
     return GEMM_OK;
 }
 
+gemm_status_t ensure_flags(DeviceState &ds) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (ds.sk_flags) return GEMM_OK;
+    void *p = nullptr;
+    const size_t bytes = static_cast<size_t>(kMaxFlagSlots) * 4;
+    if (cudaMalloc(&p, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_OUT_OF_MEMORY;
+    }
+    if (cudaMemset(p, 0, bytes) != cudaSuccess) {
+        cudaFree(p);
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    ds.sk_flags = static_cast<unsigned int *>(p);
+    return GEMM_OK;
+}
+
+unsigned int next_epoch(DeviceState &ds) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (++ds.epoch == 0) ds.epoch = 1;   // 0 is the value of fresh flags
+    return ds.epoch;
+}
+
 gemm_status_t launch_fill_zero(int64_t M, int64_t N, void *C, int64_t ldc, int esize, int num_sms,
                                cudaStream_t stream) {
     const long long total = M * N;
@@ -665,11 +892,19 @@ gemm_status_t launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_
     const int variant = resolve_variant(o.kernel_variant);
     const VariantInfo vi = variant_info(variant);
     gemm_plan_t plan;
-    gemm_status_t st = make_plan(M, N, K, layout_a, layout_b, out_dtype, o.split_k, o.non_persistent ? 0 : 1, variant,
-                                 ds.desc, kernel_desc(variant, ds.var[variant]), &plan);
+    gemm_status_t st = make_plan(M, N, K, layout_a, layout_b, out_dtype, o, !pb.fixed, ds.desc,
+                                 kernel_desc(variant, ds.var[variant]), &plan);
     if (st != GEMM_OK) return st;
     const int64_t ldp = (N + 3) / 4 * 4;
+    const int64_t clusters = plan.launch_ctas / vi.cta_group;
     float *partials = nullptr;
+    if (plan.stream_k_tiles > 0) {
+        if (clusters * vi.cta_group * EPI_WARPS > kMaxFlagSlots) return GEMM_ERR_NOT_SUPPORTED;
+        st = ensure_flags(ds);
+        if (st != GEMM_OK) return st;
+        st = ensure_workspace(ds, static_cast<size_t>(plan.workspace_bytes));
+        if (st != GEMM_OK) return st;
+    }
     if (plan.split_k > 1) {
         if (pb.fixed) {
             const int64_t per_split = M * ldp;   // < 2^62: M, N < 2^31
@@ -712,6 +947,15 @@ gemm_status_t launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_
     const int timeout_ms = o.timeout_ms > 0 ? o.timeout_ms : DEFAULT_TIMEOUT_MS;
     p.timeout_ns = static_cast<unsigned long long>(timeout_ms) * 1000000ull;
     p.skip_load = o.debug_skip_load;
+    p.num_clusters = static_cast<int>(clusters);
+    p.dp_tiles = static_cast<int>(plan.dp_tiles);
+    p.sk_tiles = static_cast<int>(plan.stream_k_tiles);
+    p.sk_iters = plan.stream_k_tiles * plan.k_tiles;
+    if (plan.stream_k_tiles > 0) {
+        p.sk_partials = ds.workspace;
+        p.sk_flags = ds.sk_flags;
+        p.epoch = next_epoch(ds);
+    }
 
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(plan.launch_ctas));
@@ -784,17 +1028,19 @@ gemm_status_t gemm_kernel_desc(int kernel_variant, gemm_kernel_desc_t *kern) {
 }
 
 gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, gemm_layout_t layout_a, gemm_layout_t layout_b,
-                        gemm_dtype_t out_dtype, int split_k, int kernel_variant, gemm_plan_t *plan) {
+                        gemm_dtype_t out_dtype, const gemm_options_t *opts, gemm_plan_t *plan) {
     if (!plan) return GEMM_ERR_INVALID_VALUE;
-    gemm_status_t st = check_problem(M, N, K, layout_a, layout_b, out_dtype, split_k);
+    gemm_options_t o{};
+    if (opts) o = *opts;
+    gemm_status_t st = check_problem(M, N, K, layout_a, layout_b, out_dtype, o.split_k);
     if (st != GEMM_OK) return st;
-    if (kernel_variant < 0 || kernel_variant >= VARIANT_COUNT) return GEMM_ERR_INVALID_VALUE;
+    if (o.kernel_variant < 0 || o.kernel_variant >= VARIANT_COUNT) return GEMM_ERR_INVALID_VALUE;
     int device = 0;
     DeviceState *ds = nullptr;
     st = current_device(&device, &ds);
     if (st != GEMM_OK) return st;
-    const int v = resolve_variant(kernel_variant);
-    return make_plan(M, N, K, layout_a, layout_b, out_dtype, split_k, 1, v, ds->desc, kernel_desc(v, ds->var[v]), plan);
+    const int v = resolve_variant(o.kernel_variant);
+    return make_plan(M, N, K, layout_a, layout_b, out_dtype, o, true, ds->desc, kernel_desc(v, ds->var[v]), plan);
 }
 
 gemm_status_t gemm_bf16_ex(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,

@@ -86,16 +86,17 @@ int resolve_variant(int requested) {
 }
 
 gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_layout_t la, gemm_layout_t lb,
-                        gemm_dtype_t out, int split_k, int persistent, int variant,
+                        gemm_dtype_t out, const gemm_options_t &o, bool allow_stream_k,
                         const gemm_device_desc_t &dev, const gemm_kernel_desc_t &kern, gemm_plan_t *plan) {
-    gemm_status_t st = check_problem(M, N, K, la, lb, out, split_k);
+    gemm_status_t st = check_problem(M, N, K, la, lb, out, o.split_k);
     if (st != GEMM_OK) return st;
-    if (variant < 0 || variant >= VARIANT_COUNT) return GEMM_ERR_INVALID_VALUE;
+    if (o.kernel_variant < 0 || o.kernel_variant >= VARIANT_COUNT) return GEMM_ERR_INVALID_VALUE;
     if (dev.num_sms <= 0) return GEMM_ERR_INVALID_VALUE;
-    const int v = resolve_variant(variant);
+    const int v = resolve_variant(o.kernel_variant);
     const VariantInfo vi = variant_info(v);
     const int cs = kern.cluster_size > 0 ? kern.cluster_size : 1;
     if (cs != vi.cta_group) return GEMM_ERR_INVALID_VALUE;
+    const bool persistent = o.non_persistent == 0;
     std::memset(plan, 0, sizeof *plan);
     int b = 0, lim = 0;
     st = occupancy(kern, dev, &b, &lim);
@@ -120,12 +121,24 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_layout_t la, gemm_
     plan->ctas_per_sm = b;
     plan->occupancy_limiter = lim;
     plan->persistent = persistent ? 1 : 0;
-    plan->tiles = cdiv(M, vi.tile_m) * cdiv(N, vi.bn);
+    const int64_t T = cdiv(M, vi.tile_m) * cdiv(N, vi.bn);
+    plan->tiles = T;
     plan->k_tiles = (int)cdiv(K, TILE_K);
-    plan->split_k = (plan->tiles > 0) ? choose_split(plan->tiles, plan->k_tiles, (int)clusters, split_k) : 1;
+
+    // Stream-K tail: only with the plan's own choice of split, on a persistent
+    // grid (every cluster resident, as the hand-off between clusters needs).
+    int64_t sk_tiles = 0;
+    if (allow_stream_k && persistent && o.split_k == 0 && o.no_stream_k == 0 && plan->k_tiles >= 2 && T > 0 &&
+        T * 2 > clusters && T % clusters != 0) {
+        sk_tiles = T >= 2 * clusters ? clusters + T % clusters : T;
+    }
+    plan->stream_k_tiles = sk_tiles;
+    plan->dp_tiles = T - sk_tiles;
+    plan->split_k = (T > 0 && sk_tiles == 0) ? choose_split(T, plan->k_tiles, (int)clusters, o.split_k) : 1;
     plan->k_tiles_per_split = plan->k_tiles > 0 ? (int)cdiv(plan->k_tiles, plan->split_k) : 0;
-    plan->grid = plan->tiles * plan->split_k * cs;
+    plan->grid = T * plan->split_k * cs;
     plan->launch_ctas = persistent ? (plan->grid < resident ? plan->grid : resident) : plan->grid;
+    if (sk_tiles > 0) plan->launch_ctas = resident;   // every cluster takes a share of the tail
     plan->m_padded = cdiv(M, vi.tile_m) * vi.tile_m;
     plan->n_padded = cdiv(N, vi.bn) * vi.bn;
     plan->k_padded = cdiv(K, TILE_K) * TILE_K;
@@ -133,13 +146,22 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_layout_t la, gemm_
         const int64_t waves = cdiv(plan->grid, resident);
         plan->eta_wave = (double)plan->grid / ((double)waves * (double)resident);
     }
+    if (sk_tiles > 0) {
+        const double ideal = (double)T * plan->k_tiles / (double)clusters;
+        const int64_t worst = cdiv(plan->dp_tiles, clusters) * plan->k_tiles + cdiv(sk_tiles * plan->k_tiles, clusters);
+        plan->eta_stream_k = ideal / (double)worst;
+    }
     if (M > 0 && N > 0 && K > 0) {
         plan->eta_pad = ((double)M / plan->m_padded) * ((double)N / plan->n_padded) * ((double)K / plan->k_padded);
     }
     plan->flops = 2.0 * (double)M * (double)N * (double)K;
     plan->smem_bytes = vi.smem;
     plan->tmem_cols = vi.tmem_cols;
-    plan->workspace_bytes = plan->split_k > 1 ? (int64_t)plan->split_k * M * ((N + 3) / 4 * 4) * 4 : 0;
+    if (plan->split_k > 1) {
+        plan->workspace_bytes = (int64_t)plan->split_k * M * ((N + 3) / 4 * 4) * 4;
+    } else if (sk_tiles > 0) {
+        plan->workspace_bytes = clusters * (int64_t)vi.tile_m * vi.bn * 4;
+    }
     return GEMM_OK;
 }
 
@@ -154,11 +176,12 @@ gemm_status_t gemm_occupancy(const gemm_kernel_desc_t *kern, const gemm_device_d
 }
 
 gemm_status_t gemm_plan_for_device(int64_t M, int64_t N, int64_t K, gemm_layout_t layout_a, gemm_layout_t layout_b,
-                                   gemm_dtype_t out_dtype, int split_k, int persistent, int kernel_variant,
-                                   const gemm_device_desc_t *dev, const gemm_kernel_desc_t *kern, gemm_plan_t *plan) {
+                                   gemm_dtype_t out_dtype, const gemm_options_t *opts, const gemm_device_desc_t *dev,
+                                   const gemm_kernel_desc_t *kern, gemm_plan_t *plan) {
     if (!dev || !kern || !plan) return GEMM_ERR_INVALID_VALUE;
-    return gemm::make_plan(M, N, K, layout_a, layout_b, out_dtype, split_k, persistent, kernel_variant, *dev, *kern,
-                           plan);
+    gemm_options_t o{};
+    if (opts) o = *opts;
+    return gemm::make_plan(M, N, K, layout_a, layout_b, out_dtype, o, true, *dev, *kern, plan);
 }
 
 const char *gemm_status_string(gemm_status_t s) {

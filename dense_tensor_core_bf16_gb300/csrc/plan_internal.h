@@ -7,8 +7,9 @@ namespace gemm {
 gemm_status_t check_problem(int64_t M, int64_t N, int64_t K, gemm_layout_t la, gemm_layout_t lb,
                             gemm_dtype_t out, int split_k);
 gemm_status_t occupancy(const gemm_kernel_desc_t &k, const gemm_device_desc_t &d, int *b, int *limiter);
+// allow_stream_k: false for callers without a growable workspace.
 gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_layout_t la, gemm_layout_t lb,
-                        gemm_dtype_t out, int split_k, int persistent, int variant,
+                        gemm_dtype_t out, const gemm_options_t &o, bool allow_stream_k,
                         const gemm_device_desc_t &dev, const gemm_kernel_desc_t &kern, gemm_plan_t *plan);
 int resolve_variant(int requested);
 int choose_split(int64_t tiles, int k_tiles, int capacity, int requested);

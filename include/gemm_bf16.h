@@ -148,6 +148,10 @@ typedef struct {
     int kernel_variant;          /* gemm_kernel_variant_t actually used */
     int cluster_size;            /* CTAs per tile */
     int64_t resident_ctas;       /* S b: CTAs resident at once */
+    int64_t stream_k_tiles;      /* tiles whose k-iterations are spread over all clusters (0: none) */
+    int64_t dp_tiles;            /* tiles computed whole, one cluster each */
+    double eta_stream_k;         /* with a stream-K tail: ideal / actual per-cluster work
+                                    (tiles*k_tiles/clusters over the largest share); 0 without */
 } gemm_plan_t;
 
 /* Options of gemm_bf16_ex.  Zero-initialise and set what you need. */
@@ -163,6 +167,7 @@ typedef struct {
                                     CTA 0) unissued, so its consumer's wait runs out and the call
                                     ends with GEMM_ERR_DEVICE_TIMEOUT on the device */
     int kernel_variant;          /* gemm_kernel_variant_t; 0 = the plan chooses */
+    int no_stream_k;             /* 1: never spread a tail of tiles over the clusters (stream-K) */
 } gemm_options_t;
 
 /* Fill `dev` with the facts of CUDA device `device`. */
@@ -179,21 +184,32 @@ gemm_status_t gemm_kernel_desc(int kernel_variant, gemm_kernel_desc_t *kern);
 gemm_status_t gemm_occupancy(const gemm_kernel_desc_t *kern, const gemm_device_desc_t *dev,
                              int *ctas_per_sm, int *limiter);
 
-/* Plan a GEMM for explicit device and kernel facts; host arithmetic only, no
- * CUDA call.  Same argument rules as gemm_bf16 for the sizes, layouts and
- * out dtype.  `kern` describes the footprint of `kernel_variant` (an explicit
- * variant; GEMM_KERNEL_AUTO resolves to the default variant). */
+/*
+ * Plan a GEMM for explicit device and kernel facts; host arithmetic only, no
+ * CUDA call.  Same argument rules as gemm_bf16_ex (opts may be NULL); `kern`
+ * describes the footprint of the variant opts selects (GEMM_KERNEL_AUTO
+ * resolves to the default variant).
+ *
+ * Work decomposition, in order:
+ *   - split_k > 1: split-K as asked (clamped to the k-tile count);
+ *   - split_k = 0 and the tiles fill at most half of the resident clusters:
+ *     split-K chosen by the plan;
+ *   - split_k = 0, a persistent launch, stream-K not disabled, and the tile
+ *     count T not a multiple of the resident clusters C: a stream-K tail --
+ *     the last C + (T mod C) tiles (all T when T < 2C) have their k-iterations
+ *     dealt out evenly over the C clusters, the rest are computed whole;
+ *   - otherwise one cluster per tile.
+ */
 gemm_status_t gemm_plan_for_device(int64_t M, int64_t N, int64_t K,
                                    gemm_layout_t layout_a, gemm_layout_t layout_b,
-                                   gemm_dtype_t out_dtype, int split_k, int persistent,
-                                   int kernel_variant, const gemm_device_desc_t *dev,
+                                   gemm_dtype_t out_dtype, const gemm_options_t *opts,
+                                   const gemm_device_desc_t *dev,
                                    const gemm_kernel_desc_t *kern, gemm_plan_t *plan);
 
-/* Plan a GEMM on the current CUDA device with one of this library's kernel
- * variants (GEMM_KERNEL_AUTO: the one gemm_bf16 would use). */
+/* Plan a GEMM on the current CUDA device exactly as gemm_bf16_ex would run it. */
 gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K,
                         gemm_layout_t layout_a, gemm_layout_t layout_b,
-                        gemm_dtype_t out_dtype, int split_k, int kernel_variant, gemm_plan_t *plan);
+                        gemm_dtype_t out_dtype, const gemm_options_t *opts, gemm_plan_t *plan);
 
 /*
  * C = A . B on `stream`.
@@ -260,7 +276,11 @@ gemm_status_t gemm_bf16_splitk_noalloc(int64_t M, int64_t N, int64_t K,
                                        gemm_dtype_t out_dtype, int split_k, void *stream);
 
 /* gemm_bf16 with options (launch mode, raster group, timing event, device
- * time limit).  opts == NULL behaves as gemm_bf16 with split_k = 0. */
+ * time limit, kernel variant, stream-K).  opts == NULL behaves as gemm_bf16
+ * with split_k = 0.  A stream-K tail keeps fp32 partial tiles in the library's
+ * workspace and hands them between the resident clusters of one launch
+ * through flags in device memory; like split-K, calls that share the
+ * workspace must not overlap in time. */
 gemm_status_t gemm_bf16_ex(int64_t M, int64_t N, int64_t K,
                            const void *A, int64_t lda, const void *B, int64_t ldb,
                            void *C, int64_t ldc,

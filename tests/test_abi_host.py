@@ -70,9 +70,10 @@ def kern(variant, regs=64, max_active_clusters=0):
     return k
 
 
-def _plan(M, N, K, split=1, persistent=1, d=None, regs=64, out=g.GEMM_OUT_BF16, variant=1, mac=0):
-    st, p = g.gemm_plan_for_device(M, N, K, g.GEMM_ROW_MAJOR, g.GEMM_COL_MAJOR, out, split, persistent, variant,
-                                   d or dev(), kern(variant, regs, mac))
+def _plan(M, N, K, split=1, persistent=1, d=None, regs=64, out=g.GEMM_OUT_BF16, variant=1, mac=0, no_sk=0):
+    o = g.options(split_k=split, non_persistent=0 if persistent else 1, kernel_variant=variant, no_stream_k=no_sk)
+    st, p = g.gemm_plan_for_device(M, N, K, g.GEMM_ROW_MAJOR, g.GEMM_COL_MAJOR, out, o, d or dev(),
+                                   kern(variant, regs, mac))
     assert st == 0
     return p
 
@@ -170,10 +171,49 @@ def test_plan_split_k_clamped_and_auto():
 
 
 def test_plan_auto_variant_is_the_pair_kernel():
-    st, p = g.gemm_plan_for_device(4096, 4096, 4096, 0, 1, 1, 0, 1, 0, dev(), kern(2))
+    st, p = g.gemm_plan_for_device(4096, 4096, 4096, 0, 1, 1, None, dev(), kern(2))
     assert st == 0 and p.kernel_variant == 2
-    st, _ = g.gemm_plan_for_device(4096, 4096, 4096, 0, 1, 1, 0, 1, 0, dev(), kern(1))
+    st, _ = g.gemm_plan_for_device(4096, 4096, 4096, 0, 1, 1, None, dev(), kern(1))
     assert st == 1     # a footprint that does not match the variant
+
+
+@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("shape", WORKLOADS + [(4096, 4096, 8192), (2560, 4096, 4096), (1000, 9000, 3000)])
+def test_plan_stream_k_tail(shape, variant):
+    """With the plan's own split on a persistent grid: T tiles on C clusters;
+    a tail of C + (T mod C) tiles (all T if T < 2C) is spread over the
+    clusters when T mod C != 0 and T > C/2; the largest per-cluster share is
+    ceil(dp/C) whole tiles plus ceil(sk k-iterations / C)."""
+    M, N, K = shape
+    tm, tn, cs = TILES[variant]
+    p = _plan(M, N, K, split=0, variant=variant)
+    C = 152 // cs
+    T = pf.grid(M, N, tm, tn)
+    KB = math.ceil(K / 64)
+    want_sk = 0
+    if KB >= 2 and 2 * T > C and T % C:
+        want_sk = C + T % C if T >= 2 * C else T
+    assert p.stream_k_tiles == want_sk and p.dp_tiles == T - want_sk
+    if want_sk:
+        assert p.split_k == 1 and p.launch_ctas == C * cs
+        worst = math.ceil((T - want_sk) / C) * KB + math.ceil(want_sk * KB / C)
+        assert p.eta_stream_k == pytest.approx(T * KB / C / worst, rel=1e-12)
+        assert p.workspace_bytes == C * tm * tn * 4
+    else:
+        assert p.eta_stream_k == 0
+    # off on request, and never on a one-CTA-per-tile grid or with an explicit split
+    assert _plan(M, N, K, split=0, variant=variant, no_sk=1).stream_k_tiles == 0
+    assert _plan(M, N, K, split=0, variant=variant, persistent=0).stream_k_tiles == 0
+    assert _plan(M, N, K, split=1, variant=variant).stream_k_tiles == 0
+
+
+def test_plan_stream_k_hand_values():
+    """4096^3 on 76 pairs of 256x256 tiles: T = 256, 256 mod 76 = 28, a tail
+    of 104 tiles (6656 k-iterations, 87.6 per cluster) after 152 whole tiles;
+    the largest share is 2 x 64 + 88 = 216 k-iterations of an ideal 215.58."""
+    p = _plan(4096, 4096, 4096, split=0, variant=2)
+    assert (p.tiles, p.stream_k_tiles, p.dp_tiles) == (256, 104, 152)
+    assert p.eta_stream_k == pytest.approx((256 * 64 / 76) / 216, rel=1e-12)
 
 
 def _call(M, N, K, A=16, lda=64, B=16, ldb=64, C=16, ldc=64, la=0, lb=1, out=0, split=1):
@@ -211,12 +251,13 @@ def test_plan_argument_checks():
     k = kern(1)
     plan = g.gemm_plan_t()
     L = g.lib()
-    assert L.gemm_plan_for_device(4, 4, 4, 0, 1, 0, 0, 1, 1, None, ctypes.byref(k), ctypes.byref(plan)) == 1
-    st, _ = g.gemm_plan_for_device(4, 4, 4, 1, 1, 0, 0, 1, 1, dev(), k)
+    assert L.gemm_plan_for_device(4, 4, 4, 0, 1, 0, None, None, ctypes.byref(k), ctypes.byref(plan)) == 1
+    o1 = g.options(kernel_variant=1)
+    st, _ = g.gemm_plan_for_device(4, 4, 4, 1, 1, 0, o1, dev(), k)
     assert st == 3
-    st, _ = g.gemm_plan_for_device(4, 4, 4, 0, 1, 0, 0, 1, 7, dev(), k)
+    st, _ = g.gemm_plan_for_device(4, 4, 4, 0, 1, 0, g.options(kernel_variant=7), dev(), k)
     assert st == 1
     too_big = kern(1)
     too_big.smem_per_cta = 240000
-    st, _ = g.gemm_plan_for_device(4, 4, 4, 0, 1, 0, 0, 1, 1, dev(), too_big)
+    st, _ = g.gemm_plan_for_device(4, 4, 4, 0, 1, 0, o1, dev(), too_big)
     assert st == 1

@@ -170,6 +170,33 @@ def test_non_persistent_matches_persistent_bitwise(oracle_lib, variant):
     assert check_f32(C1, ref, sabs)[0] == 0
 
 
+# shapes for the stream-K tail (C = 76 resident pairs, 152 single CTAs):
+#  v2 1792x1536x2048: 7x6 = 42 tiles, all spread (32 k-tiles over ~18-iteration shares: 2-3 clusters per tile)
+#  v2 3328x3072x512: 13x12 = 156 tiles = 76 whole + a tail of 80
+#  v1 1280x2048x2048: 10x8 = 80 tiles on 152 CTAs, all spread
+#  v1/v2/v3 1800x1500x2000: ragged in every dimension
+SK_CASES = [(2, (1792, 1536, 2048)), (2, (3328, 3072, 512)), (1, (1280, 2048, 2048)),
+            (1, (1800, 1500, 2000)), (2, (1800, 1500, 2000)), (3, (1800, 1500, 2000))]
+
+
+@pytest.mark.parametrize("variant,shape", SK_CASES)
+def test_stream_k_tail(oracle_lib, variant, shape):
+    g = _lib()
+    M, N, K = shape
+    st, plan = g.gemm_plan(M, N, K, opts=g.options(kernel_variant=variant))
+    assert st == 0 and plan.stream_k_tiles > 0, "shape chosen to exercise the stream-K tail"
+    A, Bt = operands(M, N, K, "normal", True, SEED + 20)
+    C1 = full_check(oracle_lib, A, Bt, M, N, K, torch.float32, kernel_variant=variant)
+    C2 = run_gpu(A, Bt, M, N, K, torch.float32, kernel_variant=variant)
+    assert np.array_equal(C1, C2), "stream-K result differs run to run"
+    full_check(oracle_lib, A, Bt, M, N, K, torch.bfloat16, kernel_variant=variant)
+    # exact on small integers, like the whole-tile path
+    Ai, Bti = operands(M, N, K, "int4", False, SEED + 21)
+    Ce = full_check(oracle_lib, Ai, Bti, M, N, K, torch.float32, exact=True, kernel_variant=variant)
+    Cd = run_gpu(Ai, Bti, M, N, K, torch.float32, kernel_variant=variant, no_stream_k=True)
+    assert np.array_equal(Ce, Cd)
+
+
 def test_variants_agree_bitwise_on_integers(oracle_lib):
     """Every variant gives the exact product on small-integer inputs, so all
     three agree bit for bit."""
@@ -252,7 +279,7 @@ def test_plan_on_device_matches_closed_forms(variant):
     dev = g.gemm_device_desc_query(0)
     kern = g.gemm_kernel_desc(variant)
     assert kern.regs_per_thread > 0
-    st, plan = g.gemm_plan(4096, 4096, 4096, kernel_variant=variant)
+    st, plan = g.gemm_plan(4096, 4096, 4096, opts=g.options(split_k=1, kernel_variant=variant))
     assert st == 0
     S = dev.num_sms
     b, _ = pf.ctas_per_sm(regs_per_thread=kern.regs_per_thread, threads=kern.threads_per_cta,
@@ -331,9 +358,23 @@ def test_large_16384x8192x8192_persistent_and_one_cta_per_tile(oracle_lib):
     g = _lib()
     dA, dBt = to_dev(A), to_dev(Bt)
     for variant in VARIANTS:
-        C1 = g.matmul(dA, dBt.t(), out_dtype=torch.bfloat16, kernel_variant=variant)
+        # one CTA (pair) per tile and a persistent grid over whole tiles sum in
+        # the same order: bit-identical
         C2 = g.matmul(dA, dBt.t(), out_dtype=torch.bfloat16, non_persistent=True, kernel_variant=variant)
-        assert torch.equal(C1.view(torch.int16), C2.view(torch.int16)), f"variant {variant}"
+        C3 = g.matmul(dA, dBt.t(), out_dtype=torch.bfloat16, no_stream_k=True, kernel_variant=variant)
+        assert torch.equal(C3.view(torch.int16), C2.view(torch.int16)), f"variant {variant}"
+        del C3
+        sampled_check(oracle_lib, A, Bt, M, N, K, from_dev_bf16(C2), "bf16", n_random=2000, seed=variant)
         del C2
-        sampled_check(oracle_lib, A, Bt, M, N, K, from_dev_bf16(C1), "bf16", n_random=3000, seed=variant)
+        # the default persistent launch adds a stream-K tail (tiles mod clusters != 0)
+        st, plan = g.gemm_plan(M, N, K, opts=g.options(kernel_variant=variant))
+        assert st == 0 and plan.stream_k_tiles > 0
+        C1 = g.matmul(dA, dBt.t(), out_dtype=torch.bfloat16, kernel_variant=variant)
+        sampled_check(oracle_lib, A, Bt, M, N, K, from_dev_bf16(C1), "bf16", n_random=3000, seed=10 + variant)
+        # and every row of the last tile row, where the tail tiles lie
+        rows = np.repeat(np.arange(M - plan.tile_m, M, 7), 16)
+        cols = np.tile(np.linspace(0, N - 1, 16).astype(np.int64), rows.size // 16)
+        ref, sabs = oracle_lib.gemm_entries(A, Bt, M, N, K, rows, cols)
+        nbad, _, _, detail = check_bf16(from_dev_bf16(C1)[rows, cols], ref, sabs, oracle_lib)
+        assert nbad == 0, detail
         del C1
