@@ -345,6 +345,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+    // Everything above overlaps the tail of the previous kernel in the stream;
+    // no global memory (operands, C, workspace, flags) is touched before it
+    // has finished.
+    ptx::grid_dependency_wait();
+    ptx::grid_launch_dependents();
 
     if (warp == 0) {
         // ---------------- producer: TMA copies into the ring ----------------
@@ -962,11 +967,14 @@ gemm_status_t launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_
     cfg.blockDim = dim3(NUM_THREADS);
     cfg.dynamicSmemBytes = vi.smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr = cluster_attr(vi.cta_group);
-    if (vi.cta_group > 1) {
-        cfg.attrs = &attr;
-        cfg.numAttrs = 1;
-    }
+    // Programmatic stream serialisation: this launch may begin while the
+    // previous kernel in the stream finishes (see grid_dependency_wait).
+    cudaLaunchAttribute attrs[2];
+    attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[0].val.programmaticStreamSerializationAllowed = 1;
+    attrs[1] = cluster_attr(vi.cta_group);
+    cfg.attrs = attrs;
+    cfg.numAttrs = vi.cta_group > 1 ? 2 : 1;
     if (cudaLaunchKernelEx(&cfg, kernel_fn(variant), tmap_a, tmap_b, p) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;

@@ -73,6 +73,17 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
+// ---- programmatic dependent launch ---------------------------------------------
+
+// Block until every grid this one depends on (the previous kernel in the
+// stream, when launched with programmatic stream serialisation) has completed
+// and its memory operations are visible; a no-op without such a dependency.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next grid in the stream to begin launching (its CTAs still need
+// free SMs, and wait in grid_dependency_wait() for this grid to finish).
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // ---- clusters ------------------------------------------------------------------
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
