@@ -275,6 +275,8 @@ def run_gpu(args, wname: str, w: dict, cpu_baseline: bool):
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)] if two_kernels else None
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)] if two_kernels else None
     mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)] if two_kernels else None
+    for ev in mids or []:
+        ev.record(stream)   # torch creates the CUDA event on its first record; the library records it again
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()

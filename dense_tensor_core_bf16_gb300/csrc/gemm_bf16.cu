@@ -894,7 +894,7 @@ gemm_status_t launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_
                           void *C, int64_t ldc, gemm_layout_t layout_a, gemm_layout_t layout_b,
                           gemm_dtype_t out_dtype, const gemm_options_t &o, cudaStream_t s, DeviceState &ds,
                           const PartialBuffer &pb) {
-    const int variant = resolve_variant(o.kernel_variant);
+    const int variant = choose_variant(M, N, K, o.kernel_variant, ds.desc);
     const VariantInfo vi = variant_info(variant);
     gemm_plan_t plan;
     gemm_status_t st = make_plan(M, N, K, layout_a, layout_b, out_dtype, o, !pb.fixed, ds.desc,
@@ -1047,7 +1047,7 @@ gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, gemm_layout_t layout_a,
     DeviceState *ds = nullptr;
     st = current_device(&device, &ds);
     if (st != GEMM_OK) return st;
-    const int v = resolve_variant(o.kernel_variant);
+    const int v = choose_variant(M, N, K, o.kernel_variant, ds->desc);
     return make_plan(M, N, K, layout_a, layout_b, out_dtype, o, true, ds->desc, kernel_desc(v, ds->var[v]), plan);
 }
 

@@ -85,6 +85,22 @@ int resolve_variant(int requested) {
     return requested;
 }
 
+// The automatic choice between the single-CTA 128x256 and the pair 256x256
+// kernels: both spend the same time on one k-tile of one tile, so compare the
+// k-tiles each resident cluster would run with the work spread evenly,
+// ceil(T * k_tiles / C) -- T tiles, C = S single CTAs or S/2 pairs -- and
+// give the pair kernel the advantage it shows at equal work (its tensor
+// pipes stay about 7 % busier: half the B traffic per SM, a deeper ring).
+int choose_variant(int64_t M, int64_t N, int64_t K, int requested, const gemm_device_desc_t &dev) {
+    if (requested != VARIANT_AUTO) return requested;
+    const int64_t kb = cdiv(K, TILE_K) > 0 ? cdiv(K, TILE_K) : 1;
+    const int64_t c1 = dev.num_sms > 0 ? dev.num_sms : 1;
+    const int64_t c2 = dev.num_sms / 2 > 0 ? dev.num_sms / 2 : 1;
+    const int64_t w1 = cdiv(cdiv(M, 128) * cdiv(N, 256) * kb, c1);
+    const int64_t w2 = cdiv(cdiv(M, 256) * cdiv(N, 256) * kb, c2);
+    return w1 * 100 < w2 * 93 ? VARIANT_1SM_128x256 : VARIANT_2SM_256x256;
+}
+
 gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_layout_t la, gemm_layout_t lb,
                         gemm_dtype_t out, const gemm_options_t &o, bool allow_stream_k,
                         const gemm_device_desc_t &dev, const gemm_kernel_desc_t &kern, gemm_plan_t *plan) {
@@ -92,7 +108,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_layout_t la, gemm_
     if (st != GEMM_OK) return st;
     if (o.kernel_variant < 0 || o.kernel_variant >= VARIANT_COUNT) return GEMM_ERR_INVALID_VALUE;
     if (dev.num_sms <= 0) return GEMM_ERR_INVALID_VALUE;
-    const int v = resolve_variant(o.kernel_variant);
+    const int v = choose_variant(M, N, K, o.kernel_variant, dev);
     const VariantInfo vi = variant_info(v);
     const int cs = kern.cluster_size > 0 ? kern.cluster_size : 1;
     if (cs != vi.cta_group) return GEMM_ERR_INVALID_VALUE;

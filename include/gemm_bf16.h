@@ -68,7 +68,11 @@ typedef enum {
  *     tile, tcgen05.mma.cta_group::2 with M = 256; each CTA stages its own
  *     128 rows of A and half of the tile's columns of B, and holds its 128
  *     rows of the accumulator.
- * GEMM_KERNEL_AUTO lets the plan choose. */
+ * GEMM_KERNEL_AUTO lets the plan choose: both kernels spend the same time
+ * on one k-tile of one tile, so it compares the k-tiles per resident cluster
+ * with the work spread evenly, ceil(T k_tiles / C) (C = S single CTAs or S/2
+ * pairs), and takes the single-CTA kernel only when that is under 93 % of
+ * the pair kernel's (which keeps its tensor pipes about 7 % busier). */
 typedef enum {
     GEMM_KERNEL_AUTO = 0,
     GEMM_KERNEL_1SM_128x256 = 1,

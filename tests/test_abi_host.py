@@ -170,11 +170,19 @@ def test_plan_split_k_clamped_and_auto():
     assert p.split_k == 1
 
 
-def test_plan_auto_variant_is_the_pair_kernel():
+def test_plan_auto_variant():
+    """Equal balanced work (4096^3: 216 k-tiles per cluster either way) goes to
+    the pair kernel; M = 128 with a long K goes to the single-CTA kernel
+    (ceil(1024/152) = 7 k-tiles per CTA against ceil(1024/76) = 14 per pair)."""
     st, p = g.gemm_plan_for_device(4096, 4096, 4096, 0, 1, 1, None, dev(), kern(2))
     assert st == 0 and p.kernel_variant == 2
     st, _ = g.gemm_plan_for_device(4096, 4096, 4096, 0, 1, 1, None, dev(), kern(1))
     assert st == 1     # a footprint that does not match the variant
+    st, p = g.gemm_plan_for_device(128, 256, 65536, 0, 1, 0, None, dev(), kern(1))
+    assert st == 0 and p.kernel_variant == 1 and p.split_k == 152
+    for shape in [(16384, 8192, 8192), (4097, 4096, 4096), (3968, 4096, 4096), (256, 256, 256)]:
+        st, p = g.gemm_plan_for_device(*shape, 0, 1, 1, None, dev(), kern(2))
+        assert st == 0 and p.kernel_variant == 2, shape
 
 
 @pytest.mark.parametrize("variant", [1, 2])
