@@ -54,9 +54,8 @@ struct KernelParams {
     int split_k;
     int group_m;                 // m-tiles per raster group
     long long num_units;         // tiles * split_k
-    void *out;                   // C, or the fp32 partial buffer when split_k > 1
-    long long ld_out;            // leading dimension of `out`, elements
-    long long split_stride;      // elements between consecutive partial slices
+    void *out;                   // C
+    long long ld_out;            // leading dimension of C, elements
     int out_bf16;                // 1: bf16 stores, 0: fp32 stores
     unsigned long long timeout_ns;
     int skip_load;               // test hook (0 = off)
@@ -67,7 +66,10 @@ struct KernelParams {
     int dp_tiles;
     int sk_tiles;
     long long sk_iters;          // sk_tiles * k_tiles
-    float *sk_partials;          // [num_clusters][tile rows][BN] fp32 partial tiles
+    // fp32 partial tiles, one slot of tile rows x BN each: with split-K,
+    // [split][tile] (slot split * tiles + tile); with a stream-K tail, one
+    // slot per cluster.  Slots are laid out warp-major (see the epilogue).
+    float *partials;
     unsigned int *sk_flags;      // [num_clusters][CTA group][4 epilogue warps]
     unsigned int epoch;          // value the flags of this launch carry (never 0)
 };
@@ -219,8 +221,7 @@ __device__ __forceinline__ void store_row_chunk(const KernelParams &p, const Uni
             }
         }
     } else {
-        float *dst = static_cast<float *>(p.out) + static_cast<long long>(w.split) * p.split_stride +
-                     static_cast<long long>(row) * p.ld_out + col0;
+        float *dst = static_cast<float *>(p.out) + static_cast<long long>(row) * p.ld_out + col0;
         if (col0 + 32 <= p.N) {
             float4 *d4 = reinterpret_cast<float4 *>(dst);
 #pragma unroll
@@ -499,9 +500,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const long long slot_floats = static_cast<long long>(V.tile_m) * BN;
             const int warp_chunk0 = (static_cast<int>(rank) * EPI_WARPS + quarter) * (BN / 32);
             auto slot_ptr = [&](long long slot, int chunk) {
-                return reinterpret_cast<float4 *>(p.sk_partials + slot * slot_floats) +
+                return reinterpret_cast<float4 *>(p.partials + slot * slot_floats) +
                        (static_cast<long long>(warp_chunk0 + chunk) * 8) * 32 + lane;
             };
+            // where this unit's partial tile goes: its split-K slot, or (stream-K)
+            // this cluster's slot
+            const bool to_slot = w.kind == KIND_PARTIAL || p.split_k > 1;
+            const long long my_slot =
+                p.split_k > 1 ? static_cast<long long>(w.split) * p.tiles_m * p.tiles_n +
+                                    static_cast<long long>(w.tm) * p.tiles_n + w.tn
+                              : cluster;
             // stream-K owner: partial sums of the first contributor, one chunk ahead
             float4 pre[8];
             auto prefetch = [&](int chunk) {
@@ -514,14 +522,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 const int col0 = col_base + c * 32;
-                if (w.kind != KIND_PARTIAL && col0 >= p.N) break;   // same for the whole warp
+                if (!to_slot && col0 >= p.N) break;   // same for the whole warp
                 uint32_t r[32];
                 __syncwarp();
                 ptx::tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r);
                 ptx::tmem_wait_ld();
-                if (w.kind == KIND_PARTIAL) {
-                    // the whole tile-row chunk, in range or not: the owner reads it back
-                    float4 *dst = slot_ptr(cluster, c);
+                if (to_slot) {
+                    // the whole tile-row chunk, in range or not: a reader takes it back
+                    float4 *dst = slot_ptr(my_slot, c);
 #pragma unroll
                     for (int v = 0; v < 8; ++v) {
                         __stcg(dst + v * 32, make_float4(__uint_as_float(r[4 * v + 0]), __uint_as_float(r[4 * v + 1]),
@@ -598,48 +606,99 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
-// C[m][n] = sum over s = 0, 1, ..., split-1 of P[s][m][n], in that order, then
-// cast to the output type.  One thread per 4 consecutive columns of a row.
-__global__ void __launch_bounds__(256)
-    splitk_combine_kernel(const float *__restrict__ part, long long ldp, long long split_stride, int split, int M,
-                          int N, void *C, long long ldc, int out_bf16) {
-    const long long n4 = (N + 3) / 4;
-    const long long total = static_cast<long long>(M) * n4;
-    for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
-         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const int m = static_cast<int>(idx / n4);
-        const int col = static_cast<int>(idx - static_cast<long long>(m) * n4) * 4;
-        const float *src = part + static_cast<long long>(m) * ldp + col;
-        float4 acc = __ldcs(reinterpret_cast<const float4 *>(src));
-#pragma unroll 8
-        for (int s = 1; s < split; ++s) {
-            const float4 v = __ldcs(reinterpret_cast<const float4 *>(src + s * split_stride));
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
-        }
-        const float a[4] = {acc.x, acc.y, acc.z, acc.w};
-        if (out_bf16) {
-            __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(C) + static_cast<long long>(m) * ldc + col;
-            if (col + 4 <= N) {
-                const __nv_bfloat162 lo = __floats2bfloat162_rn(a[0], a[1]);
-                const __nv_bfloat162 hi = __floats2bfloat162_rn(a[2], a[3]);
-                uint2 v;
-                v.x = *reinterpret_cast<const uint32_t *>(&lo);
-                v.y = *reinterpret_cast<const uint32_t *>(&hi);
-                *reinterpret_cast<uint2 *>(dst) = v;
-            } else {
-                for (int j = 0; j < 4 && col + j < N; ++j) dst[j] = __float2bfloat16_rn(a[j]);
+// C[m][n] = the sum over the split slices s = 0 .. split-1 of slice s's
+// partial tile, in a fixed order, then cast to the output type.  Partial
+// slots are warp-major (as the GEMM epilogue writes them): float4 q of a slot
+// holds row wq*32 + lane, columns chunk*32 + 4v .. +3, where
+// q = ((wq*(bn/32) + chunk)*8 + v)*32 + lane.
+// A CTA of 8 warps takes 32 consecutive float4s of the slots (one per lane);
+// warp w adds slices w, w+8, w+16, ... in increasing order (16 loads in
+// flight), and warp 0 then adds the 8 warp sums in order w = 0 .. 7.  The
+// order is the same on every run.
+constexpr int COMBINE_WARPS = 8;
+
+__global__ void __launch_bounds__(COMBINE_WARPS * 32)
+    splitk_combine_kernel(const float *__restrict__ part, int split, long long tiles, int tiles_n, int tile_m, int bn,
+                          int M, int N, void *C, long long ldc, int out_bf16) {
+    __shared__ float4 warp_sum[COMBINE_WARPS][32];
+    ptx::grid_dependency_wait();   // the partials come from the previous kernel in the stream
+    ptx::grid_launch_dependents();
+    const long long slot_f4 = static_cast<long long>(tile_m) * bn / 4;
+    const long long split_f4 = tiles * slot_f4;
+    const int chunks = bn / 32;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const float4 *P = reinterpret_cast<const float4 *>(part);
+    for (long long base = blockIdx.x * 32LL; base < split_f4; base += gridDim.x * 32LL) {
+        const long long idx = base + lane;
+        const bool live = idx < split_f4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (live) {
+            const float4 *src = P + idx;
+            int s = warp;
+            for (; s + 15 * COMBINE_WARPS < split; s += 16 * COMBINE_WARPS) {
+                float4 w[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) w[j] = __ldcs(src + static_cast<long long>(s + j * COMBINE_WARPS) * split_f4);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    acc.x += w[j].x;
+                    acc.y += w[j].y;
+                    acc.z += w[j].z;
+                    acc.w += w[j].w;
+                }
             }
-        } else {
-            float *dst = static_cast<float *>(C) + static_cast<long long>(m) * ldc + col;
-            if (col + 4 <= N) {
-                *reinterpret_cast<float4 *>(dst) = acc;
-            } else {
-                for (int j = 0; j < 4 && col + j < N; ++j) dst[j] = a[j];
+            for (; s < split; s += COMBINE_WARPS) {
+                const float4 w1 = __ldcs(src + static_cast<long long>(s) * split_f4);
+                acc.x += w1.x;
+                acc.y += w1.y;
+                acc.z += w1.z;
+                acc.w += w1.w;
             }
         }
+        warp_sum[warp][lane] = acc;
+        __syncthreads();
+        if (warp == 0 && live) {
+            float4 t = warp_sum[0][lane];
+            for (int w2 = 1; w2 < COMBINE_WARPS && w2 < split; ++w2) {
+                const float4 u = warp_sum[w2][lane];
+                t.x += u.x;
+                t.y += u.y;
+                t.z += u.z;
+                t.w += u.w;
+            }
+            const long long tile = idx / slot_f4;
+            const int q = static_cast<int>(idx - tile * slot_f4);
+            const int v = (q >> 5) & 7;
+            const int chunk = (q >> 8) % chunks;
+            const int wq = (q >> 8) / chunks;
+            const int row = static_cast<int>(tile / tiles_n) * tile_m + wq * 32 + lane;
+            const int col = static_cast<int>(tile % tiles_n) * bn + chunk * 32 + v * 4;
+            if (row < M && col < N) {
+                const float a[4] = {t.x, t.y, t.z, t.w};
+                if (out_bf16) {
+                    __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(C) + static_cast<long long>(row) * ldc + col;
+                    if (col + 4 <= N) {
+                        const __nv_bfloat162 lo = __floats2bfloat162_rn(a[0], a[1]);
+                        const __nv_bfloat162 hi = __floats2bfloat162_rn(a[2], a[3]);
+                        uint2 u2;
+                        u2.x = *reinterpret_cast<const uint32_t *>(&lo);
+                        u2.y = *reinterpret_cast<const uint32_t *>(&hi);
+                        *reinterpret_cast<uint2 *>(dst) = u2;
+                    } else {
+                        for (int j = 0; j < 4 && col + j < N; ++j) dst[j] = __float2bfloat16_rn(a[j]);
+                    }
+                } else {
+                    float *dst = static_cast<float *>(C) + static_cast<long long>(row) * ldc + col;
+                    if (col + 4 <= N) {
+                        *reinterpret_cast<float4 *>(dst) = t;
+                    } else {
+                        for (int j = 0; j < 4 && col + j < N; ++j) dst[j] = a[j];
+                    }
+                }
+            }
+        }
+        __syncthreads();
     }
 }
 
@@ -894,13 +953,12 @@ gemm_status_t launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_
                           void *C, int64_t ldc, gemm_layout_t layout_a, gemm_layout_t layout_b,
                           gemm_dtype_t out_dtype, const gemm_options_t &o, cudaStream_t s, DeviceState &ds,
                           const PartialBuffer &pb) {
-    const int variant = choose_variant(M, N, K, o.kernel_variant, ds.desc);
+    const int variant = choose_variant(M, N, K, o.kernel_variant, o.split_k, ds.desc);
     const VariantInfo vi = variant_info(variant);
     gemm_plan_t plan;
     gemm_status_t st = make_plan(M, N, K, layout_a, layout_b, out_dtype, o, !pb.fixed, ds.desc,
                                  kernel_desc(variant, ds.var[variant]), &plan);
     if (st != GEMM_OK) return st;
-    const int64_t ldp = (N + 3) / 4 * 4;
     const int64_t clusters = plan.launch_ctas / vi.cta_group;
     float *partials = nullptr;
     if (plan.stream_k_tiles > 0) {
@@ -912,7 +970,7 @@ gemm_status_t launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_
     }
     if (plan.split_k > 1) {
         if (pb.fixed) {
-            const int64_t per_split = M * ldp;   // < 2^62: M, N < 2^31
+            const int64_t per_split = plan.tiles * vi.tile_m * vi.bn;   // padded tiles; < 2^62
             if (per_split > pb.floats || plan.split_k > pb.floats / per_split) return GEMM_ERR_INVALID_VALUE;
             partials = pb.ptr;
         } else {
@@ -938,17 +996,10 @@ gemm_status_t launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_
     p.split_k = plan.split_k;
     p.group_m = o.raster_group_m > 0 ? o.raster_group_m : DEFAULT_RASTER_GROUP_M;
     p.num_units = plan.tiles * plan.split_k;
-    if (plan.split_k > 1) {
-        p.out = partials;
-        p.ld_out = ldp;
-        p.split_stride = M * ldp;
-        p.out_bf16 = 0;
-    } else {
-        p.out = C;
-        p.ld_out = ldc;
-        p.split_stride = 0;
-        p.out_bf16 = out_dtype == GEMM_OUT_BF16 ? 1 : 0;
-    }
+    p.out = C;
+    p.ld_out = ldc;
+    p.out_bf16 = out_dtype == GEMM_OUT_BF16 ? 1 : 0;
+    p.partials = partials;
     const int timeout_ms = o.timeout_ms > 0 ? o.timeout_ms : DEFAULT_TIMEOUT_MS;
     p.timeout_ns = static_cast<unsigned long long>(timeout_ms) * 1000000ull;
     p.skip_load = o.debug_skip_load;
@@ -957,7 +1008,7 @@ gemm_status_t launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_
     p.sk_tiles = static_cast<int>(plan.stream_k_tiles);
     p.sk_iters = plan.stream_k_tiles * plan.k_tiles;
     if (plan.stream_k_tiles > 0) {
-        p.sk_partials = ds.workspace;
+        p.partials = ds.workspace;
         p.sk_flags = ds.sk_flags;
         p.epoch = next_epoch(ds);
     }
@@ -982,17 +1033,22 @@ gemm_status_t launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_
     if (o.mainloop_done_event && cudaEventRecord(static_cast<cudaEvent_t>(o.mainloop_done_event), s) != cudaSuccess)
         return GEMM_ERR_LAUNCH;
     if (plan.split_k > 1) {
-        const long long total = M * ((N + 3) / 4);
-        long long blocks = (total + 255) / 256;
-        const long long cap = 4LL * ds.desc.num_sms;
+        const long long total = plan.tiles * vi.tile_m * vi.bn / 4;   // float4s per slice
+        long long blocks = (total + 31) / 32;
+        const long long cap = 8LL * ds.desc.num_sms;
         if (blocks > cap) blocks = cap;
         cudaLaunchConfig_t cc{};
         cc.gridDim = dim3(static_cast<unsigned>(blocks));
-        cc.blockDim = dim3(256);
+        cc.blockDim = dim3(COMBINE_WARPS * 32);
         cc.stream = s;
-        if (cudaLaunchKernelEx(&cc, splitk_combine_kernel, static_cast<const float *>(partials),
-                               static_cast<long long>(ldp), static_cast<long long>(M * ldp), plan.split_k,
-                               static_cast<int>(M), static_cast<int>(N), C, static_cast<long long>(ldc),
+        cudaLaunchAttribute pdl{};
+        pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        pdl.val.programmaticStreamSerializationAllowed = 1;
+        cc.attrs = &pdl;
+        cc.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cc, splitk_combine_kernel, static_cast<const float *>(partials), plan.split_k,
+                               static_cast<long long>(plan.tiles), p.tiles_n, vi.tile_m, vi.bn, static_cast<int>(M),
+                               static_cast<int>(N), C, static_cast<long long>(ldc),
                                out_dtype == GEMM_OUT_BF16 ? 1 : 0) != cudaSuccess) {
             cudaGetLastError();
             return GEMM_ERR_LAUNCH;
@@ -1047,7 +1103,7 @@ gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, gemm_layout_t layout_a,
     DeviceState *ds = nullptr;
     st = current_device(&device, &ds);
     if (st != GEMM_OK) return st;
-    const int v = choose_variant(M, N, K, o.kernel_variant, ds->desc);
+    const int v = choose_variant(M, N, K, o.kernel_variant, o.split_k, ds->desc);
     return make_plan(M, N, K, layout_a, layout_b, out_dtype, o, true, ds->desc, kernel_desc(v, ds->var[v]), plan);
 }
 

@@ -91,13 +91,21 @@ int resolve_variant(int requested) {
 // ceil(T * k_tiles / C) -- T tiles, C = S single CTAs or S/2 pairs -- and
 // give the pair kernel the advantage it shows at equal work (its tensor
 // pipes stay about 7 % busier: half the B traffic per SM, a deeper ring).
-int choose_variant(int64_t M, int64_t N, int64_t K, int requested, const gemm_device_desc_t &dev) {
+int choose_variant(int64_t M, int64_t N, int64_t K, int requested, int split_k, const gemm_device_desc_t &dev) {
     if (requested != VARIANT_AUTO) return requested;
     const int64_t kb = cdiv(K, TILE_K) > 0 ? cdiv(K, TILE_K) : 1;
     const int64_t c1 = dev.num_sms > 0 ? dev.num_sms : 1;
     const int64_t c2 = dev.num_sms / 2 > 0 ? dev.num_sms / 2 : 1;
-    const int64_t w1 = cdiv(cdiv(M, 128) * cdiv(N, 256) * kb, c1);
-    const int64_t w2 = cdiv(cdiv(M, 256) * cdiv(N, 256) * kb, c2);
+    const int64_t t1 = cdiv(M, 128) * cdiv(N, 256), t2 = cdiv(M, 256) * cdiv(N, 256);
+    int64_t w1, w2;
+    if (split_k > 1) {   // a given split: rounds of work units times k-tiles per unit
+        const int64_t s = split_k < kb ? split_k : kb;
+        w1 = cdiv(t1 * s, c1) * cdiv(kb, s);
+        w2 = cdiv(t2 * s, c2) * cdiv(kb, s);
+    } else {
+        w1 = cdiv(t1 * kb, c1);
+        w2 = cdiv(t2 * kb, c2);
+    }
     return w1 * 100 < w2 * 93 ? VARIANT_1SM_128x256 : VARIANT_2SM_256x256;
 }
 
@@ -108,7 +116,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_layout_t la, gemm_
     if (st != GEMM_OK) return st;
     if (o.kernel_variant < 0 || o.kernel_variant >= VARIANT_COUNT) return GEMM_ERR_INVALID_VALUE;
     if (dev.num_sms <= 0) return GEMM_ERR_INVALID_VALUE;
-    const int v = choose_variant(M, N, K, o.kernel_variant, dev);
+    const int v = choose_variant(M, N, K, o.kernel_variant, o.split_k, dev);
     const VariantInfo vi = variant_info(v);
     const int cs = kern.cluster_size > 0 ? kern.cluster_size : 1;
     if (cs != vi.cta_group) return GEMM_ERR_INVALID_VALUE;
@@ -174,7 +182,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_layout_t la, gemm_
     plan->smem_bytes = vi.smem;
     plan->tmem_cols = vi.tmem_cols;
     if (plan->split_k > 1) {
-        plan->workspace_bytes = (int64_t)plan->split_k * M * ((N + 3) / 4 * 4) * 4;
+        plan->workspace_bytes = (int64_t)plan->split_k * T * vi.tile_m * vi.bn * 4;
     } else if (sk_tiles > 0) {
         plan->workspace_bytes = clusters * (int64_t)vi.tile_m * vi.bn * 4;
     }

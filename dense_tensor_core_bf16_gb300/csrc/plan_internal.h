@@ -12,7 +12,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_layout_t la, gemm_
                         gemm_dtype_t out, const gemm_options_t &o, bool allow_stream_k,
                         const gemm_device_desc_t &dev, const gemm_kernel_desc_t &kern, gemm_plan_t *plan);
 int resolve_variant(int requested);
-int choose_variant(int64_t M, int64_t N, int64_t K, int requested, const gemm_device_desc_t &dev);
+int choose_variant(int64_t M, int64_t N, int64_t K, int requested, int split_k, const gemm_device_desc_t &dev);
 int choose_split(int64_t tiles, int k_tiles, int capacity, int requested);
 
 }  // namespace gemm

@@ -147,7 +147,8 @@ typedef struct {
     double eta_pad;
     double flops;                /* 2 M N K */
     int64_t smem_bytes;          /* dynamic shared memory per CTA of the main kernel */
-    int64_t workspace_bytes;     /* split-K partial buffer: split_k * M * round_up(N, 4) * 4 */
+    int64_t workspace_bytes;     /* fp32 partial tiles: split-K, split_k * tiles * tile_m * tile_n * 4;
+                                    stream-K tail, one tile per resident cluster */
     int tmem_cols;               /* tensor-memory columns per CTA */
     int kernel_variant;          /* gemm_kernel_variant_t actually used */
     int cluster_size;            /* CTAs per tile */
@@ -259,9 +260,11 @@ gemm_status_t gemm_bf16(int64_t M, int64_t N, int64_t K,
  *
  * Arguments, layouts, alignment rules and results are those of gemm_bf16.
  * The split actually used (split_k, or the plan's choice when split_k is 0)
- * must satisfy  split * M * round_up(N, 4) <= GEMM_NOALLOC_SCRATCH_FLOATS;
- * otherwise the call returns GEMM_ERR_INVALID_VALUE and launches nothing.
- * split_k = 1 uses no scratch at all.
+ * must satisfy  split * tiles * tile_m * tile_n <= GEMM_NOALLOC_SCRATCH_FLOATS
+ * (the plan's workspace_bytes / 4; with 128 x 256 tiles and M, N multiples
+ * of them that is split * M * N); otherwise the call returns
+ * GEMM_ERR_INVALID_VALUE and launches nothing.  split_k = 1 uses no scratch
+ * at all, and this entry point never uses a stream-K tail.
  *
  * The first call on a device looks up the array's address on that device
  * (cudaGetSymbolAddress); make that first call before any stream capture.
