@@ -202,42 +202,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_bits, uint32_t hi_bi
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-// Store 32 consecutive fp32 accumulator values of one row, columns col0..col0+31.
-__device__ __forceinline__ void store_row_chunk(const KernelParams &p, const Unit &w, int row, int col0,
-                                                const uint32_t (&r)[32]) {
-    if (p.out_bf16) {
-        __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.out) + static_cast<long long>(row) * p.ld_out + col0;
-        if (col0 + 32 <= p.N) {
-            uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                d4[v] = make_uint4(pack_bf16x2(r[8 * v + 0], r[8 * v + 1]), pack_bf16x2(r[8 * v + 2], r[8 * v + 3]),
-                                   pack_bf16x2(r[8 * v + 4], r[8 * v + 5]), pack_bf16x2(r[8 * v + 6], r[8 * v + 7]));
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                if (col0 + j < p.N) dst[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
-            }
-        }
-    } else {
-        float *dst = static_cast<float *>(p.out) + static_cast<long long>(row) * p.ld_out + col0;
-        if (col0 + 32 <= p.N) {
-            float4 *d4 = reinterpret_cast<float4 *>(dst);
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-                d4[v] = make_float4(__uint_as_float(r[4 * v + 0]), __uint_as_float(r[4 * v + 1]),
-                                    __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                if (col0 + j < p.N) dst[j] = __uint_as_float(r[j]);
-            }
-        }
-    }
-}
-
 // Stream-K flags: a release store of the launch's epoch after a partial is
 // written, and a bounded acquire spin for it on the reader's side.
 __device__ __forceinline__ void publish_flag(unsigned int *flag, unsigned int epoch) {
@@ -279,7 +243,7 @@ __device__ __forceinline__ bool wait_flag(const unsigned int *flag, unsigned int
 template <int CG, int BN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                     const KernelParams p) {
+                     const __grid_constant__ CUtensorMap tmap_c, const KernelParams p) {
     constexpr VariantInfo V = make_variant(CG, BN);
     constexpr int STAGES = V.stages;
     constexpr int BAR_FULL = 0;                           // [STAGES] operands landed (leader's count both CTAs)
@@ -300,7 +264,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
     const uint32_t sA = ptx::smem_addr(smem);                      // STAGES A tiles
     const uint32_t sB = sA + STAGES * V.a_stage;                   // STAGES B tiles
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * V.stage);
+    const uint32_t sEpi = sA + STAGES * V.stage;                   // epilogue staging (1024-aligned)
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * V.stage + EPI_STAGING_BYTES);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NUM_BARRIERS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     const uint32_t bar0 = ptx::smem_addr(bars);
@@ -328,6 +293,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tensormap(&tmap_a);
         ptx::prefetch_tensormap(&tmap_b);
+        ptx::prefetch_tensormap(&tmap_c);
     }
     if (warp == 1) {
         if constexpr (PAIR) {
@@ -463,7 +429,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else {
         // ---------------- epilogue: TMEM -> registers -> global ---------------
         const int quarter = warp & 3;            // TMEM lanes this warp may read: 32*quarter ..
-        const int row_in_cta = quarter * 32 + lane;
+        // This warp's two staging buffers for TMA stores of C.  A 32 x 32 chunk
+        // is staged row per lane, with the 16-byte pieces of each row permuted
+        // the way the tensor map's swizzle reads them (bf16: 64-byte rows,
+        // piece ^ ((row >> 1) & 3); fp32: 128-byte rows, piece ^ (row & 7)),
+        // which also keeps the 32 lanes' writes free of bank conflicts.
+        const uint32_t epi_buf0 = sEpi + static_cast<uint32_t>(quarter) * 2u * EPI_BUF_BYTES;
+        uint32_t stores_issued = 0;
         uint32_t tc = 0;
         Schedule sched(p, cluster);
         Unit w;
@@ -474,8 +446,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 wait_phase<PAIR>(bar(BAR_ACC_FULL + buf), use & 1u, abort_flag, p.timeout_ns, SITE_EPI_ACC, true);
             if (!__all_sync(0xffffffffu, ok)) break;
             ptx::tc_fence_after_sync();
-            const int row_in_tile = static_cast<int>(rank) * CTA_ROWS + row_in_cta;
-            const int row = w.tm * V.tile_m + row_in_tile;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * BN;
             const int col_base = w.tn * BN;
             const int flag_idx = static_cast<int>(rank) * EPI_WARPS + quarter;   // within a slot
@@ -568,7 +538,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         }
                     }
                 }
-                if (row < p.M) store_row_chunk(p, w, row, col0, r);
+                // stage the chunk and hand it to TMA (which clips rows >= M, cols >= N)
+                const int warp_row0 = w.tm * V.tile_m + static_cast<int>(rank) * CTA_ROWS + quarter * 32;
+                if (warp_row0 < p.M) {
+                    if (stores_issued >= 2 && lane == 0) ptx::bulk_wait_group_read<1>();   // this buffer read out
+                    __syncwarp();
+                    const uint32_t buf = epi_buf0 + (stores_issued & 1u) * EPI_BUF_BYTES;
+                    if (p.out_bf16) {
+                        const uint32_t row_base = buf + static_cast<uint32_t>(lane) * 64u;
+                        const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            ptx::st_shared_v4(row_base + ((static_cast<uint32_t>(v) ^ sw) << 4),
+                                              pack_bf16x2(r[8 * v + 0], r[8 * v + 1]), pack_bf16x2(r[8 * v + 2], r[8 * v + 3]),
+                                              pack_bf16x2(r[8 * v + 4], r[8 * v + 5]), pack_bf16x2(r[8 * v + 6], r[8 * v + 7]));
+                        }
+                    } else {
+                        const uint32_t row_base = buf + static_cast<uint32_t>(lane) * 128u;
+                        const uint32_t sw = static_cast<uint32_t>(lane) & 7u;
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            ptx::st_shared_v4(row_base + ((static_cast<uint32_t>(v) ^ sw) << 4), r[4 * v + 0], r[4 * v + 1],
+                                              r[4 * v + 2], r[4 * v + 3]);
+                        }
+                    }
+                    ptx::fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::tma_store_2d(&tmap_c, buf, col0, warp_row0);
+                        ptx::bulk_commit_group();
+                    }
+                    ++stores_issued;
+                }
             }
             if (w.kind == KIND_PARTIAL) {
                 // publish: every lane's stores, then one release of the flag
@@ -588,6 +589,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     }
 
+    if (warp >= 2 && lane == 0) ptx::bulk_wait_group_all();   // C written before the CTA ends
     __syncwarp();
     ptx::tc_fence_before_sync();
     if constexpr (PAIR) {
@@ -723,7 +725,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
-using KernelFn = void (*)(CUtensorMap, CUtensorMap, KernelParams);
+using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, KernelParams);
 
 KernelFn kernel_fn(int variant) {
     switch (variant) {
@@ -867,6 +869,22 @@ gemm_status_t encode_operand(CUtensorMap *map, const void *ptr, int64_t k, int64
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_LAUNCH;
 }
 
+// C (row-major, `rows` x `cols`, `ld` apart) as 32 x 32 boxes for the
+// epilogue's TMA stores, swizzled as the epilogue stages them: bf16 rows are
+// 64 bytes (64-byte swizzle), fp32 rows 128 bytes (128-byte swizzle).
+gemm_status_t encode_output(CUtensorMap *map, void *ptr, int64_t cols, int64_t rows, int64_t ld, bool bf16) {
+    const int esize = bf16 ? 2 : 4;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * esize};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t elem_strides[2] = {1, 1};
+    CUresult r = g_encode_tiled(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr,
+                                dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                bf16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_LAUNCH;
+}
+
 gemm_status_t ensure_workspace(DeviceState &ds, size_t bytes) {
     std::lock_guard<std::mutex> lock(g_mutex);
     if (ds.workspace_bytes >= bytes) return GEMM_OK;
@@ -980,10 +998,12 @@ gemm_status_t launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_
         }
     }
 
-    CUtensorMap tmap_a, tmap_b;
+    CUtensorMap tmap_a, tmap_b, tmap_c;
     st = encode_operand(&tmap_a, A, K, M, lda, CTA_ROWS);
     if (st != GEMM_OK) return st;
     st = encode_operand(&tmap_b, B, K, N, ldb, vi.b_rows);
+    if (st != GEMM_OK) return st;
+    st = encode_output(&tmap_c, C, N, M, ldc, out_dtype == GEMM_OUT_BF16);
     if (st != GEMM_OK) return st;
 
     KernelParams p{};
@@ -1026,7 +1046,7 @@ gemm_status_t launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_
     attrs[1] = cluster_attr(vi.cta_group);
     cfg.attrs = attrs;
     cfg.numAttrs = vi.cta_group > 1 ? 2 : 1;
-    if (cudaLaunchKernelEx(&cfg, kernel_fn(variant), tmap_a, tmap_b, p) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, kernel_fn(variant), tmap_a, tmap_b, tmap_c, p) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
     }

@@ -30,6 +30,10 @@ constexpr int EPI_WARPS = 4;
 constexpr int NUM_BARRIERS_FIXED = 2 * ACC_BUFS + 1;   // + 2 per stage
 constexpr int SMEM_LIMIT = 232448;        // opt-in dynamic shared memory per CTA on sm_100-class parts
 constexpr int MAX_STAGES = 8;
+// Epilogue staging: per epilogue warp, two buffers of one 32 x 32 chunk of C
+// (fp32 at most: 4 KiB), which TMA stores to global memory.
+constexpr int EPI_BUF_BYTES = 4096;
+constexpr int EPI_STAGING_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;
 
 enum Variant : int {
     VARIANT_AUTO = 0,
@@ -59,10 +63,10 @@ GEMM_HD constexpr VariantInfo make_variant(int cg, int bn) {
     const int b = (bn / cg) * TILE_K * 2;
     const int st = a + b;
     const int fixed = 1024 + (NUM_BARRIERS_FIXED + 2 * MAX_STAGES) * 8 + 16;
-    int stages = (SMEM_LIMIT - fixed) / st;
+    int stages = (SMEM_LIMIT - fixed - EPI_STAGING_BYTES) / st;
     if (stages > MAX_STAGES) stages = MAX_STAGES;
     return VariantInfo{cg, bn, CTA_ROWS * cg, bn / cg, a, b, st, stages,
-                       1024 + stages * st + (NUM_BARRIERS_FIXED + 2 * stages) * 8 + 16,
+                       1024 + stages * st + EPI_STAGING_BYTES + (NUM_BARRIERS_FIXED + 2 * stages) * 8 + 16,
                        pow2_at_least(ACC_BUFS * bn)};
 }
 
@@ -73,7 +77,7 @@ GEMM_HD constexpr VariantInfo variant_info(int v) {
 }
 
 static_assert(variant_info(VARIANT_1SM_128x256).stages == 4, "1-SM 128x256: four 48 KiB stages");
-static_assert(variant_info(VARIANT_2SM_256x256).stages == 7, "2-SM 256x256: seven 32 KiB stages");
+static_assert(variant_info(VARIANT_2SM_256x256).stages == 6, "2-SM 256x256: six 32 KiB stages");
 static_assert(variant_info(VARIANT_2SM_256x256).smem <= SMEM_LIMIT, "fits");
 static_assert(variant_info(VARIANT_2SM_256x128).smem <= SMEM_LIMIT, "fits");
 
