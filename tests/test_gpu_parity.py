@@ -122,6 +122,10 @@ SMALL_SHAPES = [
     (1, 1, 8),
     (64, 40, 8),
     (384, 1024, 512),    # 3 x 4 tiles, several rounds per CTA when the grid is capped
+    (1, 257, 17),        # one row, ragged N, K not a multiple of 8 (lda padded to 24)
+    (3, 5, 7),
+    (17, 1, 300),        # one column
+    (2, 4096, 8),
 ]
 
 
