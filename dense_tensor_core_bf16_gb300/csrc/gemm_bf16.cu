@@ -313,8 +313,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
     // Everything above overlaps the tail of the previous kernel in the stream;
-    // no global memory (operands, C, workspace, flags) is touched before it
-    // has finished.
+    // no global memory (operands, C, workspace, flags) is read or written
+    // before it has finished.  The producer only asks L2 to start fetching
+    // the operands of its first STAGES k-tiles: L2 is the point of coherence,
+    // so if the previous kernel writes them, the loads after the wait still
+    // see its data.
+    if (warp == 0 && lane == 0) {
+        Schedule first(p, cluster);
+        Unit w0;
+        if (first.next(p, w0)) {
+            const int row_a = w0.tm * V.tile_m + static_cast<int>(rank) * CTA_ROWS;
+            const int row_b = w0.tn * BN + static_cast<int>(rank) * V.b_rows;
+            for (int kb = 0; kb < w0.kb_count && kb < STAGES; ++kb) {
+                ptx::tma_prefetch_l2_2d(&tmap_a, (w0.kb_begin + kb) * TILE_K, row_a);
+                ptx::tma_prefetch_l2_2d(&tmap_b, (w0.kb_begin + kb) * TILE_K, row_b);
+            }
+        }
+    }
     ptx::grid_dependency_wait();
     ptx::grid_launch_dependents();
 
@@ -489,14 +504,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             };
             const bool owner_fast = w.kind == KIND_OWNER && contrib_end == cluster + 2;   // the common case
             if (owner_fast) prefetch(0);
-#pragma unroll 1
+            // chunks this warp handles: all of them for a partial tile, else
+            // those that start inside C (the same for the whole warp)
+            const int n_chunks = to_slot ? BN / 32 : min(BN / 32, (p.N - col_base + 31) / 32);
+            // Two register sets: chunk c+1 is read from TMEM while chunk c is
+            // converted and stored.
+            uint32_t rbuf[2][32];
+            __syncwarp();
+            ptx::tmem_ld_32x32b_x32(t_row, rbuf[0]);
+            ptx::tmem_wait_ld(rbuf[0]);
+#pragma unroll
             for (int c = 0; c < BN / 32; ++c) {
+                if (c >= n_chunks) break;
                 const int col0 = col_base + c * 32;
-                if (!to_slot && col0 >= p.N) break;   // same for the whole warp
-                uint32_t r[32];
-                __syncwarp();
-                ptx::tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r);
-                ptx::tmem_wait_ld();
+                uint32_t (&r)[32] = rbuf[c & 1];
+                if (c + 1 < n_chunks) {
+                    __syncwarp();
+                    ptx::tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>((c + 1) * 32), rbuf[(c + 1) & 1]);
+                }
                 if (to_slot) {
                     // the whole tile-row chunk, in range or not: a reader takes it back
                     float4 *dst = slot_ptr(my_slot, c);
@@ -505,6 +530,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         __stcg(dst + v * 32, make_float4(__uint_as_float(r[4 * v + 0]), __uint_as_float(r[4 * v + 1]),
                                                          __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
                     }
+                    if (c + 1 < n_chunks) ptx::tmem_wait_ld(rbuf[(c + 1) & 1]);
                     continue;
                 }
                 if (w.kind == KIND_OWNER) {
@@ -570,6 +596,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     ++stores_issued;
                 }
+                if (c + 1 < n_chunks) ptx::tmem_wait_ld(rbuf[(c + 1) & 1]);
             }
             if (w.kind == KIND_PARTIAL) {
                 // publish: every lane's stores, then one release of the flag
