@@ -660,7 +660,15 @@ __global__ void __launch_bounds__(COMBINE_WARPS * 32)
     const float4 *P = reinterpret_cast<const float4 *>(part);
     for (long long base = blockIdx.x * 32LL; base < split_f4; base += gridDim.x * 32LL) {
         const long long idx = base + lane;
-        const bool live = idx < split_f4;
+        // where this float4 lands in C
+        const long long tile = idx / slot_f4;
+        const int q = static_cast<int>(idx - tile * slot_f4);
+        const int v = (q >> 5) & 7;
+        const int chunk = (q >> 8) % chunks;
+        const int wq = (q >> 8) / chunks;
+        const int row = static_cast<int>(tile / tiles_n) * tile_m + wq * 32 + lane;
+        const int col = static_cast<int>(tile % tiles_n) * bn + chunk * 32 + v * 4;
+        const bool live = idx < split_f4 && row < M && col < N;   // padding of the tiles is never read
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         if (live) {
             const float4 *src = P + idx;
@@ -696,14 +704,7 @@ __global__ void __launch_bounds__(COMBINE_WARPS * 32)
                 t.z += u.z;
                 t.w += u.w;
             }
-            const long long tile = idx / slot_f4;
-            const int q = static_cast<int>(idx - tile * slot_f4);
-            const int v = (q >> 5) & 7;
-            const int chunk = (q >> 8) % chunks;
-            const int wq = (q >> 8) / chunks;
-            const int row = static_cast<int>(tile / tiles_n) * tile_m + wq * 32 + lane;
-            const int col = static_cast<int>(tile % tiles_n) * bn + chunk * 32 + v * 4;
-            if (row < M && col < N) {
+            {
                 const float a[4] = {t.x, t.y, t.z, t.w};
                 if (out_bf16) {
                     __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(C) + static_cast<long long>(row) * ldc + col;
