@@ -50,7 +50,7 @@ enum : unsigned {
 struct KernelParams {
     int M, N, K;
     int tiles_m, tiles_n;
-    int k_tiles;                 // ceil(K / TILE_K)
+    int k_tiles;                 // ceil(K / k-tile width of the variant)
     int split_k;
     int group_m;                 // m-tiles per raster group
     long long num_units;         // tiles * split_k
@@ -240,11 +240,13 @@ __device__ __forceinline__ bool wait_flag(const unsigned int *flag, unsigned int
 //     CTAs' tensor memory, and its commits arrive on the barriers of both
 //     CTAs; each CTA's epilogue drains its own 128 rows and tells the leader
 //     when its half of an accumulator is free.
-template <int CG, int BN>
+template <int CG, int BN, int TK>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                      const __grid_constant__ CUtensorMap tmap_c, const KernelParams p) {
-    constexpr VariantInfo V = make_variant(CG, BN);
+    constexpr VariantInfo V = make_variant(CG, BN, TK);
+    constexpr int A_BOX = CTA_ROWS * TILE_K * 2;    // bytes of one A box (128 rows x 128 bytes)
+    constexpr int B_BOX = V.b_rows * TILE_K * 2;    // bytes of one B box
     constexpr int STAGES = V.stages;
     constexpr int BAR_FULL = 0;                           // [STAGES] operands landed (leader's count both CTAs)
     constexpr int BAR_EMPTY = STAGES;                     // [STAGES] slot free again
@@ -325,8 +327,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int row_a = w0.tm * V.tile_m + static_cast<int>(rank) * CTA_ROWS;
             const int row_b = w0.tn * BN + static_cast<int>(rank) * V.b_rows;
             for (int kb = 0; kb < w0.kb_count && kb < STAGES; ++kb) {
-                ptx::tma_prefetch_l2_2d(&tmap_a, (w0.kb_begin + kb) * TILE_K, row_a);
-                ptx::tma_prefetch_l2_2d(&tmap_b, (w0.kb_begin + kb) * TILE_K, row_b);
+                for (int j = 0; j < V.k_boxes; ++j) {
+                    ptx::tma_prefetch_l2_2d(&tmap_a, (w0.kb_begin + kb) * TK + j * TILE_K, row_a);
+                    ptx::tma_prefetch_l2_2d(&tmap_b, (w0.kb_begin + kb) * TK + j * TILE_K, row_b);
+                }
             }
         }
     }
@@ -356,14 +360,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         continue;   // test hook: this slot is never filled
                     }
                     if (leader) ptx::mbar_arrive_expect_tx(bar(BAR_FULL + s), TX_BYTES);
-                    const int kc = (w.kb_begin + kb) * TILE_K;
-                    if constexpr (PAIR) {
-                        const uint32_t full_leader = ptx::mapa_shared(bar(BAR_FULL + s), 0);
-                        ptx::tma_load_2d_pair(sA + s * V.a_stage, &tmap_a, full_leader, kc, row_a);
-                        ptx::tma_load_2d_pair(sB + s * V.b_stage, &tmap_b, full_leader, kc, row_b);
-                    } else {
-                        ptx::tma_load_2d(sA + s * V.a_stage, &tmap_a, bar(BAR_FULL + s), kc, row_a);
-                        ptx::tma_load_2d(sB + s * V.b_stage, &tmap_b, bar(BAR_FULL + s), kc, row_b);
+                    const int kc = (w.kb_begin + kb) * TK;
+#pragma unroll
+                    for (int j = 0; j < V.k_boxes; ++j) {
+                        const uint32_t dst_a = sA + s * V.a_stage + j * A_BOX;
+                        const uint32_t dst_b = sB + s * V.b_stage + j * B_BOX;
+                        if constexpr (PAIR) {
+                            const uint32_t full_leader = ptx::mapa_shared(bar(BAR_FULL + s), 0);
+                            ptx::tma_load_2d_pair(dst_a, &tmap_a, full_leader, kc + j * TILE_K, row_a);
+                            ptx::tma_load_2d_pair(dst_b, &tmap_b, full_leader, kc + j * TILE_K, row_b);
+                        } else {
+                            ptx::tma_load_2d(dst_a, &tmap_a, bar(BAR_FULL + s), kc + j * TILE_K, row_a);
+                            ptx::tma_load_2d(dst_b, &tmap_b, bar(BAR_FULL + s), kc + j * TILE_K, row_b);
+                        }
                     }
                 }
             }
@@ -405,17 +414,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     ptx::tc_fence_after_sync();
-                    const uint64_t a_desc = ptx::smem_desc_kmajor_sw128(sA + s * V.a_stage);
-                    const uint64_t b_desc = ptx::smem_desc_kmajor_sw128(sB + s * V.b_stage);
 #pragma unroll
-                    for (int k = 0; k < TILE_K / MMA_K; ++k) {
-                        // next 16 elements of K: +32 bytes inside the swizzled
-                        // 128-byte row, i.e. +2 in the address>>4 field
+                    for (int k = 0; k < TK / MMA_K; ++k) {
+                        // box k/4 of the k-tile; inside it, the next 16 elements
+                        // of K are +32 bytes in the swizzled 128-byte row, i.e.
+                        // +2 in the address>>4 field of the descriptor
+                        const int j = k / (TILE_K / MMA_K);
+                        const uint32_t step = 2u * static_cast<uint32_t>(k % (TILE_K / MMA_K));
+                        const uint64_t a_desc = ptx::smem_desc_kmajor_sw128(sA + s * V.a_stage + j * A_BOX) + step;
+                        const uint64_t b_desc = ptx::smem_desc_kmajor_sw128(sB + s * V.b_stage + j * B_BOX) + step;
                         const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
                         if constexpr (PAIR) {
-                            ptx::mma_bf16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, IDESC, acc);
+                            ptx::mma_bf16_pair(d_tmem, a_desc, b_desc, IDESC, acc);
                         } else {
-                            ptx::mma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, IDESC, acc);
+                            ptx::mma_bf16(d_tmem, a_desc, b_desc, IDESC, acc);
                         }
                     }
                     // slot reusable (in every CTA) once these MMAs have read it
@@ -757,9 +769,9 @@ using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, KernelParams);
 
 KernelFn kernel_fn(int variant) {
     switch (variant) {
-        case VARIANT_2SM_256x256: return gemm_bf16_kernel<2, 256>;
-        case VARIANT_2SM_256x128: return gemm_bf16_kernel<2, 128>;
-        default: return gemm_bf16_kernel<1, 256>;
+        case VARIANT_2SM_256x256: return gemm_bf16_kernel<2, 256, 128>;
+        case VARIANT_2SM_256x128: return gemm_bf16_kernel<2, 128, 64>;
+        default: return gemm_bf16_kernel<1, 256, 64>;
     }
 }
 

@@ -8,8 +8,11 @@
 //     256 x BN block with tcgen05.mma.cta_group::2 (M = 256): each CTA stages
 //     its own 128 rows of A and BN/2 rows of B, and holds its 128 rows of the
 //     accumulator in its own tensor memory.
-// Operands arrive in TILE_K-wide k-tiles (64 bf16 = 128 bytes, one swizzle
-// span) through a ring of as many stages as the shared memory holds.
+// Operands arrive in k-tiles of 64 or 128 bf16 (one or two 128-byte swizzle
+// spans, loaded as one TMA box each) through a ring of as many stages as the
+// shared memory holds.  One k-tile is one wait on the ring and one commit by
+// the MMA thread: 128-wide k-tiles give the Tensor Core 8 MMAs per wait, which
+// it needs to stay busy (4 per wait leaves it idle about a tenth of the time).
 #pragma once
 
 #if defined(__CUDACC__)
@@ -20,7 +23,7 @@
 
 namespace gemm {
 
-constexpr int TILE_K = 64;
+constexpr int TILE_K = 64;                // bf16 per TMA box row: 128 bytes, one swizzle span
 constexpr int MMA_K = 16;                 // K of one kind::f16 tcgen05.mma
 constexpr int CTA_ROWS = 128;             // rows of C per CTA = TMEM lanes
 constexpr int ACC_BUFS = 2;               // accumulators in TMEM (epilogue overlaps the next tile)
@@ -48,6 +51,8 @@ GEMM_HD constexpr int pow2_at_least(int x, int p = 32) { return p >= x ? p : pow
 struct VariantInfo {
     int cta_group;   // CTAs cooperating on one tile (cluster size)
     int bn;          // columns of C per tile
+    int tile_k;      // K per k-tile (a multiple of TILE_K)
+    int k_boxes;     // TMA boxes per operand per k-tile (tile_k / TILE_K)
     int tile_m;      // rows of C per tile (128 * cta_group)
     int b_rows;      // rows of B (N direction) each CTA stages
     int a_stage;     // bytes of A per stage per CTA
@@ -58,26 +63,26 @@ struct VariantInfo {
     int tmem_cols;   // tensor-memory columns per CTA (power of two >= 32)
 };
 
-GEMM_HD constexpr VariantInfo make_variant(int cg, int bn) {
-    const int a = CTA_ROWS * TILE_K * 2;
-    const int b = (bn / cg) * TILE_K * 2;
+GEMM_HD constexpr VariantInfo make_variant(int cg, int bn, int tk) {
+    const int a = CTA_ROWS * tk * 2;
+    const int b = (bn / cg) * tk * 2;
     const int st = a + b;
     const int fixed = 1024 + (NUM_BARRIERS_FIXED + 2 * MAX_STAGES) * 8 + 16;
     int stages = (SMEM_LIMIT - fixed - EPI_STAGING_BYTES) / st;
     if (stages > MAX_STAGES) stages = MAX_STAGES;
-    return VariantInfo{cg, bn, CTA_ROWS * cg, bn / cg, a, b, st, stages,
+    return VariantInfo{cg, bn, tk, tk / TILE_K, CTA_ROWS * cg, bn / cg, a, b, st, stages,
                        1024 + stages * st + EPI_STAGING_BYTES + (NUM_BARRIERS_FIXED + 2 * stages) * 8 + 16,
                        pow2_at_least(ACC_BUFS * bn)};
 }
 
 GEMM_HD constexpr VariantInfo variant_info(int v) {
-    return v == VARIANT_2SM_256x256 ? make_variant(2, 256)
-         : v == VARIANT_2SM_256x128 ? make_variant(2, 128)
-                                    : make_variant(1, 256);
+    return v == VARIANT_2SM_256x256 ? make_variant(2, 256, 128)
+         : v == VARIANT_2SM_256x128 ? make_variant(2, 128, 64)
+                                    : make_variant(1, 256, 64);
 }
 
 static_assert(variant_info(VARIANT_1SM_128x256).stages == 4, "1-SM 128x256: four 48 KiB stages");
-static_assert(variant_info(VARIANT_2SM_256x256).stages == 6, "2-SM 256x256: six 32 KiB stages");
+static_assert(variant_info(VARIANT_2SM_256x256).stages == 3, "2-SM 256x256: three 64 KiB stages");
 static_assert(variant_info(VARIANT_2SM_256x256).smem <= SMEM_LIMIT, "fits");
 static_assert(variant_info(VARIANT_2SM_256x128).smem <= SMEM_LIMIT, "fits");
 

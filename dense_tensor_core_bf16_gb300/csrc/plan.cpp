@@ -86,8 +86,8 @@ int resolve_variant(int requested) {
 }
 
 // The automatic choice between the single-CTA 128x256 and the pair 256x256
-// kernels: both spend the same time on one k-tile of one tile, so compare the
-// k-tiles each resident cluster would run with the work spread evenly,
+// kernels: both spend the same time on 64 of K of one tile, so compare the
+// 64-wide k-steps each resident cluster would run with the work spread evenly,
 // ceil(T * k_tiles / C) -- T tiles, C = S single CTAs or S/2 pairs -- and
 // give the pair kernel the advantage it shows at equal work (its tensor
 // pipes stay about 7 % busier: half the B traffic per SM, a deeper ring).
@@ -138,7 +138,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_layout_t la, gemm_
     plan->resident_ctas = resident;
     plan->tile_m = vi.tile_m;
     plan->tile_n = vi.bn;
-    plan->tile_k = TILE_K;
+    plan->tile_k = vi.tile_k;
     plan->stages = vi.stages;
     plan->threads_per_cta = kern.threads_per_cta;
     plan->num_sms = dev.num_sms;
@@ -147,7 +147,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_layout_t la, gemm_
     plan->persistent = persistent ? 1 : 0;
     const int64_t T = cdiv(M, vi.tile_m) * cdiv(N, vi.bn);
     plan->tiles = T;
-    plan->k_tiles = (int)cdiv(K, TILE_K);
+    plan->k_tiles = (int)cdiv(K, vi.tile_k);
 
     // Stream-K tail: only with the plan's own choice of split, on a persistent
     // grid (every cluster resident, as the hand-off between clusters needs).
@@ -165,7 +165,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_layout_t la, gemm_
     if (sk_tiles > 0) plan->launch_ctas = resident;   // every cluster takes a share of the tail
     plan->m_padded = cdiv(M, vi.tile_m) * vi.tile_m;
     plan->n_padded = cdiv(N, vi.bn) * vi.bn;
-    plan->k_padded = cdiv(K, TILE_K) * TILE_K;
+    plan->k_padded = cdiv(K, vi.tile_k) * vi.tile_k;
     if (plan->grid > 0) {
         const int64_t waves = cdiv(plan->grid, resident);
         plan->eta_wave = (double)plan->grid / ((double)waves * (double)resident);

@@ -82,6 +82,7 @@ WORKLOADS = [(256, 256, 256), (4096, 4096, 4096), (4095, 4096, 4096), (4097, 409
              (4096, 4096, 4088), (4096, 4104, 4096), (3968, 4096, 4096), (16384, 8192, 8192),
              (128, 256, 65536), (1, 1, 1), (129, 257, 65)]
 TILES = {1: (128, 256, 1), 2: (256, 256, 2), 3: (256, 128, 2)}
+TILE_K = {1: 64, 2: 128, 3: 64}
 
 
 def test_kernel_desc_without_a_device():
@@ -110,15 +111,16 @@ def test_plan_matches_oracle_closed_forms(shape, S, mac, variant):
         clusters = min(clusters, mac)
     R = clusters * cs
     assert p.resident_ctas == R and p.cluster_size == cs and p.kernel_variant == variant
-    assert (p.tile_m, p.tile_n, p.tile_k) == (tm, tn, 64)
+    tk = TILE_K[variant]
+    assert (p.tile_m, p.tile_n, p.tile_k) == (tm, tn, tk)
     assert p.tiles == pf.grid(M, N, tm, tn)
     assert p.grid == pf.grid(M, N, tm, tn, p.split_k) * cs
     assert p.eta_wave == pytest.approx(float(pf.eta_wave(p.grid, R, 1)), rel=1e-15)
-    assert p.eta_pad == pytest.approx(float(pf.eta_pad(M, N, K, tm, tn, 64)), rel=1e-15)
+    assert p.eta_pad == pytest.approx(float(pf.eta_pad(M, N, K, tm, tn, tk)), rel=1e-15)
     assert p.flops == pf.flops(M, N, K)
-    assert (p.m_padded, p.n_padded, p.k_padded) == (pf.padded(M, tm), pf.padded(N, tn), pf.padded(K, 64))
+    assert (p.m_padded, p.n_padded, p.k_padded) == (pf.padded(M, tm), pf.padded(N, tn), pf.padded(K, tk))
     assert p.launch_ctas == min(p.grid, R)
-    assert p.k_tiles == math.ceil(K / 64)
+    assert p.k_tiles == math.ceil(K / tk)
 
 
 def test_plan_hand_values_148_sms():
@@ -197,7 +199,7 @@ def test_plan_stream_k_tail(shape, variant):
     p = _plan(M, N, K, split=0, variant=variant)
     C = 152 // cs
     T = pf.grid(M, N, tm, tn)
-    KB = math.ceil(K / 64)
+    KB = math.ceil(K / TILE_K[variant])
     want_sk = 0
     if KB >= 2 and 2 * T > C and T % C:
         want_sk = C + T % C if T >= 2 * C else T
@@ -216,12 +218,16 @@ def test_plan_stream_k_tail(shape, variant):
 
 
 def test_plan_stream_k_hand_values():
-    """4096^3 on 76 pairs of 256x256 tiles: T = 256, 256 mod 76 = 28, a tail
-    of 104 tiles (6656 k-iterations, 87.6 per cluster) after 152 whole tiles;
-    the largest share is 2 x 64 + 88 = 216 k-iterations of an ideal 215.58."""
+    """4096^3 on 76 pairs of 256x256 tiles with 128-wide k-tiles: T = 256,
+    256 mod 76 = 28, a tail of 104 tiles (3328 k-iterations, 43.8 per
+    cluster) after 152 whole tiles; the largest share is 2 x 32 + 44 = 108
+    k-iterations of an ideal 256 x 32 / 76 = 107.79."""
     p = _plan(4096, 4096, 4096, split=0, variant=2)
-    assert (p.tiles, p.stream_k_tiles, p.dp_tiles) == (256, 104, 152)
-    assert p.eta_stream_k == pytest.approx((256 * 64 / 76) / 216, rel=1e-12)
+    assert (p.tiles, p.stream_k_tiles, p.dp_tiles, p.k_tiles) == (256, 104, 152, 32)
+    assert p.eta_stream_k == pytest.approx((256 * 32 / 76) / 108, rel=1e-12)
+    p = _plan(4096, 4096, 4096, split=0, variant=1)   # 64-wide k-tiles: 2 x ... on 152 CTAs
+    assert (p.tiles, p.stream_k_tiles, p.k_tiles) == (512, 208, 64)
+    assert p.eta_stream_k == pytest.approx((512 * 64 / 152) / (2 * 64 + math.ceil(208 * 64 / 152)), rel=1e-12)
 
 
 def _call(M, N, K, A=16, lda=64, B=16, ldb=64, C=16, ldc=64, la=0, lb=1, out=0, split=1):

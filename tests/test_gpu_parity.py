@@ -382,3 +382,27 @@ def test_large_16384x8192x8192_persistent_and_one_cta_per_tile(oracle_lib):
         nbad, _, _, detail = check_bf16(from_dev_bf16(C1)[rows, cols], ref, sabs, oracle_lib)
         assert nbad == 0, detail
         del C1
+
+
+def test_side_stream_and_workspace_release(oracle_lib):
+    """The C ABI on a non-default stream, and split-K after the workspace was
+    released (it grows again on demand)."""
+    g = _lib()
+    M, N, K = 300, 520, 2000
+    A, Bt = operands(M, N, K, "int4", False, SEED + 30)
+    ref, _ = oracle_lib.gemm(A, Bt, M, N, K)
+    dA, dBt = to_dev_padded(A), to_dev_padded(Bt)
+    side = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(side):
+        C1 = torch.empty((M, 520), dtype=torch.float32, device="cuda")
+        g.matmul(dA, dBt.t(), out=C1, split_k=5, stream=side)
+    side.synchronize()
+    assert np.array_equal(C1.cpu().numpy().astype(np.float64), ref)
+    g.gemm_release_workspace()
+    C2 = g.matmul(dA, dBt.t(), out_dtype=torch.float32, split_k=7)
+    assert np.array_equal(C2.cpu().numpy().astype(np.float64), ref)
+    st, plan = g.gemm_plan(M, N, K, opts=g.options(split_k=7))
+    assert st == 0 and g.gemm_reserve_workspace(plan.workspace_bytes) == 0
+    st, where = g.gemm_get_device_status(side.cuda_stream)
+    assert st == 0, f"{where:#x}"
