@@ -59,6 +59,14 @@ WORKLOADS = {
                   desc="gemm_bf16 4096x4104x4096, bf16 row x col -> bf16, N(0,1)/sqrt(K)"),
     "m3968": dict(M=3968, N=4096, K=4096, out="bf16", dist="normal", scaled=True, split_k=0,
                   desc="gemm_bf16 3968x4096x4096, bf16 row x col -> bf16, N(0,1)/sqrt(K)"),
+    "square4096_b_row": dict(M=4096, N=4096, K=4096, out="bf16", dist="normal", scaled=True, split_k=0,
+                             b_row=True,
+                             desc="gemm_bf16 M=N=K=4096, A bf16 row-major, B bf16 row-major (A @ B with a "
+                                  "contiguous K x N B), C bf16, N(0,1)/sqrt(K)"),
+    "square4096_a_col_b_row": dict(M=4096, N=4096, K=4096, out="bf16", dist="normal", scaled=True, split_k=0,
+                                   a_col=True, b_row=True,
+                                   desc="gemm_bf16 M=N=K=4096, A bf16 column-major, B bf16 row-major, C bf16, "
+                                        "N(0,1)/sqrt(K)"),
     "large": dict(M=16384, N=8192, K=8192, out="bf16", dist="normal", scaled=True, split_k=0,
                   desc="gemm_bf16 16384x8192x8192, bf16 row x col -> bf16, N(0,1)/sqrt(K)"),
     "large_one_cta_per_tile": dict(M=16384, N=8192, K=8192, out="bf16", dist="normal", scaled=True, split_k=0,
@@ -221,7 +229,16 @@ def run_gpu(args, wname: str, w: dict, cpu_baseline: bool):
 
     kw = dict(split_k=w["split_k"], non_persistent=w.get("non_persistent", False), kernel_variant=args.variant,
               no_stream_k=args.no_stream_k)
-    st, plan = g.gemm_plan(M, N, K, g.GEMM_ROW_MAJOR, g.GEMM_COL_MAJOR,
+    # operand storage: A row-major (M x K) or column-major (stored K x M); B
+    # column-major (stored N x K) or row-major (stored K x N)
+    a_col, b_row = w.get("a_col", False), w.get("b_row", False)
+    layout_a = g.GEMM_COL_MAJOR if a_col else g.GEMM_ROW_MAJOR
+    layout_b = g.GEMM_ROW_MAJOR if b_row else g.GEMM_COL_MAJOR
+    a_view = (lambda t: t.t()) if a_col else (lambda t: t)
+    b_view = (lambda t: t) if b_row else (lambda t: t.t())
+    A_store = np.ascontiguousarray(A_h.T) if a_col else A_h
+    B_store = np.ascontiguousarray(Bt_h.T) if b_row else Bt_h
+    st, plan = g.gemm_plan(M, N, K, layout_a, layout_b,
                            g.GEMM_OUT_BF16 if w["out"] == "bf16" else g.GEMM_OUT_F32,
                            g.options(split_k=kw["split_k"], non_persistent=int(kw["non_persistent"]),
                                      kernel_variant=kw["kernel_variant"], no_stream_k=int(kw["no_stream_k"])))
@@ -238,14 +255,14 @@ def run_gpu(args, wname: str, w: dict, cpu_baseline: bool):
     set_bytes = 2 * M * K + 2 * N * K + esize * M * N
     copies = max(2, math.ceil(2 * l2 / set_bytes) + 1)
 
-    A0 = torch.from_numpy(A_h.view(np.int16)).cuda().view(torch.bfloat16)
-    B0 = torch.from_numpy(Bt_h.view(np.int16)).cuda().view(torch.bfloat16)
+    A0 = torch.from_numpy(A_store.view(np.int16)).cuda().view(torch.bfloat16)
+    B0 = torch.from_numpy(B_store.view(np.int16)).cuda().view(torch.bfloat16)
     sets = []
     for i in range(copies):
         a = A0 if i == 0 else A0.clone()
         b = B0 if i == 0 else B0.clone()
         c = torch.empty((M, N), dtype=out_dtype, device="cuda")
-        sets.append((a, b.t(), c))
+        sets.append((a_view(a), b_view(b), c))
     launches_per_step = 1 + (1 if plan.split_k > 1 else 0)
 
     def step(i, **extra):
@@ -325,6 +342,7 @@ def run_gpu(args, wname: str, w: dict, cpu_baseline: bool):
         "data": f"synthetic (seeded SplitMix64, {w['dist']}{'/sqrt(K)' if w['scaled'] else ''}, seed {seed})",
         "config": {
             "workload": w["desc"], "M": M, "N": N, "K": K, "out": w["out"],
+            "layout_a": "column-major" if a_col else "row-major", "layout_b": "row-major" if b_row else "column-major",
             "kernel_variant": g.KERNEL_VARIANTS[plan.kernel_variant], "cluster_size": plan.cluster_size,
             "tile": f"{plan.tile_m}x{plan.tile_n}x{plan.tile_k}", "stages": plan.stages,
             "split_k": plan.split_k, "persistent": bool(plan.persistent), "grid_G": plan.grid,
@@ -361,14 +379,14 @@ def run_gpu(args, wname: str, w: dict, cpu_baseline: bool):
 
     # end to end through the public API: pinned host operands in, C back out, every step
     e2e_steps = min(args.steps, 20)
-    hA = torch.from_numpy(A_h.view(np.int16)).view(torch.bfloat16).pin_memory()
-    hB = torch.from_numpy(Bt_h.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hA = torch.from_numpy(A_store.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hB = torch.from_numpy(B_store.view(np.int16)).view(torch.bfloat16).pin_memory()
     hC = torch.empty((M, N), dtype=out_dtype).pin_memory()
-    dA, dB, dC = sets[0][0], sets[0][1].t(), sets[0][2]
+    dA, dB, dC = A0, B0, sets[0][2]     # the storage of set 0
     for _ in range(2):
         dA.copy_(hA, non_blocking=True)
         dB.copy_(hB, non_blocking=True)
-        g.matmul(dA, dB.t(), out=dC, **kw)
+        g.matmul(a_view(dA), b_view(dB), out=dC, **kw)
         hC.copy_(dC, non_blocking=True)
     torch.cuda.synchronize()
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -378,7 +396,7 @@ def run_gpu(args, wname: str, w: dict, cpu_baseline: bool):
     for _ in range(e2e_steps):
         dA.copy_(hA, non_blocking=True)
         dB.copy_(hB, non_blocking=True)
-        g.matmul(dA, dB.t(), out=dC, **kw)
+        g.matmul(a_view(dA), b_view(dB), out=dC, **kw)
         hC.copy_(dC, non_blocking=True)
     f1.record(stream)
     torch.cuda.synchronize()

@@ -244,9 +244,10 @@ def matmul(A, B, *, out_dtype=None, out=None, split_k: int = 0, non_persistent: 
            debug_skip_load: int = 0, kernel_variant: int = 0, no_stream_k: bool = False):
     """C = A @ B through ``gemm_bf16_ex``.
 
-    ``A``: (M, K) torch.bfloat16 CUDA tensor, row-major (stride (lda, 1)).
-    ``B``: (K, N) torch.bfloat16 CUDA tensor, column-major (stride (1, ldb)),
-    e.g. ``Bt.t()`` for a contiguous (N, K) ``Bt``.
+    ``A``: (M, K) torch.bfloat16 CUDA tensor, row-major (stride (lda, 1)) or
+    column-major (stride (1, lda), e.g. ``At.t()`` for a contiguous (K, M) ``At``).
+    ``B``: (K, N) torch.bfloat16 CUDA tensor, column-major (stride (1, ldb),
+    e.g. ``Bt.t()`` for a contiguous (N, K) ``Bt``) or row-major (stride (ldb, 1)).
     ``out``: optional (M, N) row-major float32 or bfloat16 tensor (stride (ldc, 1)).
     Raises :class:`GemmError` on a non-zero status.
     """
@@ -264,17 +265,29 @@ def matmul(A, B, *, out_dtype=None, out=None, split_k: int = 0, non_persistent: 
         raise ValueError("out has the wrong shape")
     if M and N and out.stride(1) != 1:
         raise ValueError("out must be row-major")
-    if M and K and A.stride(1) != 1:
-        raise ValueError("A must be row-major (stride (lda, 1))")
-    if N and K and B.stride(0) != 1:
-        raise ValueError("B must be column-major (stride (1, ldb))")
     odt = {torch.float32: GEMM_OUT_F32, torch.bfloat16: GEMM_OUT_BF16}.get(out.dtype)
     if odt is None:
         raise TypeError("out must be float32 or bfloat16")
-    # a single row (column) has no real leading dimension; report the
-    # smallest aligned one so the alignment rule does not reject it
-    lda = A.stride(0) if M > 1 else _round_up(K, 8)
-    ldb = B.stride(1) if N > 1 else _round_up(K, 8)
+    # Layouts from the strides.  A: row-major when K is contiguous (or K <= 1),
+    # else column-major when M is contiguous (or M <= 1); B alike, column-major
+    # first.  A dimension of extent 1 has no real leading dimension: report the
+    # smallest aligned one so the alignment rule does not reject it.
+    if K <= 1 or A.stride(1) == 1:
+        a_layout = GEMM_ROW_MAJOR
+        lda = A.stride(0) if M > 1 else _round_up(K, 8)
+    elif M <= 1 or A.stride(0) == 1:
+        a_layout = GEMM_COL_MAJOR
+        lda = A.stride(1) if K > 1 else _round_up(M, 8)
+    else:
+        raise ValueError("A must be row-major (stride (lda, 1)) or column-major (stride (1, lda))")
+    if K <= 1 or B.stride(0) == 1:
+        b_layout = GEMM_COL_MAJOR
+        ldb = B.stride(1) if N > 1 else _round_up(K, 8)
+    elif N <= 1 or B.stride(1) == 1:
+        b_layout = GEMM_ROW_MAJOR
+        ldb = B.stride(0) if K > 1 else _round_up(N, 8)
+    else:
+        raise ValueError("B must be column-major (stride (1, ldb)) or row-major (stride (ldb, 1))")
     ldc = out.stride(0) if M > 1 else _round_up(N, 8)
     opts = gemm_options_t(split_k=split_k, non_persistent=int(non_persistent), raster_group_m=raster_group_m,
                           mainloop_done_event=(mainloop_done_event.cuda_event if mainloop_done_event is not None
@@ -282,7 +295,7 @@ def matmul(A, B, *, out_dtype=None, out=None, split_k: int = 0, non_persistent: 
                           timeout_ms=timeout_ms, debug_skip_load=debug_skip_load, kernel_variant=kernel_variant,
                           no_stream_k=int(no_stream_k))
     st = gemm_bf16_ex(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc,
-                      GEMM_ROW_MAJOR, GEMM_COL_MAJOR, odt, opts, _stream_handle(stream))
+                      a_layout, b_layout, odt, opts, _stream_handle(stream))
     if st:
         raise GemmError(st, "gemm_bf16_ex")
     return out

@@ -59,6 +59,7 @@ struct KernelParams {
     int out_bf16;                // 1: bf16 stores, 0: fp32 stores
     unsigned long long timeout_ns;
     int skip_load;               // test hook (0 = off)
+    int a_mn, b_mn;              // 1: the operand is MN-major in memory (A column-major, B row-major)
     // Stream-K tail (sk_tiles > 0; split_k is then 1): tiles [0, dp_tiles) are
     // computed whole, round robin over the clusters; the k-iterations of tiles
     // [dp_tiles, tiles) are spread evenly over the clusters, which run them first.
@@ -245,8 +246,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                      const __grid_constant__ CUtensorMap tmap_c, const KernelParams p) {
     constexpr VariantInfo V = make_variant(CG, BN, TK);
-    constexpr int A_BOX = CTA_ROWS * TILE_K * 2;    // bytes of one A box (128 rows x 128 bytes)
-    constexpr int B_BOX = V.b_rows * TILE_K * 2;    // bytes of one B box
+    // Operand boxes.  K-major (A row-major, B column-major): TK/64 boxes of
+    // rows x 64 K, each rows x 128 bytes.  MN-major (A column-major, B
+    // row-major): rows/64 boxes of 64 M/N x TK, each TK rows of 128 bytes.
+    // The stage holds the same bytes either way.
+    constexpr int A_BOX = CTA_ROWS * TILE_K * 2;    // bytes of one K-major A box (128 rows x 128 bytes)
+    constexpr int B_BOX = V.b_rows * TILE_K * 2;    // bytes of one K-major B box
+    constexpr int MN_BOX = TK * TILE_K * 2;         // bytes of one MN-major box (TK rows x 128 bytes)
     constexpr int STAGES = V.stages;
     constexpr int BAR_FULL = 0;                           // [STAGES] operands landed (leader's count both CTAs)
     constexpr int BAR_EMPTY = STAGES;                     // [STAGES] slot free again
@@ -278,6 +284,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;
     const bool leader = rank == 0;
     const long long cluster = blockIdx.x / CG;
+    const bool a_mn = p.a_mn != 0, b_mn = p.b_mn != 0;
+    // Box j of an operand of `rows` rows per CTA starting at row0, in k-tile kc:
+    // its tensor-map coordinates (inner first) and its offset in the stage.
+    constexpr int K_BOXES = V.k_boxes;
+    auto box_count = [](bool mn, int rows) { return mn ? rows / TILE_K : K_BOXES; };
+    auto box_x = [](bool mn, int j, int kc, int row0) { return mn ? row0 + j * TILE_K : kc + j * TILE_K; };
+    auto box_y = [](bool mn, int j, int kc, int row0) { return mn ? kc : row0; };
+    auto box_off = [](bool mn, int j, int rows) { return static_cast<uint32_t>(j * (mn ? MN_BOX : rows * TILE_K * 2)); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -327,10 +341,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int row_a = w0.tm * V.tile_m + static_cast<int>(rank) * CTA_ROWS;
             const int row_b = w0.tn * BN + static_cast<int>(rank) * V.b_rows;
             for (int kb = 0; kb < w0.kb_count && kb < STAGES; ++kb) {
-                for (int j = 0; j < V.k_boxes; ++j) {
-                    ptx::tma_prefetch_l2_2d(&tmap_a, (w0.kb_begin + kb) * TK + j * TILE_K, row_a);
-                    ptx::tma_prefetch_l2_2d(&tmap_b, (w0.kb_begin + kb) * TK + j * TILE_K, row_b);
-                }
+                const int kc = (w0.kb_begin + kb) * TK;
+                for (int j = 0; j < box_count(a_mn, CTA_ROWS); ++j)
+                    ptx::tma_prefetch_l2_2d(&tmap_a, box_x(a_mn, j, kc, row_a), box_y(a_mn, j, kc, row_a));
+                for (int j = 0; j < box_count(b_mn, V.b_rows); ++j)
+                    ptx::tma_prefetch_l2_2d(&tmap_b, box_x(b_mn, j, kc, row_b), box_y(b_mn, j, kc, row_b));
             }
         }
     }
@@ -361,18 +376,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     if (leader) ptx::mbar_arrive_expect_tx(bar(BAR_FULL + s), TX_BYTES);
                     const int kc = (w.kb_begin + kb) * TK;
-#pragma unroll
-                    for (int j = 0; j < V.k_boxes; ++j) {
-                        const uint32_t dst_a = sA + s * V.a_stage + j * A_BOX;
-                        const uint32_t dst_b = sB + s * V.b_stage + j * B_BOX;
+                    // the full barrier of the stage: the leader's, for both CTAs of a pair
+                    const uint32_t full = PAIR ? ptx::mapa_shared(bar(BAR_FULL + s), 0) : bar(BAR_FULL + s);
+                    auto load = [&](const CUtensorMap *map, uint32_t dst, int x, int y) {
                         if constexpr (PAIR) {
-                            const uint32_t full_leader = ptx::mapa_shared(bar(BAR_FULL + s), 0);
-                            ptx::tma_load_2d_pair(dst_a, &tmap_a, full_leader, kc + j * TILE_K, row_a);
-                            ptx::tma_load_2d_pair(dst_b, &tmap_b, full_leader, kc + j * TILE_K, row_b);
+                            ptx::tma_load_2d_pair(dst, map, full, x, y);
                         } else {
-                            ptx::tma_load_2d(dst_a, &tmap_a, bar(BAR_FULL + s), kc + j * TILE_K, row_a);
-                            ptx::tma_load_2d(dst_b, &tmap_b, bar(BAR_FULL + s), kc + j * TILE_K, row_b);
+                            ptx::tma_load_2d(dst, map, full, x, y);
                         }
+                    };
+                    const int na = box_count(a_mn, CTA_ROWS), nb = box_count(b_mn, V.b_rows);
+                    for (int j = 0; j < na || j < nb; ++j) {
+                        if (j < na)
+                            load(&tmap_a, sA + s * V.a_stage + box_off(a_mn, j, CTA_ROWS), box_x(a_mn, j, kc, row_a),
+                                 box_y(a_mn, j, kc, row_a));
+                        if (j < nb)
+                            load(&tmap_b, sB + s * V.b_stage + box_off(b_mn, j, V.b_rows), box_x(b_mn, j, kc, row_b),
+                                 box_y(b_mn, j, kc, row_b));
                     }
                 }
             }
@@ -406,6 +426,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + buf * BN;
+                const uint32_t idesc = IDESC | (a_mn ? 1u << 15 : 0u) | (b_mn ? 1u << 16 : 0u);
                 for (int kb = 0; kb < w.kb_count; ++kb, ++it) {
                     const uint32_t s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1u;
@@ -416,18 +437,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ptx::tc_fence_after_sync();
 #pragma unroll
                     for (int k = 0; k < TK / MMA_K; ++k) {
-                        // box k/4 of the k-tile; inside it, the next 16 elements
-                        // of K are +32 bytes in the swizzled 128-byte row, i.e.
-                        // +2 in the address>>4 field of the descriptor
+                        // K-major: box k/4 of the k-tile; inside it, the next 16
+                        // elements of K are +32 bytes in the swizzled 128-byte
+                        // row, i.e. +2 in the address>>4 field of the descriptor.
+                        // MN-major: 16 more rows of K, two swizzle atoms on.
                         const int j = k / (TILE_K / MMA_K);
                         const uint32_t step = 2u * static_cast<uint32_t>(k % (TILE_K / MMA_K));
-                        const uint64_t a_desc = ptx::smem_desc_kmajor_sw128(sA + s * V.a_stage + j * A_BOX) + step;
-                        const uint64_t b_desc = ptx::smem_desc_kmajor_sw128(sB + s * V.b_stage + j * B_BOX) + step;
+                        const uint32_t a_base = sA + s * V.a_stage, b_base = sB + s * V.b_stage;
+                        const uint64_t a_desc =
+                            a_mn ? ptx::smem_desc_mnmajor_sw128(a_base + k * (MMA_K * 128), MN_BOX)
+                                 : ptx::smem_desc_kmajor_sw128(a_base + j * A_BOX) + step;
+                        const uint64_t b_desc =
+                            b_mn ? ptx::smem_desc_mnmajor_sw128(b_base + k * (MMA_K * 128), MN_BOX)
+                                 : ptx::smem_desc_kmajor_sw128(b_base + j * B_BOX) + step;
                         const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
                         if constexpr (PAIR) {
-                            ptx::mma_bf16_pair(d_tmem, a_desc, b_desc, IDESC, acc);
+                            ptx::mma_bf16_pair(d_tmem, a_desc, b_desc, idesc, acc);
                         } else {
-                            ptx::mma_bf16(d_tmem, a_desc, b_desc, IDESC, acc);
+                            ptx::mma_bf16(d_tmem, a_desc, b_desc, idesc, acc);
                         }
                     }
                     // slot reusable (in every CTA) once these MMAs have read it
@@ -897,11 +924,15 @@ gemm_kernel_desc_t kernel_desc(int variant, const VariantState &vs) {
     return k;
 }
 
-// A K-major bf16 operand with `rows` rows of `k` elements, `ld` apart.
-gemm_status_t encode_operand(CUtensorMap *map, const void *ptr, int64_t k, int64_t rows, int64_t ld, int box_rows) {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
+// A bf16 operand stored as `outer` lines of `inner` contiguous elements, `ld`
+// apart, read in boxes of 64 inner elements (128 bytes, one swizzle span) x
+// `box_outer` lines.  K-major operands: inner = K, lines = rows of the tile.
+// MN-major operands: inner = M or N, lines = K.
+gemm_status_t encode_operand(CUtensorMap *map, const void *ptr, int64_t inner, int64_t outer, int64_t ld,
+                             int box_outer) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(TILE_K), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(TILE_K), static_cast<cuuint32_t>(box_outer)};
     cuuint32_t elem_strides[2] = {1, 1};
     CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
                                 elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -983,14 +1014,19 @@ gemm_status_t launch_fill_zero(int64_t M, int64_t N, void *C, int64_t ldc, int e
                : GEMM_ERR_LAUNCH;
 }
 
-// Checks shared by every GEMM entry point; no CUDA calls.
+// Checks shared by every GEMM entry point; no CUDA calls.  Leading
+// dimensions: A row-major lda >= K, column-major lda >= M; B column-major
+// ldb >= K, row-major ldb >= N.
 gemm_status_t check_operands(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
-                             const void *C, int64_t ldc, gemm_dtype_t out_dtype) {
+                             const void *C, int64_t ldc, gemm_layout_t layout_a, gemm_layout_t layout_b,
+                             gemm_dtype_t out_dtype) {
     const int esize = out_dtype == GEMM_OUT_BF16 ? 2 : 4;
     if (!C || ldc < N) return GEMM_ERR_INVALID_VALUE;
     if (reinterpret_cast<uintptr_t>(C) % 16 != 0 || (ldc * esize) % 16 != 0) return GEMM_ERR_MISALIGNED;
     if (K > 0) {
-        if (!A || !B || lda < K || ldb < K) return GEMM_ERR_INVALID_VALUE;
+        const int64_t min_lda = layout_a == GEMM_ROW_MAJOR ? K : M;
+        const int64_t min_ldb = layout_b == GEMM_COL_MAJOR ? K : N;
+        if (!A || !B || lda < min_lda || ldb < min_ldb) return GEMM_ERR_INVALID_VALUE;
         if (reinterpret_cast<uintptr_t>(A) % 16 != 0 || reinterpret_cast<uintptr_t>(B) % 16 != 0 || lda % 8 != 0 ||
             ldb % 8 != 0)
             return GEMM_ERR_MISALIGNED;
@@ -1039,9 +1075,10 @@ gemm_status_t launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_
     }
 
     CUtensorMap tmap_a, tmap_b, tmap_c;
-    st = encode_operand(&tmap_a, A, K, M, lda, CTA_ROWS);
+    const bool a_mn = layout_a == GEMM_COL_MAJOR, b_mn = layout_b == GEMM_ROW_MAJOR;
+    st = a_mn ? encode_operand(&tmap_a, A, M, K, lda, vi.tile_k) : encode_operand(&tmap_a, A, K, M, lda, CTA_ROWS);
     if (st != GEMM_OK) return st;
-    st = encode_operand(&tmap_b, B, K, N, ldb, vi.b_rows);
+    st = b_mn ? encode_operand(&tmap_b, B, N, K, ldb, vi.tile_k) : encode_operand(&tmap_b, B, K, N, ldb, vi.b_rows);
     if (st != GEMM_OK) return st;
     st = encode_output(&tmap_c, C, N, M, ldc, out_dtype == GEMM_OUT_BF16);
     if (st != GEMM_OK) return st;
@@ -1063,6 +1100,8 @@ gemm_status_t launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_
     const int timeout_ms = o.timeout_ms > 0 ? o.timeout_ms : DEFAULT_TIMEOUT_MS;
     p.timeout_ns = static_cast<unsigned long long>(timeout_ms) * 1000000ull;
     p.skip_load = o.debug_skip_load;
+    p.a_mn = a_mn ? 1 : 0;
+    p.b_mn = b_mn ? 1 : 0;
     p.num_clusters = static_cast<int>(clusters);
     p.dp_tiles = static_cast<int>(plan.dp_tiles);
     p.sk_tiles = static_cast<int>(plan.stream_k_tiles);
@@ -1178,7 +1217,7 @@ gemm_status_t gemm_bf16_ex(int64_t M, int64_t N, int64_t K, const void *A, int64
         o.kernel_variant >= VARIANT_COUNT)
         return GEMM_ERR_INVALID_VALUE;
     if (M == 0 || N == 0) return GEMM_OK;
-    st = check_operands(M, N, K, A, lda, B, ldb, C, ldc, out_dtype);
+    st = check_operands(M, N, K, A, lda, B, ldb, C, ldc, layout_a, layout_b, out_dtype);
     if (st != GEMM_OK) return st;
 
     int device = 0;
@@ -1291,7 +1330,7 @@ extern "C" gemm_status_t gemm_bf16_splitk_noalloc(int64_t M, int64_t N, int64_t 
     gemm_status_t st = check_problem(M, N, K, layout_a, layout_b, out_dtype, split_k);
     if (st != GEMM_OK) return st;
     if (M == 0 || N == 0) return GEMM_OK;
-    st = check_operands(M, N, K, A, lda, B, ldb, C, ldc, out_dtype);
+    st = check_operands(M, N, K, A, lda, B, ldb, C, ldc, layout_a, layout_b, out_dtype);
     if (st != GEMM_OK) return st;
 
     int device = 0;

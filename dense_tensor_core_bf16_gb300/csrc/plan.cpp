@@ -27,7 +27,6 @@ gemm_status_t check_problem(int64_t M, int64_t N, int64_t K, gemm_layout_t la, g
         return GEMM_ERR_INVALID_VALUE;
     if (out != GEMM_OUT_F32 && out != GEMM_OUT_BF16) return GEMM_ERR_INVALID_VALUE;
     if (split_k < 0) return GEMM_ERR_INVALID_VALUE;
-    if (la != GEMM_ROW_MAJOR || lb != GEMM_COL_MAJOR) return GEMM_ERR_NOT_SUPPORTED;
     return GEMM_OK;
 }
 

@@ -299,9 +299,26 @@ __device__ __forceinline__ uint64_t smem_desc_kmajor_sw128(uint32_t saddr) {
     return d;
 }
 
+// Shared-memory descriptor of an MN-major operand tile with 128-byte
+// swizzling: rows of 128 bytes hold 64 consecutive M (or N) elements at one k;
+// 8 such rows (k .. k+7) form a 1024-byte swizzle atom.  Atoms follow each
+// other along K (stride byte offset 1024 B), and blocks of 64 M/N elements
+// are `mn_block_bytes` apart (leading byte offset).  One K = 16 MMA reads two
+// atoms along K, so the next 16 elements of K start 2048 bytes further.
+__device__ __forceinline__ uint64_t smem_desc_mnmajor_sw128(uint32_t saddr, uint32_t mn_block_bytes) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((mn_block_bytes >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
 // Instruction descriptor of kind::f16: D fp32 (bits 4-5 = 1), A bf16 (7-9 = 1),
-// B bf16 (10-12 = 1), no negation, both operands K-major (bits 15, 16 = 0),
-// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+// B bf16 (10-12 = 1), no negation, both operands K-major (bits 15, 16 = 0;
+// set bit 15 / 16 for an MN-major A / B), N >> 3 in bits 17-22, M >> 4 in
+// bits 24-28.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
     return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
            (static_cast<uint32_t>(m >> 4) << 24);

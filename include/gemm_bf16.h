@@ -55,7 +55,7 @@ typedef enum {
     GEMM_OK = 0,
     GEMM_ERR_INVALID_VALUE = 1,   /* negative or too large size, bad enum, short ld, NULL */
     GEMM_ERR_MISALIGNED = 2,      /* a pointer or leading dimension breaks the rules above */
-    GEMM_ERR_NOT_SUPPORTED = 3,   /* a layout pair this build has no kernel for */
+    GEMM_ERR_NOT_SUPPORTED = 3,   /* a request this build cannot run (too many stream-K clusters) */
     GEMM_ERR_NO_DEVICE = 4,       /* no usable CUDA device, or not an sm_103 part */
     GEMM_ERR_OUT_OF_MEMORY = 5,   /* the split-K workspace could not be grown */
     GEMM_ERR_LAUNCH = 6,          /* a CUDA runtime or driver call failed */
@@ -218,16 +218,20 @@ gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K,
 
 /*
  * C = A . B on `stream`.
- *   A: M x K bf16, layout_a must be GEMM_ROW_MAJOR (lda >= K).
- *   B: K x N bf16, layout_b must be GEMM_COL_MAJOR (ldb >= K), i.e. stored as
- *      N rows of K contiguous values.
+ *   A: M x K bf16, GEMM_ROW_MAJOR (lda >= K) or GEMM_COL_MAJOR (lda >= M,
+ *      i.e. stored as K rows of M contiguous values).
+ *   B: K x N bf16, GEMM_COL_MAJOR (ldb >= K, i.e. stored as N rows of K
+ *      contiguous values) or GEMM_ROW_MAJOR (ldb >= N).
  *   C: M x N row-major (ldc >= N), fp32 or bf16 per out_dtype.
+ *   All four layout pairs run the same kernels: an operand whose K is
+ *   contiguous is staged K-major, the others M- or N-major, and the Tensor
+ *   Core reads either form from shared memory (the transpose bits of the
+ *   instruction descriptor).
  *   split_k: 0 = the plan chooses, 1 = off, > 1 = that many K slices
  *      (clamped to the k-tile count).  With more than one slice the partial
  *      sums go to an fp32 workspace owned by the library and a second kernel
  *      adds them in slice order 0, 1, ... and writes C.
- * Other layouts return GEMM_ERR_NOT_SUPPORTED.  M == 0 or N == 0 is a no-op;
- * K == 0 writes zeros to C.
+ * M == 0 or N == 0 is a no-op; K == 0 writes zeros to C.
  * The split-K workspace grows on demand with cudaMalloc (a synchronising
  * call); reserve it beforehand with gemm_reserve_workspace() to keep
  * allocation out of timed regions and stream captures.

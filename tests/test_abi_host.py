@@ -241,8 +241,10 @@ def test_argument_checks_before_any_cuda_call():
     assert _call(4, 4, 4, la=2) == 1
     assert _call(4, 4, 4, out=5) == 1
     assert _call(4, 4, 4, split=-1) == 1
-    assert _call(4, 4, 4, la=1) == 3
-    assert _call(4, 4, 4, lb=0) == 3
+    assert _call(64, 4, 4, la=1, lda=32) == 1    # column-major A: lda < M
+    assert _call(4, 64, 4, lb=0, ldb=32) == 1    # row-major B: ldb < N
+    assert _call(60, 4, 4, la=1, lda=60) == 2    # column-major A: 120-byte lines
+    assert _call(4, 60, 4, lb=0, ldb=60) == 2    # row-major B: 120-byte lines
     assert _call(0, 4, 4) == 0            # empty: nothing to do
     assert _call(4, 0, 4) == 0
     assert _call(4, 4, 4, C=0) == 1       # NULL C
@@ -267,8 +269,12 @@ def test_plan_argument_checks():
     L = g.lib()
     assert L.gemm_plan_for_device(4, 4, 4, 0, 1, 0, None, None, ctypes.byref(k), ctypes.byref(plan)) == 1
     o1 = g.options(kernel_variant=1)
-    st, _ = g.gemm_plan_for_device(4, 4, 4, 1, 1, 0, o1, dev(), k)
-    assert st == 3
+    # every layout pair plans the same launch
+    st, p_default = g.gemm_plan_for_device(300, 500, 700, 0, 1, 0, o1, dev(), k)
+    assert st == 0
+    for la, lb in [(1, 1), (0, 0), (1, 0)]:
+        st, p = g.gemm_plan_for_device(300, 500, 700, la, lb, 0, o1, dev(), k)
+        assert st == 0 and p.as_dict() == p_default.as_dict()
     st, _ = g.gemm_plan_for_device(4, 4, 4, 0, 1, 0, g.options(kernel_variant=7), dev(), k)
     assert st == 1
     too_big = kern(1)

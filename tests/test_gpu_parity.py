@@ -270,8 +270,9 @@ def test_argument_errors_on_device():
     assert g.gemm_bf16(64, 64, 64, p + 2, 64, p, 64, C.data_ptr(), 64, 0, 1, 0, 1, s) == 2   # A off 16 B
     assert g.gemm_bf16(64, 64, 60, p, 60, p, 64, C.data_ptr(), 64, 0, 1, 0, 1, s) == 2       # lda % 8
     assert g.gemm_bf16(64, 64, 64, p, 64, p, 64, C.data_ptr(), 66, 0, 1, 0, 1, s) == 2       # ldc*4 % 16
-    assert g.gemm_bf16(64, 64, 64, p, 64, p, 64, C.data_ptr(), 64, 1, 1, 0, 1, s) == 3       # A column-major
-    assert g.gemm_bf16(64, 64, 64, p, 64, p, 64, C.data_ptr(), 64, 0, 0, 0, 1, s) == 3       # B row-major
+    assert g.gemm_bf16(64, 64, 64, p, 56, p, 64, C.data_ptr(), 64, 1, 1, 0, 1, s) == 1       # col-major A: lda < M
+    assert g.gemm_bf16(64, 64, 64, p, 64, p, 60, C.data_ptr(), 64, 0, 0, 0, 1, s) == 1       # row-major B: ldb < N
+    assert g.gemm_bf16(60, 64, 64, p, 60, p, 64, C.data_ptr(), 64, 1, 1, 0, 1, s) == 2       # col-major A: lda % 8
     assert g.gemm_bf16(64, 64, 64, p, 32, p, 64, C.data_ptr(), 64, 0, 1, 0, 1, s) == 1       # lda < K
     assert g.gemm_bf16(-1, 64, 64, p, 64, p, 64, C.data_ptr(), 64, 0, 1, 0, 1, s) == 1
 
