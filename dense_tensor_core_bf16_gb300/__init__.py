@@ -75,10 +75,19 @@ class gemm_plan_t(ctypes.Structure):
         return d
 
 
+class gemm_epilogue_t(ctypes.Structure):
+    _fields_ = [("alpha", ctypes.c_float), ("beta", ctypes.c_float), ("bias", ctypes.c_void_p),
+                ("activation", ctypes.c_int)]
+
+
 class gemm_options_t(ctypes.Structure):
     _fields_ = [("split_k", ctypes.c_int), ("non_persistent", ctypes.c_int), ("raster_group_m", ctypes.c_int),
                 ("mainloop_done_event", ctypes.c_void_p), ("timeout_ms", ctypes.c_int),
-                ("debug_skip_load", ctypes.c_int), ("kernel_variant", ctypes.c_int), ("no_stream_k", ctypes.c_int)]
+                ("debug_skip_load", ctypes.c_int), ("kernel_variant", ctypes.c_int), ("no_stream_k", ctypes.c_int),
+                ("epilogue", ctypes.POINTER(gemm_epilogue_t))]
+
+
+ACTIVATIONS = {"none": 0, "relu": 1, "gelu": 2}
 
 
 _lock = threading.Lock()

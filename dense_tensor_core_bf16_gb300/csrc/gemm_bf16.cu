@@ -1216,6 +1216,7 @@ gemm_status_t gemm_bf16_ex(int64_t M, int64_t N, int64_t K, const void *A, int64
     if (o.timeout_ms < 0 || o.raster_group_m < 0 || o.debug_skip_load < 0 || o.kernel_variant < 0 ||
         o.kernel_variant >= VARIANT_COUNT)
         return GEMM_ERR_INVALID_VALUE;
+    if (o.epilogue) return GEMM_ERR_NOT_SUPPORTED;
     if (M == 0 || N == 0) return GEMM_OK;
     st = check_operands(M, N, K, A, lda, B, ldb, C, ldc, layout_a, layout_b, out_dtype);
     if (st != GEMM_OK) return st;

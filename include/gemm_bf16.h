@@ -159,6 +159,35 @@ typedef struct {
                                     (tiles*k_tiles/clusters over the largest share); 0 without */
 } gemm_plan_t;
 
+/* Elementwise work fused into the store of C (gemm_bf16_ex with
+ * opts->epilogue != NULL), per output element:
+ *
+ *     C[m][n] := act(alpha * (A.B)[m][n] + beta * C[m][n] + bias[n])
+ *
+ * The Tensor Core's operation is D = A x B + C, and the work between the
+ * matrix products -- activation functions, residual adds -- runs on the
+ * ordinary lanes (lesson "The Tensor Core", its opening and the paragraph on
+ * what work the Tensor Cores speed up): here the epilogue threads do it on
+ * the fp32 accumulator before the single rounding to C's type.  The pages name
+ * no particular activation; these are offered:
+ *   GEMM_ACT_NONE  x
+ *   GEMM_ACT_RELU  max(x, 0)
+ *   GEMM_ACT_GELU  x * Phi(x) = x/2 * (1 + erf(x / sqrt 2)), the erf form
+ * The sum and the activation are evaluated in fp32 in the order written
+ * (alpha * acc, then + beta * C, then + bias).  C is read in place before it
+ * is overwritten (only when beta != 0); bias is NULL or a device array of N
+ * fp32 values on a 16-byte boundary.  With K == 0 the product is zero and
+ * C := act(beta * C + bias).  Split-K applies it in the combine kernel after
+ * the slices are added; a stream-K tile after its partial sums are added. */
+typedef enum { GEMM_ACT_NONE = 0, GEMM_ACT_RELU = 1, GEMM_ACT_GELU = 2 } gemm_activation_t;
+
+typedef struct {
+    float alpha;                 /* scale of A.B */
+    float beta;                  /* scale of the previous C; 0: C is not read */
+    const float *bias;           /* N fp32 values added per column, or NULL */
+    int activation;              /* gemm_activation_t */
+} gemm_epilogue_t;
+
 /* Options of gemm_bf16_ex.  Zero-initialise and set what you need. */
 typedef struct {
     int split_k;                 /* 0: the plan chooses; 1: off; >1: clamped to [1, k_tiles] */
@@ -173,6 +202,8 @@ typedef struct {
                                     ends with GEMM_ERR_DEVICE_TIMEOUT on the device */
     int kernel_variant;          /* gemm_kernel_variant_t; 0 = the plan chooses */
     int no_stream_k;             /* 1: never spread a tail of tiles over the clusters (stream-K) */
+    const gemm_epilogue_t *epilogue;   /* NULL: C = A.B; else the fused epilogue above (read
+                                          during the call, not kept) */
 } gemm_options_t;
 
 /* Fill `dev` with the facts of CUDA device `device`. */

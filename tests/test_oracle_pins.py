@@ -346,3 +346,80 @@ def test_occupancy_worked_example():
     assert (b0, lim0) == (1, "registers")
     # shared memory alone also allows exactly one
     assert (227 * 1024) // ex["smem_per_cta_bytes"] == 1
+
+
+# ---- the fused epilogue: act(alpha * P + beta * C + bias[n]) -------------------------
+
+def test_epilogue_identity_and_scaling_are_exact():
+    from oracle import epilogue as ep
+    P = np.array([[1.5, -2.0, 0.0], [3.25, -0.75, 8.0]])
+    assert np.array_equal(ep.epilogue(P), P)                         # alpha 1, beta 0, no bias
+    assert np.array_equal(ep.epilogue(P, alpha=2.0), 2.0 * P)        # a power of two scales exactly
+    assert np.array_equal(ep.epilogue(P, alpha=-1.0), -P)
+
+
+def test_epilogue_adds_c_and_broadcasts_bias_along_columns():
+    """Small integers: every sum is exact.  The bias varies along n and the
+    matrix is not square, so a bias indexed by row (or a dropped beta*C) fails."""
+    from oracle import epilogue as ep
+    P = np.arange(6, dtype=np.float64).reshape(2, 3)
+    C = np.array([[10.0, 20.0, 30.0], [40.0, 50.0, 60.0]])
+    bias = np.array([100.0, 200.0, 300.0])
+    D = ep.epilogue(P, C, bias, alpha=1.0, beta=1.0)
+    assert np.array_equal(D, [[110.0, 221.0, 332.0], [143.0, 254.0, 365.0]])
+    D = ep.epilogue(P, C, None, alpha=3.0, beta=-2.0)
+    assert np.array_equal(D, [[-20.0, -37.0, -54.0], [-71.0, -88.0, -105.0]])
+    with pytest.raises(ValueError):
+        ep.epilogue(P, None, np.zeros(2))                             # one bias value per column
+
+
+def test_epilogue_activation_applies_after_the_sum():
+    from oracle import epilogue as ep
+    P = np.array([[-3.0, 2.0]])
+    C = np.array([[5.0, -7.0]])
+    # relu(-3 + 5) = 2, not relu(-3) + 5 = 5; relu(2 - 7) = 0
+    assert np.array_equal(ep.epilogue(P, C, beta=1.0, activation="relu"), [[2.0, 0.0]])
+    assert np.array_equal(ep.epilogue(np.array([[-1.5, 0.0, 2.5]]), activation="relu"), [[0.0, 0.0, 2.5]])
+
+
+def test_gelu_closed_forms():
+    """gelu(x) = x Phi(x): gelu(0) = 0; Phi(x) + Phi(-x) = 1 gives
+    gelu(x) - gelu(-x) = x for every x; gelu(x) -> x as x grows; Phi(1) and
+    Phi(2) to 16 digits (standard normal table values)."""
+    from oracle import epilogue as ep
+    xs = np.array([[-6.0, -2.0, -1.0, -0.3, 0.0, 0.3, 1.0, 2.0, 6.0, 40.0]])
+    g = ep.epilogue(xs, activation="gelu")[0]
+    assert g[4] == 0.0
+    for x in [0.3, 1.0, 2.0, 6.0]:
+        gp = ep.epilogue(np.array([[x]]), activation="gelu")[0, 0]
+        gn = ep.epilogue(np.array([[-x]]), activation="gelu")[0, 0]
+        assert gp - gn == pytest.approx(x, rel=1e-15, abs=1e-16)
+    assert g[9] == 40.0
+    assert ep.epilogue(np.array([[1.0]]), activation="gelu")[0, 0] == pytest.approx(0.8413447460685429, rel=1e-15)
+    assert ep.epilogue(np.array([[2.0]]), activation="gelu")[0, 0] == pytest.approx(2 * 0.9772498680518208, rel=1e-15)
+    assert np.all(g[:4] < 0) and np.all(g[5:] > 0)
+
+
+def test_gelu_against_high_precision():
+    sympy = pytest.importorskip("sympy")
+    from oracle import epilogue as ep
+    xs = [-3.5, -1.25, -0.5, 0.125, 0.75, 1.7, 4.0]
+    got = ep.epilogue(np.array([xs]), activation="gelu")[0]
+    for x, v in zip(xs, got):
+        X = sympy.Rational(str(x))
+        ref = sympy.N(X / 2 * (1 + sympy.erf(X / sympy.sqrt(2))), 30)
+        assert v == pytest.approx(float(ref), rel=4e-16, abs=1e-300)
+
+
+def test_epilogue_tolerance_shape():
+    """The bound reduces to the plain fp32 accumulation bound (plus the
+    rounding of one sum) when there is nothing to fuse, and grows with the
+    magnitudes that enter the fp32 sum."""
+    from oracle import epilogue as ep
+    P = np.array([[1.0, -4.0]])
+    S = np.array([[2.0, 8.0]])
+    t0 = ep.tolerance(P, S)
+    assert np.allclose(t0, 2.0 ** -16 * S + 1e-6 + 2.0 ** -22 * np.abs(P) + 1e-6)
+    t1 = ep.tolerance(P, S, np.array([[1e3, 1e3]]), beta=1.0)
+    assert np.all(t1 > t0)
+    assert np.all(ep.tolerance(P, S, activation="gelu") > t0)
