@@ -67,6 +67,11 @@ WORKLOADS = {
                                    a_col=True, b_row=True,
                                    desc="gemm_bf16 M=N=K=4096, A bf16 column-major, B bf16 row-major, C bf16, "
                                         "N(0,1)/sqrt(K)"),
+    "square4096_residual_bias_gelu": dict(
+        M=4096, N=4096, K=4096, out="bf16", dist="normal", scaled=True, split_k=0,
+        epilogue=dict(alpha=1.0, beta=1.0, bias=True, activation="gelu"),
+        desc="gemm_bf16 M=N=K=4096, A row-major, B column-major, C bf16 := gelu(A.B + C + bias[n]) "
+             "(fused epilogue), N(0,1)/sqrt(K)"),
     "large": dict(M=16384, N=8192, K=8192, out="bf16", dist="normal", scaled=True, split_k=0,
                   desc="gemm_bf16 16384x8192x8192, bf16 row x col -> bf16, N(0,1)/sqrt(K)"),
     "large_one_cta_per_tile": dict(M=16384, N=8192, K=8192, out="bf16", dist="normal", scaled=True, split_k=0,
@@ -229,6 +234,14 @@ def run_gpu(args, wname: str, w: dict, cpu_baseline: bool):
 
     kw = dict(split_k=w["split_k"], non_persistent=w.get("non_persistent", False), kernel_variant=args.variant,
               no_stream_k=args.no_stream_k)
+    epi = w.get("epilogue")
+    if epi:
+        from dense_tensor_core_bf16_gb300 import inputs
+        # the fused epilogue: a bias of N values (seeded, like the operands); C is read (beta != 0)
+        bias_bits = inputs.matrix(1, N, dist="normal", seed=seed, stream=8)[0]
+        kw.update(alpha=epi["alpha"], beta=epi["beta"], activation=epi["activation"],
+                  bias=torch.from_numpy((bias_bits.astype(np.uint32) << 16).view(np.float32)).cuda()
+                  if epi["bias"] else None)
     # operand storage: A row-major (M x K) or column-major (stored K x M); B
     # column-major (stored N x K) or row-major (stored K x N)
     a_col, b_row = w.get("a_col", False), w.get("b_row", False)
@@ -261,7 +274,7 @@ def run_gpu(args, wname: str, w: dict, cpu_baseline: bool):
     for i in range(copies):
         a = A0 if i == 0 else A0.clone()
         b = B0 if i == 0 else B0.clone()
-        c = torch.empty((M, N), dtype=out_dtype, device="cuda")
+        c = torch.zeros((M, N), dtype=out_dtype, device="cuda")
         sets.append((a_view(a), b_view(b), c))
     launches_per_step = 1 + (1 if plan.split_k > 1 else 0)
 
@@ -343,6 +356,7 @@ def run_gpu(args, wname: str, w: dict, cpu_baseline: bool):
         "config": {
             "workload": w["desc"], "M": M, "N": N, "K": K, "out": w["out"],
             "layout_a": "column-major" if a_col else "row-major", "layout_b": "row-major" if b_row else "column-major",
+            "epilogue": w.get("epilogue"),
             "kernel_variant": g.KERNEL_VARIANTS[plan.kernel_variant], "cluster_size": plan.cluster_size,
             "tile": f"{plan.tile_m}x{plan.tile_n}x{plan.tile_k}", "stages": plan.stages,
             "split_k": plan.split_k, "persistent": bool(plan.persistent), "grid_G": plan.grid,

@@ -250,7 +250,8 @@ def _stream_handle(stream):
 
 def matmul(A, B, *, out_dtype=None, out=None, split_k: int = 0, non_persistent: bool = False,
            raster_group_m: int = 0, stream=None, mainloop_done_event=None, timeout_ms: int = 0,
-           debug_skip_load: int = 0, kernel_variant: int = 0, no_stream_k: bool = False):
+           debug_skip_load: int = 0, kernel_variant: int = 0, no_stream_k: bool = False,
+           alpha: float = 1.0, beta: float = 0.0, bias=None, activation: str = "none"):
     """C = A @ B through ``gemm_bf16_ex``.
 
     ``A``: (M, K) torch.bfloat16 CUDA tensor, row-major (stride (lda, 1)) or
@@ -258,6 +259,11 @@ def matmul(A, B, *, out_dtype=None, out=None, split_k: int = 0, non_persistent: 
     ``B``: (K, N) torch.bfloat16 CUDA tensor, column-major (stride (1, ldb),
     e.g. ``Bt.t()`` for a contiguous (N, K) ``Bt``) or row-major (stride (ldb, 1)).
     ``out``: optional (M, N) row-major float32 or bfloat16 tensor (stride (ldc, 1)).
+    ``alpha``, ``beta``, ``bias``, ``activation``: the fused epilogue
+    ``out := act(alpha * (A @ B) + beta * out + bias)`` (gemm_epilogue_t);
+    ``bias`` is None or a contiguous float32 CUDA tensor of N values;
+    ``activation`` is "none", "relu" or "gelu".  With beta != 0, ``out`` must
+    be given (its previous contents are read).
     Raises :class:`GemmError` on a non-zero status.
     """
     import torch
@@ -267,6 +273,13 @@ def matmul(A, B, *, out_dtype=None, out=None, split_k: int = 0, non_persistent: 
     K2, N = B.shape
     if K2 != K:
         raise ValueError(f"inner dimensions differ: {K} vs {K2}")
+    if activation not in ACTIVATIONS:
+        raise ValueError(f"activation must be one of {sorted(ACTIVATIONS)}")
+    if beta != 0.0 and out is None:
+        raise ValueError("beta != 0 reads the previous C: pass out=")
+    if bias is not None:
+        if bias.dtype != torch.float32 or bias.dim() != 1 or bias.numel() != B.shape[1] or not bias.is_contiguous():
+            raise ValueError("bias must be a contiguous float32 tensor of N values")
     if out is None:
         dt = out_dtype if out_dtype is not None else torch.bfloat16
         out = torch.empty((M, N), dtype=dt, device=A.device)
@@ -303,6 +316,11 @@ def matmul(A, B, *, out_dtype=None, out=None, split_k: int = 0, non_persistent: 
                                                else None),
                           timeout_ms=timeout_ms, debug_skip_load=debug_skip_load, kernel_variant=kernel_variant,
                           no_stream_k=int(no_stream_k))
+    epi = None
+    if alpha != 1.0 or beta != 0.0 or bias is not None or activation != "none":
+        epi = gemm_epilogue_t(alpha=alpha, beta=beta, bias=bias.data_ptr() if bias is not None else None,
+                              activation=ACTIVATIONS[activation])
+        opts.epilogue = ctypes.pointer(epi)
     st = gemm_bf16_ex(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc,
                       a_layout, b_layout, odt, opts, _stream_handle(stream))
     if st:

@@ -60,6 +60,11 @@ struct KernelParams {
     unsigned long long timeout_ns;
     int skip_load;               // test hook (0 = off)
     int a_mn, b_mn;              // 1: the operand is MN-major in memory (A column-major, B row-major)
+    // fused epilogue (epi = 1): C := act(alpha * acc + beta * C + bias[n])
+    int epi;
+    float alpha, beta;
+    const float *bias;           // N values or nullptr
+    int act;                     // gemm_activation_t
     // Stream-K tail (sk_tiles > 0; split_k is then 1): tiles [0, dp_tiles) are
     // computed whole, round robin over the clusters; the k-iterations of tiles
     // [dp_tiles, tiles) are spread evenly over the clusters, which run them first.
@@ -197,6 +202,111 @@ struct Schedule {
         return false;
     }
 };
+
+// ---- the fused epilogue ----------------------------------------------------
+//
+// act(alpha * acc + beta * c + b) in fp32, each operation rounded as written
+// (no contraction): the tolerance the tests hold it to counts those roundings.
+//
+// GELU is v * Phi(v) with Phi(v) = erfc(-v / sqrt 2) / 2.  erfc comes from
+// the rational approximation of Abramowitz & Stegun, Handbook of Mathematical
+// Functions, formula 7.1.26 (after Hastings): for z >= 0,
+//     erfc(z) = t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-z^2) + e(z),
+//     t = 1 / (1 + p z),  |e(z)| <= 1.5e-7,
+// and erfc(-z) = 2 - erfc(z).  With the fp32 evaluation (fast reciprocal and
+// exp within a few ulp) the error of Phi stays below 3e-7, i.e. below 2^-20 |v| on
+// v * Phi(v) -- inside the stated tolerance -- at about twenty branch-free
+// instructions per value.
+__device__ __forceinline__ float gelu(float v) {
+    const float z = fabsf(v) * 0.70710678118654752f;
+    const float t = __fdividef(1.0f, fmaf(0.3275911f, z, 1.0f));   // within 2 ulp
+    const float poly = t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, 1.061405429f, -1.453152027f), 1.421413741f), -0.284496736f),
+                                0.254829592f);
+    const float e = poly * __expf(-z * z);          // erfc(|v| / sqrt 2)
+    const float phi = v >= 0.0f ? fmaf(-0.5f, e, 1.0f) : 0.5f * e;
+    return v * phi;
+}
+
+// alpha * acc + beta * c + b, then ReLU when asked (GELU is applied apart).
+__device__ __forceinline__ float epilogue_linear(float acc, float c, float b, float alpha, float beta, int act) {
+    float v = __fmul_rn(alpha, acc);
+    v = __fadd_rn(v, __fmul_rn(beta, c));
+    v = __fadd_rn(v, b);
+    return act == GEMM_ACT_RELU ? fmaxf(v, 0.0f) : v;
+}
+
+__device__ __forceinline__ float epilogue_value(float acc, float c, float b, float alpha, float beta, int act) {
+    const float v = epilogue_linear(acc, c, b, alpha, beta, act);
+    return act == GEMM_ACT_GELU ? gelu(v) : v;
+}
+
+// Four consecutive previous values of C at (row, col) .. (row, col+3), as
+// fp32; entries at n >= N read as 0 (they are never stored).
+__device__ __forceinline__ float4 load_c4(const void *C, long long ldc, int out_bf16, int row, int col, int N) {
+    float e[4] = {0.f, 0.f, 0.f, 0.f};
+    if (out_bf16) {
+        const __nv_bfloat16 *src = static_cast<const __nv_bfloat16 *>(C) + static_cast<long long>(row) * ldc + col;
+        if (col + 4 <= N) {
+            const uint2 u = *reinterpret_cast<const uint2 *>(src);
+            e[0] = __uint_as_float(u.x << 16);
+            e[1] = __uint_as_float(u.x & 0xFFFF0000u);
+            e[2] = __uint_as_float(u.y << 16);
+            e[3] = __uint_as_float(u.y & 0xFFFF0000u);
+        } else {
+            for (int j = 0; j < 4 && col + j < N; ++j) e[j] = __bfloat162float(src[j]);
+        }
+    } else {
+        const float *src = static_cast<const float *>(C) + static_cast<long long>(row) * ldc + col;
+        if (col + 4 <= N) return *reinterpret_cast<const float4 *>(src);
+        for (int j = 0; j < 4 && col + j < N; ++j) e[j] = src[j];
+    }
+    return make_float4(e[0], e[1], e[2], e[3]);
+}
+
+// The 32 previous values of C at (row, col0 .. col0+31), as fp32; 16-byte
+// loads when the chunk lies inside C, element loads at the ragged edge.
+__device__ __forceinline__ void load_c32(float4 (&cv)[8], const void *C, long long ldc, int out_bf16, int row, int col0,
+                                         int N) {
+    if (out_bf16 && col0 + 32 <= N) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(C) +
+                                                           static_cast<long long>(row) * ldc + col0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 u = src[q];
+            cv[2 * q] = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                                    __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+            cv[2 * q + 1] = make_float4(__uint_as_float(u.z << 16), __uint_as_float(u.z & 0xFFFF0000u),
+                                        __uint_as_float(u.w << 16), __uint_as_float(u.w & 0xFFFF0000u));
+        }
+        return;
+    }
+#pragma unroll
+    for (int g = 0; g < 8; ++g) cv[g] = load_c4(C, ldc, out_bf16, row, col0 + 4 * g, N);
+}
+
+// Four bias values for columns col .. col+3 (0 beyond N or without a bias).
+__device__ __forceinline__ float4 load_bias4(const float *bias, int col, int N) {
+    if (!bias) return make_float4(0.f, 0.f, 0.f, 0.f);
+    if (col + 4 <= N) return *reinterpret_cast<const float4 *>(bias + col);
+    float e[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < 4 && col + j < N; ++j) e[j] = bias[j + col];
+    return make_float4(e[0], e[1], e[2], e[3]);
+}
+
+// GELU on one lane's row of a 32 x 32 chunk staged as fp32 in the warp's
+// buffer (piece v = columns 4v .. 4v+3 at row_base + ((v ^ sw) << 4)).  The
+// loop stays rolled: the epilogue warps share the SM's instruction cache with
+// the producer and MMA threads, and a larger epilogue body measurably slows
+// the whole kernel.
+__device__ __forceinline__ void gelu_row_smem(uint32_t row_base, uint32_t sw) {
+#pragma unroll 2
+    for (int g = 0; g < 8; ++g) {
+        const uint32_t addr = row_base + ((static_cast<uint32_t>(g) ^ sw) << 4);
+        const uint4 u = ptx::ld_shared_v4(addr);
+        ptx::st_shared_v4(addr, __float_as_uint(gelu(__uint_as_float(u.x))), __float_as_uint(gelu(__uint_as_float(u.y))),
+                          __float_as_uint(gelu(__uint_as_float(u.z))), __float_as_uint(gelu(__uint_as_float(u.w))));
+    }
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_bits, uint32_t hi_bits) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(lo_bits), __uint_as_float(hi_bits));
@@ -542,10 +652,123 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int v = 0; v < 8; ++v) pre[v] = __ldcg(src + v * 32);
             };
             const bool owner_fast = w.kind == KIND_OWNER && contrib_end == cluster + 2;   // the common case
-            if (owner_fast) prefetch(0);
             // chunks this warp handles: all of them for a partial tile, else
             // those that start inside C (the same for the whole warp)
             const int n_chunks = to_slot ? BN / 32 : min(BN / 32, (p.N - col_base + 31) / 32);
+            const int warp_row0 = w.tm * V.tile_m + static_cast<int>(rank) * CTA_ROWS + quarter * 32;
+            // stream-K owner: add the later segments of chunk c in k order
+            auto add_partials = [&](uint32_t (&r)[32], int c) {
+                for (long long c2 = cluster + 1; c2 < contrib_end; ++c2) {
+                    if (sk_range_start(p, c2 + 1) == sk_range_start(p, c2)) continue;
+                    const float4 *src = slot_ptr(c2, c);
+                    float4 q[8];
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) q[v] = __ldcg(src + v * 32);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        r[4 * v + 0] = __float_as_uint(__uint_as_float(r[4 * v + 0]) + q[v].x);
+                        r[4 * v + 1] = __float_as_uint(__uint_as_float(r[4 * v + 1]) + q[v].y);
+                        r[4 * v + 2] = __float_as_uint(__uint_as_float(r[4 * v + 2]) + q[v].z);
+                        r[4 * v + 3] = __float_as_uint(__uint_as_float(r[4 * v + 3]) + q[v].w);
+                    }
+                }
+            };
+            // stage the chunk and hand it to TMA, which clips rows >= M and
+            // columns >= N
+            auto stage_store = [&](uint32_t (&r)[32], int col0, bool with_gelu) {
+                if (warp_row0 >= p.M) return;
+                if (stores_issued >= 2 && lane == 0) ptx::bulk_wait_group_read<1>();   // this buffer read out
+                __syncwarp();
+                const uint32_t buf = epi_buf0 + (stores_issued & 1u) * EPI_BUF_BYTES;
+                if (with_gelu) {
+                    // GELU through this lane's fp32 row of the buffer (swizzled
+                    // as the fp32 staging below), and back into registers
+                    const uint32_t row_base = buf + static_cast<uint32_t>(lane) * 128u;
+                    const uint32_t sw = static_cast<uint32_t>(lane) & 7u;
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        ptx::st_shared_v4(row_base + ((static_cast<uint32_t>(v) ^ sw) << 4), r[4 * v + 0], r[4 * v + 1],
+                                          r[4 * v + 2], r[4 * v + 3]);
+                    gelu_row_smem(row_base, sw);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        const uint4 u = ptx::ld_shared_v4(row_base + ((static_cast<uint32_t>(v) ^ sw) << 4));
+                        r[4 * v + 0] = u.x;
+                        r[4 * v + 1] = u.y;
+                        r[4 * v + 2] = u.z;
+                        r[4 * v + 3] = u.w;
+                    }
+                    __syncwarp();   // the staging below writes into other lanes' rows
+                }
+                if (p.out_bf16) {
+                    const uint32_t row_base = buf + static_cast<uint32_t>(lane) * 64u;
+                    const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        ptx::st_shared_v4(row_base + ((static_cast<uint32_t>(v) ^ sw) << 4),
+                                          pack_bf16x2(r[8 * v + 0], r[8 * v + 1]), pack_bf16x2(r[8 * v + 2], r[8 * v + 3]),
+                                          pack_bf16x2(r[8 * v + 4], r[8 * v + 5]), pack_bf16x2(r[8 * v + 6], r[8 * v + 7]));
+                    }
+                } else {
+                    const uint32_t row_base = buf + static_cast<uint32_t>(lane) * 128u;
+                    const uint32_t sw = static_cast<uint32_t>(lane) & 7u;
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        ptx::st_shared_v4(row_base + ((static_cast<uint32_t>(v) ^ sw) << 4), r[4 * v + 0], r[4 * v + 1],
+                                          r[4 * v + 2], r[4 * v + 3]);
+                    }
+                }
+                ptx::fence_proxy_async_shared();
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::tma_store_2d(&tmap_c, buf, col0, warp_row0);
+                    ptx::bulk_commit_group();
+                }
+                ++stores_issued;
+            };
+            if (p.epi && !to_slot) {
+                // Fused epilogue, one chunk at a time in a rolled loop so that the
+                // code stays small: the row's previous C and bias values are
+                // loaded first (their latencies overlap the TMEM read), the
+                // linear part and ReLU run on registers, GELU through the
+                // staging buffer (gelu_row_smem).
+                const int row = warp_row0 + lane;
+                const bool read_c = p.beta != 0.0f && row < p.M;
+#pragma unroll 1
+                for (int c = 0; c < n_chunks; ++c) {
+                    const int col0 = col_base + c * 32;
+                    if (read_c && c + 1 < n_chunks) {
+                        // the next chunk's previous values of C, on their way to L1
+                        const char *nxt = static_cast<const char *>(p.out) +
+                                          (static_cast<long long>(row) * p.ld_out + col0 + 32) * (p.out_bf16 ? 2 : 4);
+                        asm volatile("prefetch.global.L1 [%0];" ::"l"(nxt));
+                        if (!p.out_bf16) asm volatile("prefetch.global.L1 [%0];" ::"l"(nxt + 64));
+                    }
+                    float4 cv[8], bv[8];
+                    if (read_c) {
+                        load_c32(cv, p.out, p.ld_out, p.out_bf16, row, col0, p.N);
+                    } else {
+#pragma unroll
+                        for (int g = 0; g < 8; ++g) cv[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) bv[g] = load_bias4(p.bias, col0 + 4 * g, p.N);
+                    uint32_t r[32];
+                    __syncwarp();
+                    ptx::tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r);
+                    ptx::tmem_wait_ld(r);
+                    if (w.kind == KIND_OWNER) add_partials(r, c);
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {
+                        r[4 * g + 0] = __float_as_uint(epilogue_linear(__uint_as_float(r[4 * g + 0]), cv[g].x, bv[g].x, p.alpha, p.beta, p.act));
+                        r[4 * g + 1] = __float_as_uint(epilogue_linear(__uint_as_float(r[4 * g + 1]), cv[g].y, bv[g].y, p.alpha, p.beta, p.act));
+                        r[4 * g + 2] = __float_as_uint(epilogue_linear(__uint_as_float(r[4 * g + 2]), cv[g].z, bv[g].z, p.alpha, p.beta, p.act));
+                        r[4 * g + 3] = __float_as_uint(epilogue_linear(__uint_as_float(r[4 * g + 3]), cv[g].w, bv[g].w, p.alpha, p.beta, p.act));
+                    }
+                    stage_store(r, col0, p.act == GEMM_ACT_GELU);
+                }
+            } else {
+            if (owner_fast) prefetch(0);
             // Two register sets: chunk c+1 is read from TMEM while chunk c is
             // converted and stored.
             uint32_t rbuf[2][32];
@@ -573,8 +796,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     continue;
                 }
                 if (w.kind == KIND_OWNER) {
-                    // add the later segments in k order
                     if (owner_fast) {
+                        // the first (usually only) contributor's partial sums, one chunk ahead
                         float4 q[8];
 #pragma unroll
                         for (int v = 0; v < 8; ++v) q[v] = pre[v];
@@ -587,55 +810,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             r[4 * v + 3] = __float_as_uint(__uint_as_float(r[4 * v + 3]) + q[v].w);
                         }
                     } else {
-                        for (long long c2 = cluster + 1; c2 < contrib_end; ++c2) {
-                            if (sk_range_start(p, c2 + 1) == sk_range_start(p, c2)) continue;
-                            const float4 *src = slot_ptr(c2, c);
-                            float4 q[8];
-#pragma unroll
-                            for (int v = 0; v < 8; ++v) q[v] = __ldcg(src + v * 32);
-#pragma unroll
-                            for (int v = 0; v < 8; ++v) {
-                                r[4 * v + 0] = __float_as_uint(__uint_as_float(r[4 * v + 0]) + q[v].x);
-                                r[4 * v + 1] = __float_as_uint(__uint_as_float(r[4 * v + 1]) + q[v].y);
-                                r[4 * v + 2] = __float_as_uint(__uint_as_float(r[4 * v + 2]) + q[v].z);
-                                r[4 * v + 3] = __float_as_uint(__uint_as_float(r[4 * v + 3]) + q[v].w);
-                            }
-                        }
+                        add_partials(r, c);
                     }
                 }
-                // stage the chunk and hand it to TMA (which clips rows >= M, cols >= N)
-                const int warp_row0 = w.tm * V.tile_m + static_cast<int>(rank) * CTA_ROWS + quarter * 32;
-                if (warp_row0 < p.M) {
-                    if (stores_issued >= 2 && lane == 0) ptx::bulk_wait_group_read<1>();   // this buffer read out
-                    __syncwarp();
-                    const uint32_t buf = epi_buf0 + (stores_issued & 1u) * EPI_BUF_BYTES;
-                    if (p.out_bf16) {
-                        const uint32_t row_base = buf + static_cast<uint32_t>(lane) * 64u;
-                        const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            ptx::st_shared_v4(row_base + ((static_cast<uint32_t>(v) ^ sw) << 4),
-                                              pack_bf16x2(r[8 * v + 0], r[8 * v + 1]), pack_bf16x2(r[8 * v + 2], r[8 * v + 3]),
-                                              pack_bf16x2(r[8 * v + 4], r[8 * v + 5]), pack_bf16x2(r[8 * v + 6], r[8 * v + 7]));
-                        }
-                    } else {
-                        const uint32_t row_base = buf + static_cast<uint32_t>(lane) * 128u;
-                        const uint32_t sw = static_cast<uint32_t>(lane) & 7u;
-#pragma unroll
-                        for (int v = 0; v < 8; ++v) {
-                            ptx::st_shared_v4(row_base + ((static_cast<uint32_t>(v) ^ sw) << 4), r[4 * v + 0], r[4 * v + 1],
-                                              r[4 * v + 2], r[4 * v + 3]);
-                        }
-                    }
-                    ptx::fence_proxy_async_shared();
-                    __syncwarp();
-                    if (lane == 0) {
-                        ptx::tma_store_2d(&tmap_c, buf, col0, warp_row0);
-                        ptx::bulk_commit_group();
-                    }
-                    ++stores_issued;
-                }
+                stage_store(r, col0, false);
                 if (c + 1 < n_chunks) ptx::tmem_wait_ld(rbuf[(c + 1) & 1]);
+            }
             }
             if (w.kind == KIND_PARTIAL) {
                 // publish: every lane's stores, then one release of the flag
@@ -683,11 +863,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // warp w adds slices w, w+8, w+16, ... in increasing order (16 loads in
 // flight), and warp 0 then adds the 8 warp sums in order w = 0 .. 7.  The
 // order is the same on every run.
+// With the fused epilogue (ep.epi), the sum of the slices takes the place of
+// the accumulator: C := act(alpha * sum + beta * C + bias[n]).
 constexpr int COMBINE_WARPS = 8;
+
+struct EpilogueArgs {
+    int epi;
+    float alpha, beta;
+    const float *bias;
+    int act;
+};
 
 __global__ void __launch_bounds__(COMBINE_WARPS * 32)
     splitk_combine_kernel(const float *__restrict__ part, int split, long long tiles, int tiles_n, int tile_m, int bn,
-                          int M, int N, void *C, long long ldc, int out_bf16) {
+                          int M, int N, void *C, long long ldc, int out_bf16, EpilogueArgs ep) {
     __shared__ float4 warp_sum[COMBINE_WARPS][32];
     ptx::grid_dependency_wait();   // the partials come from the previous kernel in the stream
     ptx::grid_launch_dependents();
@@ -743,6 +932,14 @@ __global__ void __launch_bounds__(COMBINE_WARPS * 32)
                 t.z += u.z;
                 t.w += u.w;
             }
+            if (ep.epi) {
+                const float4 c = ep.beta != 0.0f ? load_c4(C, ldc, out_bf16, row, col, N) : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 b = load_bias4(ep.bias, col, N);
+                t.x = epilogue_value(t.x, c.x, b.x, ep.alpha, ep.beta, ep.act);
+                t.y = epilogue_value(t.y, c.y, b.y, ep.alpha, ep.beta, ep.act);
+                t.z = epilogue_value(t.z, c.z, b.z, ep.alpha, ep.beta, ep.act);
+                t.w = epilogue_value(t.w, c.w, b.w, ep.alpha, ep.beta, ep.act);
+            }
             {
                 const float a[4] = {t.x, t.y, t.z, t.w};
                 if (out_bf16) {
@@ -782,6 +979,27 @@ __global__ void __launch_bounds__(256) fill_zero_kernel(void *C, long long ldc, 
             static_cast<uint16_t *>(C)[m * ldc + n] = 0;
         } else {
             static_cast<float *>(C)[m * ldc + n] = 0.0f;
+        }
+    }
+}
+
+// K == 0 with the fused epilogue: the product is zero, C := act(beta * C + bias[n]).
+__global__ void __launch_bounds__(256) epilogue_only_kernel(void *C, long long ldc, int M, int N, int out_bf16,
+                                                            EpilogueArgs ep) {
+    const long long total = static_cast<long long>(M) * N;
+    for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long m = idx / N;
+        const long long n = idx - m * N;
+        const float b = ep.bias ? ep.bias[n] : 0.0f;
+        if (out_bf16) {
+            __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(C) + m * ldc + n;
+            const float c = ep.beta != 0.0f ? __bfloat162float(*dst) : 0.0f;
+            *dst = __float2bfloat16_rn(epilogue_value(0.0f, c, b, ep.alpha, ep.beta, ep.act));
+        } else {
+            float *dst = static_cast<float *>(C) + m * ldc + n;
+            const float c = ep.beta != 0.0f ? *dst : 0.0f;
+            *dst = epilogue_value(0.0f, c, b, ep.alpha, ep.beta, ep.act);
         }
     }
 }
@@ -999,8 +1217,31 @@ unsigned int next_epoch(DeviceState &ds) {
     return ds.epoch;
 }
 
+// The fused epilogue an options struct asks for; epi = 0 when there is none
+// or it is the identity (alpha 1, beta 0, no bias, no activation).
+EpilogueArgs epilogue_args(const gemm_options_t &o) {
+    EpilogueArgs e{0, 1.0f, 0.0f, nullptr, GEMM_ACT_NONE};
+    if (!o.epilogue) return e;
+    const gemm_epilogue_t &x = *o.epilogue;
+    e.alpha = x.alpha;
+    e.beta = x.beta;
+    e.bias = x.bias;
+    e.act = x.activation;
+    e.epi = (x.alpha != 1.0f || x.beta != 0.0f || x.bias != nullptr || x.activation != GEMM_ACT_NONE) ? 1 : 0;
+    return e;
+}
+
+gemm_status_t check_epilogue(const gemm_options_t &o) {
+    if (!o.epilogue) return GEMM_OK;
+    const gemm_epilogue_t &x = *o.epilogue;
+    if (x.activation < GEMM_ACT_NONE || x.activation > GEMM_ACT_GELU) return GEMM_ERR_INVALID_VALUE;
+    if (reinterpret_cast<uintptr_t>(x.bias) % 16 != 0) return GEMM_ERR_MISALIGNED;
+    return GEMM_OK;
+}
+
+// K == 0: C := 0, or with a fused epilogue C := act(beta * C + bias).
 gemm_status_t launch_fill_zero(int64_t M, int64_t N, void *C, int64_t ldc, int esize, int num_sms,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, const EpilogueArgs &ep) {
     const long long total = M * N;
     long long blocks = (total + 255) / 256;
     if (blocks > 4LL * num_sms) blocks = 4LL * num_sms;
@@ -1008,10 +1249,15 @@ gemm_status_t launch_fill_zero(int64_t M, int64_t N, void *C, int64_t ldc, int e
     cfg.gridDim = dim3(static_cast<unsigned>(blocks));
     cfg.blockDim = dim3(256);
     cfg.stream = stream;
-    return cudaLaunchKernelEx(&cfg, fill_zero_kernel, C, static_cast<long long>(ldc), static_cast<int>(M),
-                              static_cast<int>(N), esize) == cudaSuccess
-               ? GEMM_OK
-               : GEMM_ERR_LAUNCH;
+    cudaError_t e;
+    if (ep.epi) {
+        e = cudaLaunchKernelEx(&cfg, epilogue_only_kernel, C, static_cast<long long>(ldc), static_cast<int>(M),
+                               static_cast<int>(N), esize == 2 ? 1 : 0, ep);
+    } else {
+        e = cudaLaunchKernelEx(&cfg, fill_zero_kernel, C, static_cast<long long>(ldc), static_cast<int>(M),
+                               static_cast<int>(N), esize);
+    }
+    return e == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
 }
 
 // Checks shared by every GEMM entry point; no CUDA calls.  Leading
@@ -1102,6 +1348,12 @@ gemm_status_t launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_
     p.skip_load = o.debug_skip_load;
     p.a_mn = a_mn ? 1 : 0;
     p.b_mn = b_mn ? 1 : 0;
+    const EpilogueArgs ep = epilogue_args(o);
+    p.epi = ep.epi;
+    p.alpha = ep.alpha;
+    p.beta = ep.beta;
+    p.bias = ep.bias;
+    p.act = ep.act;
     p.num_clusters = static_cast<int>(clusters);
     p.dp_tiles = static_cast<int>(plan.dp_tiles);
     p.sk_tiles = static_cast<int>(plan.stream_k_tiles);
@@ -1148,7 +1400,7 @@ gemm_status_t launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_
         if (cudaLaunchKernelEx(&cc, splitk_combine_kernel, static_cast<const float *>(partials), plan.split_k,
                                static_cast<long long>(plan.tiles), p.tiles_n, vi.tile_m, vi.bn, static_cast<int>(M),
                                static_cast<int>(N), C, static_cast<long long>(ldc),
-                               out_dtype == GEMM_OUT_BF16 ? 1 : 0) != cudaSuccess) {
+                               out_dtype == GEMM_OUT_BF16 ? 1 : 0, ep) != cudaSuccess) {
             cudaGetLastError();
             return GEMM_ERR_LAUNCH;
         }
@@ -1216,7 +1468,8 @@ gemm_status_t gemm_bf16_ex(int64_t M, int64_t N, int64_t K, const void *A, int64
     if (o.timeout_ms < 0 || o.raster_group_m < 0 || o.debug_skip_load < 0 || o.kernel_variant < 0 ||
         o.kernel_variant >= VARIANT_COUNT)
         return GEMM_ERR_INVALID_VALUE;
-    if (o.epilogue) return GEMM_ERR_NOT_SUPPORTED;
+    st = check_epilogue(o);
+    if (st != GEMM_OK) return st;
     if (M == 0 || N == 0) return GEMM_OK;
     st = check_operands(M, N, K, A, lda, B, ldb, C, ldc, layout_a, layout_b, out_dtype);
     if (st != GEMM_OK) return st;
@@ -1226,7 +1479,7 @@ gemm_status_t gemm_bf16_ex(int64_t M, int64_t N, int64_t K, const void *A, int64
     st = current_device(&device, &ds);
     if (st != GEMM_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (K == 0) return launch_fill_zero(M, N, C, ldc, out_dtype == GEMM_OUT_BF16 ? 2 : 4, ds->desc.num_sms, s);
+    if (K == 0) return launch_fill_zero(M, N, C, ldc, out_dtype == GEMM_OUT_BF16 ? 2 : 4, ds->desc.num_sms, s, epilogue_args(o));
     return launch_gemm(M, N, K, A, lda, B, ldb, C, ldc, layout_a, layout_b, out_dtype, o, s, *ds,
                        PartialBuffer{false, nullptr, 0});
 }
@@ -1339,7 +1592,7 @@ extern "C" gemm_status_t gemm_bf16_splitk_noalloc(int64_t M, int64_t N, int64_t 
     st = current_device(&device, &ds);
     if (st != GEMM_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (K == 0) return launch_fill_zero(M, N, C, ldc, out_dtype == GEMM_OUT_BF16 ? 2 : 4, ds->desc.num_sms, s);
+    if (K == 0) return launch_fill_zero(M, N, C, ldc, out_dtype == GEMM_OUT_BF16 ? 2 : 4, ds->desc.num_sms, s, EpilogueArgs{0, 1.0f, 0.0f, nullptr, GEMM_ACT_NONE});
 
     float *scratch = nullptr;
     st = noalloc_scratch(device, &scratch);

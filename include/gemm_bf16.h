@@ -174,7 +174,9 @@ typedef struct {
  *   GEMM_ACT_RELU  max(x, 0)
  *   GEMM_ACT_GELU  x * Phi(x) = x/2 * (1 + erf(x / sqrt 2)), the erf form
  * The sum and the activation are evaluated in fp32 in the order written
- * (alpha * acc, then + beta * C, then + bias).  C is read in place before it
+ * (alpha * acc, then + beta * C, then + bias).  On the device erfc is the
+ * rational approximation of Abramowitz & Stegun 7.1.26 (absolute error at
+ * most 1.5e-7), so GELU is within 2^-20 |x| of x * Phi(x) before rounding.  C is read in place before it
  * is overwritten (only when beta != 0); bias is NULL or a device array of N
  * fp32 values on a 16-byte boundary.  With K == 0 the product is zero and
  * C := act(beta * C + bias).  Split-K applies it in the combine kernel after

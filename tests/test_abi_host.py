@@ -39,6 +39,30 @@ def test_exports_every_declared_function():
         assert n in g.__all__, f"binding lacks {n}"
 
 
+def test_binding_structs_match_the_header(tmp_path):
+    """Every struct the binding mirrors has the size and field offsets the C
+    compiler gives it from include/gemm_bf16.h."""
+    import subprocess
+    structs = {"gemm_device_desc_t": g.gemm_device_desc_t, "gemm_kernel_desc_t": g.gemm_kernel_desc_t,
+               "gemm_plan_t": g.gemm_plan_t, "gemm_options_t": g.gemm_options_t,
+               "gemm_epilogue_t": g.gemm_epilogue_t}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "gemm_bf16.h"', "int main(void) {"]
+    for name, cls in structs.items():
+        lines.append(f'  printf("{name} %zu\\n", sizeof({name}));')
+        for field, _ in cls._fields_:
+            lines.append(f'  printf("{name}.{field} %zu\\n", offsetof({name}, {field}));')
+    lines.append("  return 0; }")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.check_call(["gcc", "-I", _build.INCLUDE, "-o", str(exe), str(src)])
+    out = dict(l.rsplit(" ", 1) for l in subprocess.check_output([str(exe)], text=True).splitlines())
+    for name, cls in structs.items():
+        assert int(out[name]) == ctypes.sizeof(cls), name
+        for field, _ in cls._fields_:
+            assert int(out[f"{name}.{field}"]) == getattr(cls, field).offset, f"{name}.{field}"
+
+
 def test_status_and_limiter_strings():
     assert g.gemm_status_string(0) == "GEMM_OK"
     assert g.gemm_status_string(7) == "GEMM_ERR_DEVICE_TIMEOUT"
@@ -261,6 +285,13 @@ def test_argument_checks_before_any_cuda_call():
     assert g.gemm_bf16_ex(4, 4, 4, 16, 64, 16, 64, 16, 64, 0, 1, 0, opts, None) == 1
     opts = g.gemm_options_t(kernel_variant=9)
     assert g.gemm_bf16_ex(4, 4, 4, 16, 64, 16, 64, 16, 64, 0, 1, 0, opts, None) == 1
+    # fused epilogue: an unknown activation, a bias off its 16-byte boundary
+    bad = g.gemm_epilogue_t(alpha=1.0, beta=0.0, bias=None, activation=3)
+    assert g.gemm_bf16_ex(4, 4, 4, 16, 64, 16, 64, 16, 64, 0, 1, 0,
+                          g.gemm_options_t(epilogue=ctypes.pointer(bad)), None) == 1
+    off = g.gemm_epilogue_t(alpha=1.0, beta=1.0, bias=20, activation=1)
+    assert g.gemm_bf16_ex(4, 4, 4, 16, 64, 16, 64, 16, 64, 0, 1, 0,
+                          g.gemm_options_t(epilogue=ctypes.pointer(off)), None) == 2
 
 
 def test_plan_argument_checks():
