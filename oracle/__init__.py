@@ -11,6 +11,9 @@ Contents
   - ``oracle_gemm.c`` (built into ``_build/liboracle.so`` by :func:`build`):
     the binary64 triple loop, the selected-entries variant and the direct
     binary64 -> bf16 round-to-nearest-even.
+  - ``oracle_conv.c`` (same library): the direct 2-D convolution
+    (:func:`conv2d`, :func:`conv2d_out_size`).
+  - :mod:`oracle.epilogue`: the fused epilogue act(alpha AB + beta C + bias).
   - :mod:`oracle.plan_forms`: FLOPs, grid, wave and padding efficiency and the
     occupancy arithmetic, as the pages define them.
 
@@ -28,6 +31,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle_gemm.c")
+_SRCS = [_SRC, os.path.join(_HERE, "oracle_conv.c")]
 _OUT_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
 _lock = threading.Lock()
@@ -39,13 +43,13 @@ _CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp", "-fPIC", "-
 
 
 def build(force: bool = False) -> str:
-    """Compile ``oracle_gemm.c`` with gcc into ``oracle/_build/liboracle.so``."""
+    """Compile ``oracle_gemm.c`` and ``oracle_conv.c`` with gcc into ``oracle/_build/liboracle.so``."""
     os.makedirs(_OUT_DIR, exist_ok=True)
     if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+            and all(os.path.getmtime(_LIB_PATH) >= os.path.getmtime(f) for f in _SRCS)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    subprocess.check_call(["gcc", *_CFLAGS, "-o", tmp, _SRC, "-lm"])
+    subprocess.check_call(["gcc", *_CFLAGS, "-o", tmp, *_SRCS, "-lm"])
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -70,6 +74,8 @@ def _load():
         lib.oracle_gemm.restype = None
         lib.oracle_gemm_entries.argtypes = [i64, vp, i64, i32, vp, i64, i32, vp, vp, i64, vp, vp, i32]
         lib.oracle_gemm_entries.restype = None
+        lib.oracle_conv2d_fprop.argtypes = [i64] * 15 + [vp, vp, vp, vp, i32]
+        lib.oracle_conv2d_fprop.restype = None
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = i32
         _lib = lib
@@ -158,3 +164,33 @@ def gemm_entries(A: np.ndarray, B: np.ndarray, M: int, N: int, K: int, rows, col
                                     int(b_col_major), _ptr(r), _ptr(c), r.size,
                                     _ptr(out), _ptr(sabs), int(threads))
     return out, sabs
+
+
+def conv2d_out_size(H: int, R: int, pad: int, stride: int, dil: int) -> int:
+    """Output extent of a convolution along one spatial dimension: the number
+    of window origins p*stride - pad whose last tap, + dil*(R-1), stays below
+    H + pad."""
+    return (H + 2 * pad - dil * (R - 1) - 1) // stride + 1
+
+
+def conv2d(x: np.ndarray, w: np.ndarray, *, pad=(0, 0), stride=(1, 1), dil=(1, 1), threads: int = 0,
+           with_abs: bool = True):
+    """Forward 2-D convolution in binary64 (see oracle_conv.c).
+
+    ``x``: N x H x W x C bf16 bit patterns (NHWC); ``w``: K x R x S x C (KRSC).
+    Returns (y, Sabs) as N x P x Q x K arrays."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    w = np.ascontiguousarray(w, dtype=np.uint16)
+    N, H, W, C = x.shape
+    K, R, S, C2 = w.shape
+    if C2 != C:
+        raise ValueError("channel counts differ")
+    P = conv2d_out_size(H, R, pad[0], stride[0], dil[0])
+    Q = conv2d_out_size(W, S, pad[1], stride[1], dil[1])
+    if P < 1 or Q < 1:
+        raise ValueError("empty output")
+    y = np.zeros((N, P, Q, K), dtype=np.float64)
+    sabs = np.zeros((N, P, Q, K), dtype=np.float64) if with_abs else None
+    _load().oracle_conv2d_fprop(N, H, W, C, K, R, S, pad[0], pad[1], stride[0], stride[1], dil[0], dil[1], P, Q,
+                                _ptr(x), _ptr(w), _ptr(y), _ptr(sabs) if sabs is not None else None, int(threads))
+    return y, sabs

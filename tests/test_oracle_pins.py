@@ -423,3 +423,95 @@ def test_epilogue_tolerance_shape():
     t1 = ep.tolerance(P, S, np.array([[1e3, 1e3]]), beta=1.0)
     assert np.all(t1 > t0)
     assert np.all(ep.tolerance(P, S, activation="gelu") > t0)
+
+
+# ---- the convolution oracle (implicit GEMM workload) ----------------------------------
+
+def _bf16_bits(vals):
+    return (np.asarray(vals, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def test_conv_one_by_one_is_the_gemm():
+    """A 1 x 1 convolution with stride 1 and no padding is the GEMM of the
+    pixels (N H W x C) with the filters (K x C as B's column-major storage);
+    both sum over c in the same order, so they agree exactly."""
+    import oracle
+    rng = np.random.default_rng(3)
+    N, H, W, C, K = 2, 3, 5, 24, 7
+    x = _bf16_bits(rng.standard_normal((N, H, W, C)))
+    w = _bf16_bits(rng.standard_normal((K, 1, 1, C)))
+    y, _ = oracle.conv2d(x, w)
+    ref, _ = oracle.gemm(x.reshape(N * H * W, C), w.reshape(K, C), N * H * W, K, C)
+    assert np.array_equal(y.reshape(N * H * W, K), ref)
+
+
+@pytest.mark.parametrize("case", [
+    dict(N=1, H=4, W=5, C=3, K=2, R=3, S=2, pad=(1, 0), stride=(1, 1), dil=(1, 1)),
+    dict(N=2, H=5, W=5, C=2, K=3, R=3, S=3, pad=(1, 1), stride=(2, 2), dil=(1, 1)),
+    dict(N=1, H=6, W=7, C=2, K=2, R=2, S=3, pad=(2, 1), stride=(1, 2), dil=(2, 2)),
+])
+def test_conv_against_exact_rational_brute_force(case):
+    """Every output by the definition in exact rationals (Fractions of the
+    bf16 values), with stride, padding and dilation; the binary64 oracle must
+    match within K-many roundings."""
+    import oracle
+    rng = np.random.default_rng(11)
+    N, H, W, C, K, R, S = (case[k] for k in "N H W C K R S".split())
+    (ph, pw), (sh, sw), (dh, dw) = case["pad"], case["stride"], case["dil"]
+    x = _bf16_bits(rng.standard_normal((N, H, W, C)))
+    w = _bf16_bits(rng.standard_normal((K, R, S, C)))
+    y, sabs = oracle.conv2d(x, w, pad=(ph, pw), stride=(sh, sw), dil=(dh, dw))
+    xf = oracle.bf16_to_f64(x)
+    wf = oracle.bf16_to_f64(w)
+    P = (H + 2 * ph - dh * (R - 1) - 1) // sh + 1
+    Q = (W + 2 * pw - dw * (S - 1) - 1) // sw + 1
+    assert y.shape == (N, P, Q, K)
+    for n in range(N):
+        for p in range(P):
+            for q in range(Q):
+                for k in range(K):
+                    tot = Fraction(0)
+                    for r in range(R):
+                        for s in range(S):
+                            h, ww = p * sh - ph + r * dh, q * sw - pw + s * dw
+                            if 0 <= h < H and 0 <= ww < W:
+                                for c in range(C):
+                                    tot += Fraction(xf[n, h, ww, c]) * Fraction(wf[k, r, s, c])
+                    assert abs(Fraction(y[n, p, q, k]) - tot) <= Fraction(R * S * C) * Fraction(2) ** -53 * Fraction(sabs[n, p, q, k])
+
+
+def test_conv_padding_counts_taps():
+    """All-ones input and filter: each output counts the taps inside the
+    image times C -- 4, 6, 9 taps at a corner, an edge and the interior of a
+    3 x 3 filter with one pixel of padding."""
+    import oracle
+    C = 8
+    x = np.full((1, 4, 5, C), 0x3F80, dtype=np.uint16)
+    w = np.full((2, 3, 3, C), 0x3F80, dtype=np.uint16)
+    y, _ = oracle.conv2d(x, w, pad=(1, 1))
+    taps = np.array([[4, 6, 6, 6, 4], [6, 9, 9, 9, 6], [6, 9, 9, 9, 6], [4, 6, 6, 6, 4]]) * C
+    assert np.array_equal(y[0, :, :, 0], taps) and np.array_equal(y[0, :, :, 1], taps)
+
+
+def test_conv_identity_filter_copies_the_input():
+    """w[k][1][1][c] = [k == c] (the centre tap of a 3 x 3), padding 1: y = x."""
+    import oracle
+    rng = np.random.default_rng(5)
+    x = _bf16_bits(rng.standard_normal((2, 5, 4, 6)))
+    w = np.zeros((6, 3, 3, 6), dtype=np.uint16)
+    for c in range(6):
+        w[c, 1, 1, c] = 0x3F80
+    y, _ = oracle.conv2d(x, w, pad=(1, 1))
+    assert np.array_equal(y, oracle.bf16_to_f64(x))
+
+
+def test_conv_output_size_counts_window_origins():
+    import oracle
+    for H in range(1, 12):
+        for R in range(1, 5):
+            for pad in range(0, 3):
+                for stride in range(1, 4):
+                    for dil in range(1, 3):
+                        origins = [o for o in range(-pad, H + pad, stride) if o + dil * (R - 1) < H + pad]
+                        assert oracle.conv2d_out_size(H, R, pad, stride, dil) == max(len(origins), 0) or \
+                            (len(origins) == 0 and oracle.conv2d_out_size(H, R, pad, stride, dil) <= 0)
