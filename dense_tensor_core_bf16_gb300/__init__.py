@@ -26,6 +26,8 @@ __all__ = [
     "gemm_device_desc_query", "gemm_kernel_desc", "gemm_reserve_workspace", "gemm_release_workspace",
     "gemm_get_device_status", "gemm_status_string", "gemm_limiter_string", "matmul", "lib", "header_functions",
     "gemm_bf16_splitk_noalloc", "GEMM_NOALLOC_SCRATCH_FLOATS", "options",
+    "gemm_epilogue_t", "gemm_conv2d_desc_t", "gemm_conv2d_out_dims", "gemm_conv2d_plan", "gemm_conv2d_fprop_bf16",
+    "conv2d",
 ]
 
 GEMM_ROW_MAJOR, GEMM_COL_MAJOR = 0, 1
@@ -90,6 +92,11 @@ class gemm_options_t(ctypes.Structure):
 ACTIVATIONS = {"none": 0, "relu": 1, "gelu": 2}
 
 
+class gemm_conv2d_desc_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("N", "H", "W", "C", "K", "R", "S")] + \
+        [(n, ctypes.c_int) for n in ("pad_h", "pad_w", "stride_h", "stride_w", "dil_h", "dil_w")]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -116,6 +123,12 @@ def lib() -> ctypes.CDLL:
         L.gemm_bf16_ex.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, i32, i32, P(gemm_options_t), vp]
         L.gemm_bf16_splitk_noalloc.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, i32, i32, i32, vp]
         L.gemm_bf16_splitk_noalloc.restype = i32
+        L.gemm_conv2d_out_dims.argtypes = [P(gemm_conv2d_desc_t), P(i64), P(i64)]
+        L.gemm_conv2d_out_dims.restype = i32
+        L.gemm_conv2d_plan.argtypes = [P(gemm_conv2d_desc_t), i32, P(gemm_options_t), P(gemm_plan_t)]
+        L.gemm_conv2d_plan.restype = i32
+        L.gemm_conv2d_fprop_bf16.argtypes = [P(gemm_conv2d_desc_t), vp, vp, vp, i32, P(gemm_options_t), vp]
+        L.gemm_conv2d_fprop_bf16.restype = i32
         L.gemm_reserve_workspace.argtypes = [ctypes.c_size_t]
         L.gemm_release_workspace.argtypes = []
         L.gemm_release_workspace.restype = None
@@ -210,6 +223,27 @@ def gemm_bf16_splitk_noalloc(M, N, K, A, lda, B, ldb, C, ldc, layout_a, layout_b
     (split * M * round_up(N, 4) must fit in it)."""
     return lib().gemm_bf16_splitk_noalloc(M, N, K, A, lda, B, ldb, C, ldc, layout_a, layout_b, out_dtype,
                                           split_k, stream)
+
+
+def gemm_conv2d_out_dims(desc: gemm_conv2d_desc_t):
+    """(status, P, Q)."""
+    P, Q = ctypes.c_int64(), ctypes.c_int64()
+    st = lib().gemm_conv2d_out_dims(ctypes.byref(desc), ctypes.byref(P), ctypes.byref(Q))
+    return st, P.value, Q.value
+
+
+def gemm_conv2d_plan(desc: gemm_conv2d_desc_t, out_dtype=GEMM_OUT_BF16, opts: gemm_options_t | None = None):
+    """(status, gemm_plan_t) of the convolution's implicit GEMM on the current device."""
+    plan = gemm_plan_t()
+    st = lib().gemm_conv2d_plan(ctypes.byref(desc), out_dtype, ctypes.byref(opts) if opts is not None else None,
+                                ctypes.byref(plan))
+    return st, plan
+
+
+def gemm_conv2d_fprop_bf16(desc: gemm_conv2d_desc_t, x, w, y, out_dtype, opts: gemm_options_t | None, stream) -> int:
+    """Status code of the C call (device pointers as integers)."""
+    return lib().gemm_conv2d_fprop_bf16(ctypes.byref(desc), x, w, y, out_dtype,
+                                        ctypes.byref(opts) if opts is not None else None, stream)
 
 
 def gemm_reserve_workspace(nbytes: int) -> int:
@@ -325,4 +359,52 @@ def matmul(A, B, *, out_dtype=None, out=None, split_k: int = 0, non_persistent: 
                       a_layout, b_layout, odt, opts, _stream_handle(stream))
     if st:
         raise GemmError(st, "gemm_bf16_ex")
+    return out
+
+
+def conv2d(x, w, *, pad=(0, 0), stride=(1, 1), dil=(1, 1), out_dtype=None, out=None, split_k: int = 0,
+           no_stream_k: bool = False, stream=None, alpha: float = 1.0, beta: float = 0.0, bias=None,
+           activation: str = "none", timeout_ms: int = 0):
+    """y = conv2d(x, w) through ``gemm_conv2d_fprop_bf16`` (an implicit GEMM).
+
+    ``x``: (N, H, W, C) contiguous torch.bfloat16 CUDA tensor (NHWC).
+    ``w``: (K, R, S, C) contiguous torch.bfloat16 CUDA tensor (KRSC).
+    ``out``: optional contiguous (N, P, Q, K) float32 or bfloat16 tensor.
+    The epilogue arguments are those of :func:`matmul`, with the bias per
+    output channel.  Raises :class:`GemmError` on a non-zero status."""
+    import torch
+    if x.dtype != torch.bfloat16 or w.dtype != torch.bfloat16:
+        raise TypeError("x and w must be torch.bfloat16")
+    if x.dim() != 4 or w.dim() != 4 or not x.is_contiguous() or not w.is_contiguous():
+        raise ValueError("x must be a contiguous (N, H, W, C) tensor and w a contiguous (K, R, S, C) tensor")
+    N, H, W, C = x.shape
+    K, R, S, C2 = w.shape
+    if C2 != C:
+        raise ValueError(f"channel counts differ: {C} vs {C2}")
+    desc = gemm_conv2d_desc_t(N=N, H=H, W=W, C=C, K=K, R=R, S=S, pad_h=pad[0], pad_w=pad[1], stride_h=stride[0],
+                              stride_w=stride[1], dil_h=dil[0], dil_w=dil[1])
+    st, P, Q = gemm_conv2d_out_dims(desc)
+    if st:
+        raise GemmError(st, "gemm_conv2d_out_dims")
+    if activation not in ACTIVATIONS:
+        raise ValueError(f"activation must be one of {sorted(ACTIVATIONS)}")
+    if beta != 0.0 and out is None:
+        raise ValueError("beta != 0 reads the previous output: pass out=")
+    if out is None:
+        out = torch.empty((N, P, Q, K), dtype=out_dtype if out_dtype is not None else torch.bfloat16, device=x.device)
+    if tuple(out.shape) != (N, P, Q, K) or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous ({N}, {P}, {Q}, {K}) tensor")
+    odt = {torch.float32: GEMM_OUT_F32, torch.bfloat16: GEMM_OUT_BF16}.get(out.dtype)
+    if odt is None:
+        raise TypeError("out must be float32 or bfloat16")
+    opts = gemm_options_t(split_k=split_k, no_stream_k=int(no_stream_k), timeout_ms=timeout_ms)
+    if alpha != 1.0 or beta != 0.0 or bias is not None or activation != "none":
+        if bias is not None and (bias.dtype != torch.float32 or bias.numel() != K or not bias.is_contiguous()):
+            raise ValueError("bias must be a contiguous float32 tensor of K values")
+        epi = gemm_epilogue_t(alpha=alpha, beta=beta, bias=bias.data_ptr() if bias is not None else None,
+                              activation=ACTIVATIONS[activation])
+        opts.epilogue = ctypes.pointer(epi)
+    st = gemm_conv2d_fprop_bf16(desc, x.data_ptr(), w.data_ptr(), out.data_ptr(), odt, opts, _stream_handle(stream))
+    if st:
+        raise GemmError(st, "gemm_conv2d_fprop_bf16")
     return out

@@ -60,6 +60,17 @@ struct KernelParams {
     unsigned long long timeout_ns;
     int skip_load;               // test hook (0 = off)
     int a_mn, b_mn;              // 1: the operand is MN-major in memory (A column-major, B row-major)
+    // Implicit-GEMM convolution (conv = 1, single-CTA variant with 64-wide
+    // k-tiles): row m of A is output pixel m = (n, p, q) of an N x P x Q
+    // output, k-tile b is filter tap b / ncb (r = tap / S, s = tap % S) and
+    // channel block b % ncb of 64 channels.  The producer warp gathers A from
+    // x (NHWC) with cp.async; B is the filter (KRSC) as a 3-D tensor map
+    // (channels, taps, output channels).
+    int conv;
+    int cv_H, cv_W, cv_C, cv_S, cv_PQ, cv_Q, cv_taps;
+    int pad_h, pad_w, str_h, str_w, dil_h, dil_w;
+    int ncb;
+    const uint16_t *x;
     // fused epilogue (epi = 1): C := act(alpha * acc + beta * C + bias[n])
     int epi;
     float alpha, beta;
@@ -405,7 +416,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(bar(BAR_FULL + s), 1);    // leader's producer arrive + both CTAs' bytes
+            // leader's producer arrive + both CTAs' bytes; a convolution adds the
+            // 32 producer lanes' cp.async arrivals
+            ptx::mbar_init(bar(BAR_FULL + s), p.conv ? 1 + 32 : 1);
             ptx::mbar_init(bar(BAR_EMPTY + s), 1);   // MMA commit
         }
         for (int b = 0; b < ACC_BUFS; ++b) {
@@ -444,7 +457,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // the operands of its first STAGES k-tiles: L2 is the point of coherence,
     // so if the previous kernel writes them, the loads after the wait still
     // see its data.
-    if (warp == 0 && lane == 0) {
+    if (warp == 0 && lane == 0 && !p.conv) {
         Schedule first(p, cluster);
         Unit w0;
         if (first.next(p, w0)) {
@@ -462,7 +475,81 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::grid_dependency_wait();
     ptx::grid_launch_dependents();
 
-    if (warp == 0) {
+    if (warp == 0 && p.conv) {
+        // ---------------- producer of a convolution: gather A, TMA for B ------
+        if constexpr (!PAIR) {
+            // Lane l fills rows l, l+32, l+64, l+96 of each A stage: the 64
+            // channels (eight 16-byte pieces) of the input pixel that output
+            // pixel (row) reads at the stage's filter tap, or zeros where the
+            // tap falls in the padding, past the last pixel or past C.  The
+            // pieces go where the 128-byte swizzle puts them: piece j of row r
+            // at r * 128 + ((j ^ (r & 7)) << 4).
+            uint32_t it = 0;
+            bool ok = true;
+            Schedule sched(p, cluster);
+            Unit w;
+            while (ok && sched.next(p, w)) {
+                int rn[4], rh[4], rw[4];
+                bool rv[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int m = w.tm * CTA_ROWS + lane + 32 * i;
+                    rv[i] = m < p.M;
+                    const int n = m / p.cv_PQ;
+                    const int pq = m - n * p.cv_PQ;
+                    const int pp = pq / p.cv_Q;
+                    rn[i] = n;
+                    rh[i] = pp * p.str_h - p.pad_h;
+                    rw[i] = (pq - pp * p.cv_Q) * p.str_w - p.pad_w;
+                }
+                for (int kb = 0; kb < w.kb_count; ++kb, ++it) {
+                    const uint32_t s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    const bool got = wait_phase<false>(bar(BAR_EMPTY + s), ph ^ 1u, abort_flag, p.timeout_ns,
+                                                       SITE_PRODUCER, true);
+                    if (!__all_sync(0xffffffffu, got)) {
+                        ok = false;
+                        break;
+                    }
+                    const int b = w.kb_begin + kb;
+                    const int tap = b / p.ncb;
+                    const int c0 = (b - tap * p.ncb) * TILE_K;
+                    const int r = tap / p.cv_S;
+                    const int sx = tap - r * p.cv_S;
+                    if (lane == 0) {
+                        ptx::mbar_arrive_expect_tx(bar(BAR_FULL + s), static_cast<uint32_t>(B_BOX));
+                        ptx::tma_load_3d(sB + s * V.b_stage, &tmap_b, bar(BAR_FULL + s), c0, tap, w.tn * BN);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int row = lane + 32 * i;
+                        const int h = rh[i] + r * p.dil_h;
+                        const int wx = rw[i] + sx * p.dil_w;
+                        const bool inside = rv[i] && h >= 0 && h < p.cv_H && wx >= 0 && wx < p.cv_W;
+                        const uint16_t *src =
+                            p.x + ((static_cast<long long>(rn[i]) * p.cv_H + h) * p.cv_W + wx) * p.cv_C + c0;
+                        const uint32_t dst = sA + s * V.a_stage + static_cast<uint32_t>(row) * 128u;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const bool live = inside && c0 + 8 * j < p.cv_C;
+                            ptx::cp_async_16(dst + ((static_cast<uint32_t>(j) ^ (static_cast<uint32_t>(row) & 7u)) << 4),
+                                             live ? static_cast<const void *>(src + 8 * j) : static_cast<const void *>(p.x),
+                                             live ? 16u : 0u);
+                        }
+                    }
+                    ptx::cp_async_mbar_arrive_noinc(bar(BAR_FULL + s));
+                }
+            }
+            ptx::cp_async_wait_all();   // no copy may still land in this CTA's memory when it exits
+            if (lane == 0) {
+                const uint32_t first = it > static_cast<uint32_t>(STAGES) ? it - STAGES : 0u;
+                for (uint32_t j = first; j < it; ++j) {
+                    wait_phase<false>(bar(BAR_FULL + j % STAGES), (j / STAGES) & 1u, abort_flag, p.timeout_ns,
+                                      SITE_DRAIN, false);
+                }
+            }
+        }
+    } else if (warp == 0) {
         // ---------------- producer: TMA copies into the ring ----------------
         if (lane == 0) {
             uint32_t it = 0, issued = 0;
@@ -545,6 +632,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     ptx::tc_fence_after_sync();
+                    // a convolution's A arrived by cp.async (the generic proxy):
+                    // order it before the Tensor Core's (async-proxy) reads
+                    if (p.conv) ptx::fence_proxy_async_shared();
 #pragma unroll
                     for (int k = 0; k < TK / MMA_K; ++k) {
                         // K-major: box k/4 of the k-tile; inside it, the next 16
@@ -1289,10 +1379,31 @@ struct PartialBuffer {
 
 // Plan and enqueue one GEMM whose arguments have passed check_problem and
 // check_operands, with M, N, K > 0.
+// A convolution's implicit GEMM: the problem and the output extent.
+struct ConvLaunch {
+    const gemm_conv2d_desc_t *d;
+    int64_t P, Q;
+    int ncb;   // 64-channel blocks per tap
+};
+
+// The filter (K x R x S x C, KRSC) as a 3-D tensor map (channels, taps,
+// output channels), read in boxes of 64 channels x 1 tap x `box_rows` output
+// channels: channels past C and output channels past K read as zero.
+gemm_status_t encode_filter(CUtensorMap *map, const void *w, int64_t C, int64_t taps, int64_t K, int box_rows) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(C), static_cast<cuuint64_t>(taps), static_cast<cuuint64_t>(K)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(C) * 2, static_cast<cuuint64_t>(taps * C) * 2};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(TILE_K), 1, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t elem_strides[3] = {1, 1, 1};
+    CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(w), dims, strides, box,
+                                elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_LAUNCH;
+}
+
 gemm_status_t launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
                           void *C, int64_t ldc, gemm_layout_t layout_a, gemm_layout_t layout_b,
                           gemm_dtype_t out_dtype, const gemm_options_t &o, cudaStream_t s, DeviceState &ds,
-                          const PartialBuffer &pb) {
+                          const PartialBuffer &pb, const ConvLaunch *conv = nullptr) {
     const int variant = choose_variant(M, N, K, o.kernel_variant, o.split_k, ds.desc);
     const VariantInfo vi = variant_info(variant);
     gemm_plan_t plan;
@@ -1322,10 +1433,20 @@ gemm_status_t launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_
 
     CUtensorMap tmap_a, tmap_b, tmap_c;
     const bool a_mn = layout_a == GEMM_COL_MAJOR, b_mn = layout_b == GEMM_ROW_MAJOR;
-    st = a_mn ? encode_operand(&tmap_a, A, M, K, lda, vi.tile_k) : encode_operand(&tmap_a, A, K, M, lda, CTA_ROWS);
-    if (st != GEMM_OK) return st;
-    st = b_mn ? encode_operand(&tmap_b, B, N, K, ldb, vi.tile_k) : encode_operand(&tmap_b, B, K, N, ldb, vi.b_rows);
-    if (st != GEMM_OK) return st;
+    if (conv) {
+        // A is gathered by the kernel; its map is not read, so it describes x
+        // as pixels of C channels (any valid map would do)
+        const gemm_conv2d_desc_t &d = *conv->d;
+        st = encode_operand(&tmap_a, A, d.C, d.N * d.H * d.W, d.C, CTA_ROWS);
+        if (st != GEMM_OK) return st;
+        st = encode_filter(&tmap_b, B, d.C, d.R * d.S, d.K, vi.b_rows);
+        if (st != GEMM_OK) return st;
+    } else {
+        st = a_mn ? encode_operand(&tmap_a, A, M, K, lda, vi.tile_k) : encode_operand(&tmap_a, A, K, M, lda, CTA_ROWS);
+        if (st != GEMM_OK) return st;
+        st = b_mn ? encode_operand(&tmap_b, B, N, K, ldb, vi.tile_k) : encode_operand(&tmap_b, B, K, N, ldb, vi.b_rows);
+        if (st != GEMM_OK) return st;
+    }
     st = encode_output(&tmap_c, C, N, M, ldc, out_dtype == GEMM_OUT_BF16);
     if (st != GEMM_OK) return st;
 
@@ -1348,6 +1469,25 @@ gemm_status_t launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_
     p.skip_load = o.debug_skip_load;
     p.a_mn = a_mn ? 1 : 0;
     p.b_mn = b_mn ? 1 : 0;
+    if (conv) {
+        const gemm_conv2d_desc_t &d = *conv->d;
+        p.conv = 1;
+        p.cv_H = static_cast<int>(d.H);
+        p.cv_W = static_cast<int>(d.W);
+        p.cv_C = static_cast<int>(d.C);
+        p.cv_S = static_cast<int>(d.S);
+        p.cv_PQ = static_cast<int>(conv->P * conv->Q);
+        p.cv_Q = static_cast<int>(conv->Q);
+        p.cv_taps = static_cast<int>(d.R * d.S);
+        p.pad_h = d.pad_h;
+        p.pad_w = d.pad_w;
+        p.str_h = d.stride_h;
+        p.str_w = d.stride_w;
+        p.dil_h = d.dil_h;
+        p.dil_w = d.dil_w;
+        p.ncb = conv->ncb;
+        p.x = static_cast<const uint16_t *>(A);
+    }
     const EpilogueArgs ep = epilogue_args(o);
     p.epi = ep.epi;
     p.alpha = ep.alpha;
@@ -1540,6 +1680,80 @@ gemm_status_t gemm_get_device_status(void *stream, unsigned int *where) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------ convolution (implicit GEMM)
+
+namespace gemm {
+namespace {
+
+// The implicit GEMM of a convolution: M = N P Q, N = K, K = R S (C rounded up
+// to 64-channel blocks), on the single-CTA variant; the options as given.
+struct ConvProblem {
+    ConvLaunch launch;
+    int64_t M, N, K;
+    gemm_options_t o;
+};
+
+gemm_status_t conv_problem(const gemm_conv2d_desc_t *d, const gemm_options_t *opts, ConvProblem *cp) {
+    int64_t P = 0, Q = 0;
+    gemm_status_t st = conv_check(d, &P, &Q);
+    if (st != GEMM_OK) return st;
+    gemm_options_t o{};
+    if (opts) o = *opts;
+    if (o.kernel_variant != VARIANT_AUTO && o.kernel_variant != VARIANT_1SM_128x256) return GEMM_ERR_NOT_SUPPORTED;
+    o.kernel_variant = VARIANT_1SM_128x256;
+    const int ncb = static_cast<int>((d->C + TILE_K - 1) / TILE_K);
+    cp->launch = ConvLaunch{d, P, Q, ncb};
+    cp->M = d->N * P * Q;
+    cp->N = d->K;
+    cp->K = d->R * d->S * ncb * TILE_K;
+    cp->o = o;
+    return GEMM_OK;
+}
+
+}  // namespace
+}  // namespace gemm
+
+extern "C" gemm_status_t gemm_conv2d_plan(const gemm_conv2d_desc_t *d, gemm_dtype_t out_dtype,
+                                          const gemm_options_t *opts, gemm_plan_t *plan) {
+    if (!plan) return GEMM_ERR_INVALID_VALUE;
+    ConvProblem cp;
+    gemm_status_t st = conv_problem(d, opts, &cp);
+    if (st != GEMM_OK) return st;
+    st = check_problem(cp.M, cp.N, cp.K, GEMM_ROW_MAJOR, GEMM_COL_MAJOR, out_dtype, cp.o.split_k);
+    if (st != GEMM_OK) return st;
+    int device = 0;
+    DeviceState *ds = nullptr;
+    st = current_device(&device, &ds);
+    if (st != GEMM_OK) return st;
+    return make_plan(cp.M, cp.N, cp.K, GEMM_ROW_MAJOR, GEMM_COL_MAJOR, out_dtype, cp.o, true, ds->desc,
+                     kernel_desc(VARIANT_1SM_128x256, ds->var[VARIANT_1SM_128x256]), plan);
+}
+
+extern "C" gemm_status_t gemm_conv2d_fprop_bf16(const gemm_conv2d_desc_t *d, const void *x, const void *w, void *y,
+                                                gemm_dtype_t out_dtype, const gemm_options_t *opts, void *stream) {
+    ConvProblem cp;
+    gemm_status_t st = conv_problem(d, opts, &cp);
+    if (st != GEMM_OK) return st;
+    const gemm_options_t &o = cp.o;
+    st = check_problem(cp.M, cp.N, cp.K, GEMM_ROW_MAJOR, GEMM_COL_MAJOR, out_dtype, o.split_k);
+    if (st != GEMM_OK) return st;
+    if (o.timeout_ms < 0 || o.raster_group_m < 0 || o.debug_skip_load != 0) return GEMM_ERR_INVALID_VALUE;
+    st = check_epilogue(o);
+    if (st != GEMM_OK) return st;
+    if (!x || !w || !y) return GEMM_ERR_INVALID_VALUE;
+    const int esize = out_dtype == GEMM_OUT_BF16 ? 2 : 4;
+    if (reinterpret_cast<uintptr_t>(x) % 16 != 0 || reinterpret_cast<uintptr_t>(w) % 16 != 0 ||
+        reinterpret_cast<uintptr_t>(y) % 16 != 0 || d->C % 8 != 0 || (d->K * esize) % 16 != 0)
+        return GEMM_ERR_MISALIGNED;
+
+    int device = 0;
+    DeviceState *ds = nullptr;
+    st = current_device(&device, &ds);
+    if (st != GEMM_OK) return st;
+    return launch_gemm(cp.M, cp.N, cp.K, x, d->C, w, cp.K, y, d->K, GEMM_ROW_MAJOR, GEMM_COL_MAJOR, out_dtype, o,
+                       static_cast<cudaStream_t>(stream), *ds, PartialBuffer{false, nullptr, 0}, &cp.launch);
+}
 
 // ------------------------------------------- split-K without device allocation
 //

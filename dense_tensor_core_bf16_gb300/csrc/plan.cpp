@@ -30,6 +30,28 @@ gemm_status_t check_problem(int64_t M, int64_t N, int64_t K, gemm_layout_t la, g
     return GEMM_OK;
 }
 
+// A convolution's fields and output extent (see gemm_conv2d_desc_t).
+gemm_status_t conv_check(const gemm_conv2d_desc_t *d, int64_t *P, int64_t *Q) {
+    if (!d) return GEMM_ERR_INVALID_VALUE;
+    const int64_t big = INT_MAX;
+    if (d->N < 1 || d->H < 1 || d->W < 1 || d->C < 1 || d->K < 1 || d->R < 1 || d->S < 1) return GEMM_ERR_INVALID_VALUE;
+    if (d->N > big || d->H > big || d->W > big || d->C > big || d->K > big || d->R > big || d->S > big)
+        return GEMM_ERR_INVALID_VALUE;
+    if (d->pad_h < 0 || d->pad_w < 0 || d->stride_h < 1 || d->stride_w < 1 || d->dil_h < 1 || d->dil_w < 1)
+        return GEMM_ERR_INVALID_VALUE;
+    const int64_t p = (d->H + 2 * static_cast<int64_t>(d->pad_h) - d->dil_h * (d->R - 1) - 1);
+    const int64_t q = (d->W + 2 * static_cast<int64_t>(d->pad_w) - d->dil_w * (d->S - 1) - 1);
+    if (p < 0 || q < 0) return GEMM_ERR_INVALID_VALUE;   // the filter does not fit the padded image
+    const int64_t Pv = p / d->stride_h + 1, Qv = q / d->stride_w + 1;
+    // N P Q, the padded R S C and the input's element count stay in int range
+    if (d->N * Pv > big || d->N * Pv * Qv > big || d->R * d->S > big || d->R * d->S * cdiv(d->C, TILE_K) * TILE_K > big ||
+        d->N * d->H > big || d->N * d->H * d->W > big)
+        return GEMM_ERR_INVALID_VALUE;
+    if (P) *P = Pv;
+    if (Q) *Q = Qv;
+    return GEMM_OK;
+}
+
 int round_regs(int regs_per_thread) { return (regs_per_thread + 7) / 8 * 8; }
 
 gemm_status_t occupancy(const gemm_kernel_desc_t &k, const gemm_device_desc_t &d, int *b_out, int *lim_out) {
@@ -205,6 +227,10 @@ gemm_status_t gemm_plan_for_device(int64_t M, int64_t N, int64_t K, gemm_layout_
     gemm_options_t o{};
     if (opts) o = *opts;
     return gemm::make_plan(M, N, K, layout_a, layout_b, out_dtype, o, true, *dev, *kern, plan);
+}
+
+gemm_status_t gemm_conv2d_out_dims(const gemm_conv2d_desc_t *d, int64_t *P, int64_t *Q) {
+    return gemm::conv_check(d, P, Q);
 }
 
 const char *gemm_status_string(gemm_status_t s) {

@@ -331,6 +331,52 @@ gemm_status_t gemm_bf16_ex(int64_t M, int64_t N, int64_t K,
                            gemm_layout_t layout_a, gemm_layout_t layout_b,
                            gemm_dtype_t out_dtype, const gemm_options_t *opts, void *stream);
 
+/*
+ * 2-D convolution (forward) as an implicit GEMM.
+ *
+ * Convolutions reach the Tensor Cores through im2col / implicit GEMM (lesson
+ * "The Tensor Core", the paragraph on what work the Tensor Cores speed up):
+ *
+ *   y[n][p][q][k] = sum over r < R, s < S, c < C of
+ *                   x[n][p*stride_h - pad_h + r*dil_h][q*stride_w - pad_w + s*dil_w][c] * w[k][r][s][c]
+ *
+ * with x zero outside the image (the padding).  It is the GEMM
+ * C (N P Q x K) = A (N P Q x R S C) . B (R S C x K) in which row m of A is the
+ * receptive field of output pixel m -- never formed in memory: the kernel's
+ * producer warp gathers each A tile from x as it goes.  P and Q are
+ * (H + 2 pad - dil (R - 1) - 1) / stride + 1 (integer division, >= 1).
+ *
+ *   x: N x H x W x C bf16, NHWC, dense.       w: K x R x S x C bf16, KRSC, dense.
+ *   y: N x P x Q x K, dense (row m = (n P + p) Q + q of an N P Q x K
+ *      row-major matrix), fp32 or bf16 per out_dtype.
+ * Requirements: every size >= 1, strides and dilations >= 1, paddings >= 0;
+ * C a multiple of 8 (16-byte pixel rows); K a multiple of 8 for bf16 y or 4
+ * for fp32 y; x, w, y on 16-byte boundaries (GEMM_ERR_MISALIGNED otherwise);
+ * N P Q and R S C below 2^31.  The options work as for gemm_bf16_ex (split-K,
+ * stream-K, the fused epilogue -- a bias per output channel k); the kernel
+ * is the single-CTA 128 x 256 variant (kernel_variant must be 0 or 1).
+ */
+typedef struct {
+    int64_t N, H, W, C;          /* input */
+    int64_t K, R, S;             /* filter: K output channels of R x S taps */
+    int pad_h, pad_w;
+    int stride_h, stride_w;
+    int dil_h, dil_w;
+} gemm_conv2d_desc_t;
+
+/* The output extent P x Q of `d`; GEMM_ERR_INVALID_VALUE if it is empty or a
+ * field is out of range. */
+gemm_status_t gemm_conv2d_out_dims(const gemm_conv2d_desc_t *d, int64_t *P, int64_t *Q);
+
+/* The plan of the implicit GEMM (M = N P Q, N = K, K = R S C rounded up to
+ * whole 64-channel blocks per tap) on the current device. */
+gemm_status_t gemm_conv2d_plan(const gemm_conv2d_desc_t *d, gemm_dtype_t out_dtype, const gemm_options_t *opts,
+                               gemm_plan_t *plan);
+
+/* y = conv2d(x, w) on `stream` (opts may be NULL). */
+gemm_status_t gemm_conv2d_fprop_bf16(const gemm_conv2d_desc_t *d, const void *x, const void *w, void *y,
+                                     gemm_dtype_t out_dtype, const gemm_options_t *opts, void *stream);
+
 /* Grow the current device's split-K workspace to at least `bytes`. */
 gemm_status_t gemm_reserve_workspace(size_t bytes);
 

@@ -45,7 +45,7 @@ def test_binding_structs_match_the_header(tmp_path):
     import subprocess
     structs = {"gemm_device_desc_t": g.gemm_device_desc_t, "gemm_kernel_desc_t": g.gemm_kernel_desc_t,
                "gemm_plan_t": g.gemm_plan_t, "gemm_options_t": g.gemm_options_t,
-               "gemm_epilogue_t": g.gemm_epilogue_t}
+               "gemm_epilogue_t": g.gemm_epilogue_t, "gemm_conv2d_desc_t": g.gemm_conv2d_desc_t}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "gemm_bf16.h"', "int main(void) {"]
     for name, cls in structs.items():
         lines.append(f'  printf("{name} %zu\\n", sizeof({name}));')
@@ -312,3 +312,41 @@ def test_plan_argument_checks():
     too_big.smem_per_cta = 240000
     st, _ = g.gemm_plan_for_device(4, 4, 4, 0, 1, 0, o1, dev(), too_big)
     assert st == 1
+
+
+def _conv(**kw):
+    d = dict(N=2, H=9, W=11, C=64, K=128, R=3, S=3, pad_h=1, pad_w=1, stride_h=1, stride_w=1, dil_h=1, dil_w=1)
+    d.update(kw)
+    return g.gemm_conv2d_desc_t(**d)
+
+
+def test_conv2d_out_dims_match_the_oracle_formula():
+    import oracle
+    for H in (1, 5, 9, 17):
+        for R in (1, 2, 3, 5):
+            for pad in (0, 1, 2):
+                for stride in (1, 2, 3):
+                    for dil in (1, 2):
+                        st, P, Q = g.gemm_conv2d_out_dims(_conv(H=H, W=H + 3, R=R, S=R, pad_h=pad, pad_w=pad,
+                                                                stride_h=stride, stride_w=stride, dil_h=dil, dil_w=dil))
+                        p = oracle.conv2d_out_size(H, R, pad, stride, dil)
+                        q = oracle.conv2d_out_size(H + 3, R, pad, stride, dil)
+                        if p >= 1 and q >= 1:
+                            assert (st, P, Q) == (0, p, q)
+                        else:
+                            assert st == 1
+
+
+def test_conv2d_argument_checks_before_any_cuda_call():
+    x, w, y = 256, 512, 768   # fake, 16-byte aligned: every case below is rejected before use
+    call = lambda d, out=0, opts=None, xp=x: g.gemm_conv2d_fprop_bf16(d, xp, w, y, out, opts, None)
+    assert call(_conv(N=0)) == 1
+    assert call(_conv(stride_h=0)) == 1
+    assert call(_conv(pad_w=-1)) == 1
+    assert call(_conv(H=2, R=5, pad_h=0)) == 1                 # filter larger than the padded image
+    assert call(_conv(C=60)) == 2                               # 120-byte pixel rows
+    assert call(_conv(K=66)) == 2                               # fp32 output rows of 264 bytes
+    assert call(_conv(K=60), out=1) == 2                        # bf16 output rows of 120 bytes
+    assert call(_conv(), xp=x + 8) == 2                         # x off its 16-byte boundary
+    assert call(_conv(), opts=g.options(kernel_variant=2)) == 3    # only the single-CTA variant
+    assert call(_conv(), opts=g.options(debug_skip_load=1)) == 1
