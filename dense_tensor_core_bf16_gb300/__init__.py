@@ -364,7 +364,7 @@ def matmul(A, B, *, out_dtype=None, out=None, split_k: int = 0, non_persistent: 
 
 def conv2d(x, w, *, pad=(0, 0), stride=(1, 1), dil=(1, 1), out_dtype=None, out=None, split_k: int = 0,
            no_stream_k: bool = False, stream=None, alpha: float = 1.0, beta: float = 0.0, bias=None,
-           activation: str = "none", timeout_ms: int = 0):
+           activation: str = "none", timeout_ms: int = 0, kernel_variant: int = 0):
     """y = conv2d(x, w) through ``gemm_conv2d_fprop_bf16`` (an implicit GEMM).
 
     ``x``: (N, H, W, C) contiguous torch.bfloat16 CUDA tensor (NHWC).
@@ -397,7 +397,8 @@ def conv2d(x, w, *, pad=(0, 0), stride=(1, 1), dil=(1, 1), out_dtype=None, out=N
     odt = {torch.float32: GEMM_OUT_F32, torch.bfloat16: GEMM_OUT_BF16}.get(out.dtype)
     if odt is None:
         raise TypeError("out must be float32 or bfloat16")
-    opts = gemm_options_t(split_k=split_k, no_stream_k=int(no_stream_k), timeout_ms=timeout_ms)
+    opts = gemm_options_t(split_k=split_k, no_stream_k=int(no_stream_k), timeout_ms=timeout_ms,
+                          kernel_variant=kernel_variant)
     if alpha != 1.0 or beta != 0.0 or bias is not None or activation != "none":
         if bias is not None and (bias.dtype != torch.float32 or bias.numel() != K or not bias.is_contiguous()):
             raise ValueError("bias must be a contiguous float32 tensor of K values")

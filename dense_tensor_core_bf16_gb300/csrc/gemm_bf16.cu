@@ -60,17 +60,16 @@ struct KernelParams {
     unsigned long long timeout_ns;
     int skip_load;               // test hook (0 = off)
     int a_mn, b_mn;              // 1: the operand is MN-major in memory (A column-major, B row-major)
-    // Implicit-GEMM convolution (conv = 1, single-CTA variant with 64-wide
-    // k-tiles): row m of A is output pixel m = (n, p, q) of an N x P x Q
-    // output, k-tile b is filter tap b / ncb (r = tap / S, s = tap % S) and
-    // channel block b % ncb of 64 channels.  The producer warp gathers A from
-    // x (NHWC) with cp.async; B is the filter (KRSC) as a 3-D tensor map
+    // Implicit-GEMM convolution (conv = 1): row m of A is output pixel
+    // m = (n, p, q) of an N x P x Q output; box i (64 wide) of the GEMM's K is
+    // filter tap i / ncb (r = tap / S, s = tap % S), channels 64 (i % ncb) on.
+    // tmap_a is an im2col map of x (NHWC): a box is the 128 pixels of the
+    // CTA's rows at one tap; tmap_b is the filter (KRSC) as a 3-D map
     // (channels, taps, output channels).
     int conv;
-    int cv_H, cv_W, cv_C, cv_S, cv_PQ, cv_Q, cv_taps;
+    int cv_S, cv_PQ, cv_Q, cv_taps;
     int pad_h, pad_w, str_h, str_w, dil_h, dil_w;
     int ncb;
-    const uint16_t *x;
     // fused epilogue (epi = 1): C := act(alpha * acc + beta * C + bias[n])
     int epi;
     float alpha, beta;
@@ -416,9 +415,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            // leader's producer arrive + both CTAs' bytes; a convolution adds the
-            // 32 producer lanes' cp.async arrivals
-            ptx::mbar_init(bar(BAR_FULL + s), p.conv ? 1 + 32 : 1);
+            ptx::mbar_init(bar(BAR_FULL + s), 1);    // leader's producer arrive + both CTAs' bytes
             ptx::mbar_init(bar(BAR_EMPTY + s), 1);   // MMA commit
         }
         for (int b = 0; b < ACC_BUFS; ++b) {
@@ -475,81 +472,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::grid_dependency_wait();
     ptx::grid_launch_dependents();
 
-    if (warp == 0 && p.conv) {
-        // ---------------- producer of a convolution: gather A, TMA for B ------
-        if constexpr (!PAIR) {
-            // Lane l fills rows l, l+32, l+64, l+96 of each A stage: the 64
-            // channels (eight 16-byte pieces) of the input pixel that output
-            // pixel (row) reads at the stage's filter tap, or zeros where the
-            // tap falls in the padding, past the last pixel or past C.  The
-            // pieces go where the 128-byte swizzle puts them: piece j of row r
-            // at r * 128 + ((j ^ (r & 7)) << 4).
-            uint32_t it = 0;
-            bool ok = true;
-            Schedule sched(p, cluster);
-            Unit w;
-            while (ok && sched.next(p, w)) {
-                int rn[4], rh[4], rw[4];
-                bool rv[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int m = w.tm * CTA_ROWS + lane + 32 * i;
-                    rv[i] = m < p.M;
-                    const int n = m / p.cv_PQ;
-                    const int pq = m - n * p.cv_PQ;
-                    const int pp = pq / p.cv_Q;
-                    rn[i] = n;
-                    rh[i] = pp * p.str_h - p.pad_h;
-                    rw[i] = (pq - pp * p.cv_Q) * p.str_w - p.pad_w;
-                }
-                for (int kb = 0; kb < w.kb_count; ++kb, ++it) {
-                    const uint32_t s = it % STAGES;
-                    const uint32_t ph = (it / STAGES) & 1u;
-                    const bool got = wait_phase<false>(bar(BAR_EMPTY + s), ph ^ 1u, abort_flag, p.timeout_ns,
-                                                       SITE_PRODUCER, true);
-                    if (!__all_sync(0xffffffffu, got)) {
-                        ok = false;
-                        break;
-                    }
-                    const int b = w.kb_begin + kb;
-                    const int tap = b / p.ncb;
-                    const int c0 = (b - tap * p.ncb) * TILE_K;
-                    const int r = tap / p.cv_S;
-                    const int sx = tap - r * p.cv_S;
-                    if (lane == 0) {
-                        ptx::mbar_arrive_expect_tx(bar(BAR_FULL + s), static_cast<uint32_t>(B_BOX));
-                        ptx::tma_load_3d(sB + s * V.b_stage, &tmap_b, bar(BAR_FULL + s), c0, tap, w.tn * BN);
-                    }
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int row = lane + 32 * i;
-                        const int h = rh[i] + r * p.dil_h;
-                        const int wx = rw[i] + sx * p.dil_w;
-                        const bool inside = rv[i] && h >= 0 && h < p.cv_H && wx >= 0 && wx < p.cv_W;
-                        const uint16_t *src =
-                            p.x + ((static_cast<long long>(rn[i]) * p.cv_H + h) * p.cv_W + wx) * p.cv_C + c0;
-                        const uint32_t dst = sA + s * V.a_stage + static_cast<uint32_t>(row) * 128u;
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const bool live = inside && c0 + 8 * j < p.cv_C;
-                            ptx::cp_async_16(dst + ((static_cast<uint32_t>(j) ^ (static_cast<uint32_t>(row) & 7u)) << 4),
-                                             live ? static_cast<const void *>(src + 8 * j) : static_cast<const void *>(p.x),
-                                             live ? 16u : 0u);
-                        }
-                    }
-                    ptx::cp_async_mbar_arrive_noinc(bar(BAR_FULL + s));
-                }
-            }
-            ptx::cp_async_wait_all();   // no copy may still land in this CTA's memory when it exits
-            if (lane == 0) {
-                const uint32_t first = it > static_cast<uint32_t>(STAGES) ? it - STAGES : 0u;
-                for (uint32_t j = first; j < it; ++j) {
-                    wait_phase<false>(bar(BAR_FULL + j % STAGES), (j / STAGES) & 1u, abort_flag, p.timeout_ns,
-                                      SITE_DRAIN, false);
-                }
-            }
-        }
-    } else if (warp == 0) {
+    if (warp == 0) {
         // ---------------- producer: TMA copies into the ring ----------------
         if (lane == 0) {
             uint32_t it = 0, issued = 0;
@@ -559,6 +482,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             while (ok && sched.next(p, w)) {
                 const int row_a = w.tm * V.tile_m + static_cast<int>(rank) * CTA_ROWS;
                 const int row_b = w.tn * BN + static_cast<int>(rank) * V.b_rows;
+                // convolution: the window origin of this CTA's first output pixel
+                int cv_n = 0, cv_h = 0, cv_w = 0;
+                if (p.conv) {
+                    cv_n = row_a / p.cv_PQ;
+                    const int pq = row_a - cv_n * p.cv_PQ;
+                    const int pp = pq / p.cv_Q;
+                    cv_h = pp * p.str_h - p.pad_h;
+                    cv_w = (pq - pp * p.cv_Q) * p.str_w - p.pad_w;
+                }
                 for (int kb = 0; kb < w.kb_count; ++kb, ++it) {
                     const uint32_t s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1u;
@@ -582,6 +514,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             ptx::tma_load_2d(dst, map, full, x, y);
                         }
                     };
+                    if (p.conv) {
+                        // box j: 128 pixels x 64 channels of x at one filter tap
+                        // (im2col), and the matching 64 channels of that tap of
+                        // the filter.  Boxes past the last tap point at channel
+                        // 64 ncb (>= C): both read as zeros.
+                        for (int j = 0; j < V.k_boxes; ++j) {
+                            const int bi = (w.kb_begin + kb) * V.k_boxes + j;
+                            int tap = bi / p.ncb;
+                            int c0 = (bi - tap * p.ncb) * TILE_K;
+                            if (tap >= p.cv_taps) {
+                                tap = 0;
+                                c0 = p.ncb * TILE_K;
+                            }
+                            const int r = tap / p.cv_S;
+                            const uint16_t off_h = static_cast<uint16_t>(r * p.dil_h);
+                            const uint16_t off_w = static_cast<uint16_t>((tap - r * p.cv_S) * p.dil_w);
+                            const uint32_t dst_a = sA + s * V.a_stage + j * A_BOX;
+                            const uint32_t dst_b = sB + s * V.b_stage + j * B_BOX;
+                            if constexpr (PAIR) {
+                                ptx::tma_load_im2col_4d_pair(dst_a, &tmap_a, full, c0, cv_w, cv_h, cv_n, off_w, off_h);
+                                ptx::tma_load_3d_pair(dst_b, &tmap_b, full, c0, tap, row_b);
+                            } else {
+                                ptx::tma_load_im2col_4d(dst_a, &tmap_a, full, c0, cv_w, cv_h, cv_n, off_w, off_h);
+                                ptx::tma_load_3d(dst_b, &tmap_b, full, c0, tap, row_b);
+                            }
+                        }
+                        continue;
+                    }
                     const int na = box_count(a_mn, CTA_ROWS), nb = box_count(b_mn, V.b_rows);
                     for (int j = 0; j < na || j < nb; ++j) {
                         if (j < na)
@@ -632,9 +592,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     ptx::tc_fence_after_sync();
-                    // a convolution's A arrived by cp.async (the generic proxy):
-                    // order it before the Tensor Core's (async-proxy) reads
-                    if (p.conv) ptx::fence_proxy_async_shared();
 #pragma unroll
                     for (int k = 0; k < TK / MMA_K; ++k) {
                         // K-major: box k/4 of the k-tile; inside it, the next 16
@@ -1130,6 +1087,7 @@ struct DeviceState {
 std::mutex g_mutex;
 DeviceState g_devices[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
+PFN_cuTensorMapEncodeIm2col_v12000 g_encode_im2col = nullptr;
 
 gemm_status_t query_desc(int device, gemm_device_desc_t *d) {
     struct {
@@ -1213,6 +1171,15 @@ gemm_status_t device_state(int device, DeviceState **out) {
                 qr != cudaDriverEntryPointSuccess || fn == nullptr)
                 return GEMM_ERR_LAUNCH;
             g_encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        if (!g_encode_im2col) {
+            void *fn = nullptr;
+            cudaDriverEntryPointQueryResult qr{};
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &fn, 12000, cudaEnableDefault, &qr) !=
+                    cudaSuccess ||
+                qr != cudaDriverEntryPointSuccess || fn == nullptr)
+                return GEMM_ERR_LAUNCH;
+            g_encode_im2col = reinterpret_cast<PFN_cuTensorMapEncodeIm2col_v12000>(fn);
         }
         ds.ready = true;
     }
@@ -1386,6 +1353,27 @@ struct ConvLaunch {
     int ncb;   // 64-channel blocks per tap
 };
 
+// x (N x H x W x C, NHWC) as an im2col tensor map: a load at window origin
+// (c, w, h, n) with tap offsets (s dil_w, r dil_h) brings `rows` consecutive
+// output pixels x 64 channels.  The pixel box runs over the window origins:
+// from -pad to the last origin whose filter still fits the padded image
+// (lower corner -pad, upper corner pad - dil (filter - 1)), stepping by the
+// convolution's strides; pixels outside the image read as zero.
+gemm_status_t encode_im2col(CUtensorMap *map, const void *x, const gemm_conv2d_desc_t &d, int rows) {
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(d.C), static_cast<cuuint64_t>(d.W), static_cast<cuuint64_t>(d.H),
+                          static_cast<cuuint64_t>(d.N)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(d.C) * 2, static_cast<cuuint64_t>(d.W * d.C) * 2,
+                             static_cast<cuuint64_t>(d.H * d.W * d.C) * 2};
+    int lower[2] = {-d.pad_w, -d.pad_h};
+    int upper[2] = {d.pad_w - d.dil_w * static_cast<int>(d.S - 1), d.pad_h - d.dil_h * static_cast<int>(d.R - 1)};
+    cuuint32_t elem_strides[4] = {1, static_cast<cuuint32_t>(d.stride_w), static_cast<cuuint32_t>(d.stride_h), 1};
+    CUresult r = g_encode_im2col(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(x), dims, strides, lower,
+                                 upper, static_cast<cuuint32_t>(TILE_K), static_cast<cuuint32_t>(rows), elem_strides,
+                                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_INVALID_VALUE;
+}
+
 // The filter (K x R x S x C, KRSC) as a 3-D tensor map (channels, taps,
 // output channels), read in boxes of 64 channels x 1 tap x `box_rows` output
 // channels: channels past C and output channels past K read as zero.
@@ -1434,10 +1422,8 @@ gemm_status_t launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_
     CUtensorMap tmap_a, tmap_b, tmap_c;
     const bool a_mn = layout_a == GEMM_COL_MAJOR, b_mn = layout_b == GEMM_ROW_MAJOR;
     if (conv) {
-        // A is gathered by the kernel; its map is not read, so it describes x
-        // as pixels of C channels (any valid map would do)
         const gemm_conv2d_desc_t &d = *conv->d;
-        st = encode_operand(&tmap_a, A, d.C, d.N * d.H * d.W, d.C, CTA_ROWS);
+        st = encode_im2col(&tmap_a, A, d, CTA_ROWS);
         if (st != GEMM_OK) return st;
         st = encode_filter(&tmap_b, B, d.C, d.R * d.S, d.K, vi.b_rows);
         if (st != GEMM_OK) return st;
@@ -1472,9 +1458,6 @@ gemm_status_t launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_
     if (conv) {
         const gemm_conv2d_desc_t &d = *conv->d;
         p.conv = 1;
-        p.cv_H = static_cast<int>(d.H);
-        p.cv_W = static_cast<int>(d.W);
-        p.cv_C = static_cast<int>(d.C);
         p.cv_S = static_cast<int>(d.S);
         p.cv_PQ = static_cast<int>(conv->P * conv->Q);
         p.cv_Q = static_cast<int>(conv->Q);
@@ -1486,7 +1469,6 @@ gemm_status_t launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_
         p.dil_h = d.dil_h;
         p.dil_w = d.dil_w;
         p.ncb = conv->ncb;
-        p.x = static_cast<const uint16_t *>(A);
     }
     const EpilogueArgs ep = epilogue_args(o);
     p.epi = ep.epi;
@@ -1687,7 +1669,7 @@ namespace gemm {
 namespace {
 
 // The implicit GEMM of a convolution: M = N P Q, N = K, K = R S (C rounded up
-// to 64-channel blocks), on the single-CTA variant; the options as given.
+// to 64-channel blocks); the options as given.
 struct ConvProblem {
     ConvLaunch launch;
     int64_t M, N, K;
@@ -1700,8 +1682,10 @@ gemm_status_t conv_problem(const gemm_conv2d_desc_t *d, const gemm_options_t *op
     if (st != GEMM_OK) return st;
     gemm_options_t o{};
     if (opts) o = *opts;
-    if (o.kernel_variant != VARIANT_AUTO && o.kernel_variant != VARIANT_1SM_128x256) return GEMM_ERR_NOT_SUPPORTED;
-    o.kernel_variant = VARIANT_1SM_128x256;
+    if (o.kernel_variant < 0 || o.kernel_variant >= VARIANT_COUNT) return GEMM_ERR_INVALID_VALUE;
+    // the im2col pixel box of a 4-D tensor map spans corners in [-128, 127]
+    if (d->pad_h > 127 || d->pad_w > 127 || d->dil_h * (d->R - 1) > 127 || d->dil_w * (d->S - 1) > 127)
+        return GEMM_ERR_NOT_SUPPORTED;
     const int ncb = static_cast<int>((d->C + TILE_K - 1) / TILE_K);
     cp->launch = ConvLaunch{d, P, Q, ncb};
     cp->M = d->N * P * Q;
@@ -1726,8 +1710,9 @@ extern "C" gemm_status_t gemm_conv2d_plan(const gemm_conv2d_desc_t *d, gemm_dtyp
     DeviceState *ds = nullptr;
     st = current_device(&device, &ds);
     if (st != GEMM_OK) return st;
+    const int v = choose_variant(cp.M, cp.N, cp.K, cp.o.kernel_variant, cp.o.split_k, ds->desc);
     return make_plan(cp.M, cp.N, cp.K, GEMM_ROW_MAJOR, GEMM_COL_MAJOR, out_dtype, cp.o, true, ds->desc,
-                     kernel_desc(VARIANT_1SM_128x256, ds->var[VARIANT_1SM_128x256]), plan);
+                     kernel_desc(v, ds->var[v]), plan);
 }
 
 extern "C" gemm_status_t gemm_conv2d_fprop_bf16(const gemm_conv2d_desc_t *d, const void *x, const void *w, void *y,

@@ -130,6 +130,40 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint
         : "memory");
 }
 
+// im2col load of a 4-D NHWC tensor map: the pixel column starting at the
+// window origin (c0 = channel, w0, h0, n0), each pixel offset by the filter
+// tap (off_w, off_h) -- pixels outside the image read as zero.
+__device__ __forceinline__ void tma_load_im2col_4d(uint32_t dst, const void *tmap, uint32_t bar, int c0, int w0,
+                                                   int h0, int n0, uint16_t off_w, uint16_t off_h) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.im2col.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2], {%7, %8};" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(w0), "r"(h0), "r"(n0), "h"(off_w), "h"(off_h)
+        : "memory");
+}
+
+// The same issued by either CTA of a pair, completing on a barrier that may
+// live in the peer CTA.
+__device__ __forceinline__ void tma_load_im2col_4d_pair(uint32_t dst, const void *tmap, uint32_t cluster_bar, int c0,
+                                                        int w0, int h0, int n0, uint16_t off_w, uint16_t off_h) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.im2col.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2], {%7, %8};" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(cluster_bar), "r"(c0), "r"(w0), "r"(h0), "r"(n0), "h"(off_w),
+        "h"(off_h)
+        : "memory");
+}
+
+// 3-D load, pair form (see tma_load_2d_pair).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void *tmap, uint32_t cluster_bar, int c0, int c1,
+                                                 int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(cluster_bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
 // ---- per-thread asynchronous copies (cp.async) ---------------------------------
 
 // 16 bytes from global to shared memory, of which `src_bytes` (16 or 0) are

@@ -9,9 +9,10 @@
  *     C[M x N] = A[M x K] . B[K x N]
  *
  * with bf16 A and B, products accumulated in fp32 on the Tensor Cores, and C
- * written as fp32 or as bf16 (round to nearest even).  C is output only: the
- * "+ C" of D = A x B + C is taken with a zero C (the accumulator starts at
- * zero), so the previous contents of C are overwritten, never read.
+ * written as fp32 or as bf16 (round to nearest even).  By default C is output
+ * only: the "+ C" of D = A x B + C is taken with a zero C (the accumulator
+ * starts at zero) and the previous contents of C are overwritten, never read;
+ * the fused epilogue (gemm_epilogue_t) adds beta * C, bias and an activation.
  *
  * Conventions shared by every entry point
  *   - Dimensions are element counts; leading dimensions ("ld") are in
@@ -55,7 +56,8 @@ typedef enum {
     GEMM_OK = 0,
     GEMM_ERR_INVALID_VALUE = 1,   /* negative or too large size, bad enum, short ld, NULL */
     GEMM_ERR_MISALIGNED = 2,      /* a pointer or leading dimension breaks the rules above */
-    GEMM_ERR_NOT_SUPPORTED = 3,   /* a request this build cannot run (too many stream-K clusters) */
+    GEMM_ERR_NOT_SUPPORTED = 3,   /* a request this build cannot run (too many stream-K clusters;
+                                     a convolution beyond an im2col box's range) */
     GEMM_ERR_NO_DEVICE = 4,       /* no usable CUDA device, or not an sm_103 part */
     GEMM_ERR_OUT_OF_MEMORY = 5,   /* the split-K workspace could not be grown */
     GEMM_ERR_LAUNCH = 6,          /* a CUDA runtime or driver call failed */
@@ -342,8 +344,9 @@ gemm_status_t gemm_bf16_ex(int64_t M, int64_t N, int64_t K,
  *
  * with x zero outside the image (the padding).  It is the GEMM
  * C (N P Q x K) = A (N P Q x R S C) . B (R S C x K) in which row m of A is the
- * receptive field of output pixel m -- never formed in memory: the kernel's
- * producer warp gathers each A tile from x as it goes.  P and Q are
+ * receptive field of output pixel m -- never formed in memory: TMA's im2col
+ * mode loads each A box (128 output pixels x 64 channels at one filter tap)
+ * straight from x, zero-filling the padding.  P and Q are
  * (H + 2 pad - dil (R - 1) - 1) / stride + 1 (integer division, >= 1).
  *
  *   x: N x H x W x C bf16, NHWC, dense.       w: K x R x S x C bf16, KRSC, dense.
@@ -352,9 +355,10 @@ gemm_status_t gemm_bf16_ex(int64_t M, int64_t N, int64_t K,
  * Requirements: every size >= 1, strides and dilations >= 1, paddings >= 0;
  * C a multiple of 8 (16-byte pixel rows); K a multiple of 8 for bf16 y or 4
  * for fp32 y; x, w, y on 16-byte boundaries (GEMM_ERR_MISALIGNED otherwise);
- * N P Q and R S C below 2^31.  The options work as for gemm_bf16_ex (split-K,
- * stream-K, the fused epilogue -- a bias per output channel k); the kernel
- * is the single-CTA 128 x 256 variant (kernel_variant must be 0 or 1).
+ * N P Q and R S C below 2^31; paddings and dil (R - 1), dil (S - 1) at most
+ * 127 (GEMM_ERR_NOT_SUPPORTED beyond: the range of an im2col pixel box).  The
+ * options work as for gemm_bf16_ex (kernel variant, split-K, stream-K, the
+ * fused epilogue -- a bias per output channel k).
  */
 typedef struct {
     int64_t N, H, W, C;          /* input */

@@ -348,5 +348,7 @@ def test_conv2d_argument_checks_before_any_cuda_call():
     assert call(_conv(K=66)) == 2                               # fp32 output rows of 264 bytes
     assert call(_conv(K=60), out=1) == 2                        # bf16 output rows of 120 bytes
     assert call(_conv(), xp=x + 8) == 2                         # x off its 16-byte boundary
-    assert call(_conv(), opts=g.options(kernel_variant=2)) == 3    # only the single-CTA variant
+    assert call(_conv(), opts=g.options(kernel_variant=9)) == 1
+    assert call(_conv(pad_h=128, H=300)) == 3                   # beyond an im2col pixel box's range
+    assert call(_conv(R=65, dil_h=2, H=200)) == 3
     assert call(_conv(), opts=g.options(debug_skip_load=1)) == 1

@@ -108,7 +108,7 @@ def test_conv_split_k(oracle_lib, split):
         d = g.gemm_conv2d_desc_t(N=4, H=28, W=28, C=128, K=256, R=3, S=3, pad_h=1, pad_w=1, stride_h=1, stride_w=1,
                                  dil_h=1, dil_w=1)
         st, plan = g.gemm_conv2d_plan(d, g.GEMM_OUT_F32)
-        assert st == 0 and plan.split_k > 1 and plan.kernel_variant == 1
+        assert st == 0 and plan.split_k > 1
 
 
 def test_conv_stream_k(oracle_lib):
@@ -125,16 +125,25 @@ def test_conv_stream_k(oracle_lib):
     assert np.array_equal(y, y2), "stream-K result differs run to run"
 
 
-def test_conv_one_by_one_equals_the_gemm_bitwise():
-    """A 1 x 1 convolution is the GEMM of pixels and filters; the single-CTA
-    GEMM kernel sums over K in the same order under the same plan."""
+@pytest.mark.parametrize("variant", [0, 1, 2, 3])
+def test_conv_one_by_one_equals_the_gemm_bitwise(variant):
+    """A 1 x 1 convolution is the GEMM of pixels and filters: under the same
+    kernel variant the plan and the order of every sum are the same."""
     import dense_tensor_core_bf16_gb300 as g
     N, H, W, C, K = 2, 24, 40, 192, 320
     x, w = conv_operands(N, H, W, C, K, 1, 1, "normal", SEED + 4)
-    yc = run(x, w, "f32")
+    yc = run(x, w, "f32", kernel_variant=variant)
     A, Bt = dev(x.reshape(N * H * W, C)), dev(w.reshape(K, C))
-    yg = g.matmul(A, Bt.t(), out_dtype=torch.float32, kernel_variant=1).cpu().numpy()
+    yg = g.matmul(A, Bt.t(), out_dtype=torch.float32, kernel_variant=variant).cpu().numpy()
     assert np.array_equal(yc.reshape(N * H * W, K), yg)
+
+
+@pytest.mark.parametrize("variant", [1, 2, 3])
+@pytest.mark.parametrize("case", CASES, ids=IDS)
+def test_conv_every_variant_exact(oracle_lib, case, variant):
+    x, w = conv_operands(*(case[k] for k in "N H W C K R S".split()), "int4", SEED + 7)
+    y = run(x, w, "f32", kernel_variant=variant, **_conv_kw(case))
+    check(oracle_lib, x, w, y, "f32", exact=True, **_conv_kw(case))
 
 
 def test_conv_fused_bias_relu(oracle_lib):
