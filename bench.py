@@ -78,6 +78,15 @@ WORKLOADS = {
                                    non_persistent=True,
                                    desc="gemm_bf16 16384x8192x8192, bf16 row x col -> bf16, one CTA per tile"),
 }
+# implicit-GEMM convolutions (NHWC x KRSC -> NPQK, bf16), inputs N(0,1), filters N(0,1)/sqrt(R S C)
+WORKLOADS["conv3x3_n32_56x56_c256_k256"] = dict(
+    conv=dict(N=32, H=56, W=56, C=256, K=256, R=3, S=3, pad=(1, 1), stride=(1, 1), dil=(1, 1)), out="bf16",
+    dist="normal", scaled=True, desc="conv2d fprop as implicit GEMM, N32 H56 W56 C256 -> K256, 3x3, pad 1, stride 1, "
+                                     "NHWC/KRSC bf16 -> bf16")
+WORKLOADS["conv3x3_n32_28x28_c512_k512"] = dict(
+    conv=dict(N=32, H=28, W=28, C=512, K=512, R=3, S=3, pad=(1, 1), stride=(1, 1), dil=(1, 1)), out="bf16",
+    dist="normal", scaled=True, desc="conv2d fprop as implicit GEMM, N32 H28 W28 C512 -> K512, 3x3, pad 1, stride 1, "
+                                     "NHWC/KRSC bf16 -> bf16")
 for _s in (1, 8, 32, 74, 148):
     WORKLOADS[f"splitk{_s}"] = dict(M=128, N=256, K=65536, out="f32", dist="uniform", scaled=True, split_k=_s,
                                     desc=f"gemm_bf16 128x256x65536, bf16 row x col -> fp32, uniform[-1,1]/sqrt(K), "
@@ -446,6 +455,47 @@ def cpu_oracle_baseline(A_h, Bt_h, M, N, K, target_s: float):
                       f"{cores} OpenMP threads, {dt:.1f} s"}
 
 
+def run_reference_conv(args, w: dict, oracle, cores: int):
+    """The direct-convolution oracle on a bounded sample: one image, cut to a
+    band of input rows sized so the whole run stays within a few minutes."""
+    from dense_tensor_core_bf16_gb300 import inputs
+    cv = w["conv"]
+    seed = inputs.DEFAULT_SEED + 400
+    x_h, w_h = conv_host_operands(cv, seed)
+    conv_kw = dict(pad=cv["pad"], stride=cv["stride"], dil=cv["dil"])
+    budget_s = min(3.0, 150.0 / max(1, args.steps + args.warmup))
+    rows = min(cv["H"], cv["R"] + 1)
+    t = time.perf_counter()
+    oracle.conv2d(x_h[:1, :rows], w_h, with_abs=False, **conv_kw)
+    dt0 = max(time.perf_counter() - t, 1e-4)
+    rows = int(min(cv["H"], max(cv["R"], math.floor(rows * budget_s / dt0))))
+
+    def sample(i):
+        n = i % cv["N"]
+        return oracle.conv2d(x_h[n:n + 1, :rows], w_h, with_abs=False, **conv_kw)[0]
+
+    y = sample(0)
+    flops = 2.0 * y.size * cv["R"] * cv["S"] * cv["C"]
+    for i in range(args.warmup):
+        sample(i)
+    t = time.perf_counter()
+    for i in range(args.steps):
+        sample(i)
+    dt = time.perf_counter() - t
+    value = flops * args.steps / dt / 1e12
+    desc = (f"each step: one image cut to its first {rows} input rows ({y.shape[1]}x{y.shape[2]} output pixels x "
+            f"K={cv['K']}), direct binary64 convolution, {cores} OpenMP threads")
+    return {
+        "impl": "reference", "metric": "conv2d TFLOP/s (2 N P Q K R S C / device time) and % of GB300 dense BF16 peak, 1 GPU",
+        "value": round(value, 6), "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": f"synthetic (seeded SplitMix64, seed {seed})",
+        "config": {"workload": w["desc"], **cv},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def run_reference(args, wname: str, w: dict):
     """The oracle as the reference arm: each step is a bounded row sample."""
     import oracle
@@ -453,9 +503,11 @@ def run_reference(args, wname: str, w: dict):
     if rank != 0:
         return None, rank
     oracle.build()
+    cores = oracle.max_threads()
+    if w.get("conv"):
+        return run_reference_conv(args, w, oracle, cores), rank
     (A_h, Bt_h), seed = make_host_operands(w)
     M, N, K = w["M"], w["N"], w["K"]
-    cores = oracle.max_threads()
     budget_s = min(3.0, 150.0 / max(1, args.steps + args.warmup))
     r0 = min(M, 2)
     t = time.perf_counter()
@@ -482,6 +534,154 @@ def run_reference(args, wname: str, w: dict):
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+    return result, rank
+
+
+def conv_host_operands(cv: dict, seed: int):
+    """x (N H W C) and w (K R S C) bf16 bit patterns from the seeded generator."""
+    from dense_tensor_core_bf16_gb300 import inputs
+    N, H, W, C, K, R, S = (cv[k] for k in "N H W C K R S".split())
+    x = inputs.matrix(N * H * W, C, dist="normal", seed=seed, stream=0).reshape(N, H, W, C)
+    w = inputs.matrix(K, R * S * C, dist="normal", seed=seed, stream=1,
+                      scale=1.0 / math.sqrt(R * S * C)).reshape(K, R, S, C)
+    return x, w
+
+
+def run_gpu_conv(args, wname: str, w: dict):
+    """A convolution workload: the same contract as run_gpu (W warm-ups, K
+    steps back to back between events, barrier, max over ranks, clocks,
+    roofline, end to end with host copies)."""
+    import numpy as np
+    import torch
+    import dense_tensor_core_bf16_gb300 as g
+    from dense_tensor_core_bf16_gb300 import inputs
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    cv = w["conv"]
+    seed = inputs.DEFAULT_SEED + 400
+    x_h, w_h = conv_host_operands(cv, seed)
+    desc = g.gemm_conv2d_desc_t(N=cv["N"], H=cv["H"], W=cv["W"], C=cv["C"], K=cv["K"], R=cv["R"], S=cv["S"],
+                                pad_h=cv["pad"][0], pad_w=cv["pad"][1], stride_h=cv["stride"][0],
+                                stride_w=cv["stride"][1], dil_h=cv["dil"][0], dil_w=cv["dil"][1])
+    st, P, Q = g.gemm_conv2d_out_dims(desc)
+    if st:
+        raise g.GemmError(st, "gemm_conv2d_out_dims")
+    out_dtype = torch.bfloat16 if w["out"] == "bf16" else torch.float32
+    odt = g.GEMM_OUT_BF16 if w["out"] == "bf16" else g.GEMM_OUT_F32
+    opts = g.options(kernel_variant=args.variant, no_stream_k=int(args.no_stream_k))
+    st, plan = g.gemm_conv2d_plan(desc, odt, opts)
+    if st:
+        raise g.GemmError(st, "gemm_conv2d_plan")
+    if plan.workspace_bytes:
+        g.gemm_reserve_workspace(plan.workspace_bytes)
+    kw = dict(pad=cv["pad"], stride=cv["stride"], dil=cv["dil"], kernel_variant=args.variant,
+              no_stream_k=args.no_stream_k)
+
+    props = torch.cuda.get_device_properties(local)
+    l2 = getattr(props, "L2_cache_size", 135_528_448) or 135_528_448
+    esize = 2 if w["out"] == "bf16" else 4
+    set_bytes = x_h.nbytes + w_h.nbytes + esize * cv["N"] * P * Q * cv["K"]
+    copies = max(2, math.ceil(2 * l2 / set_bytes) + 1)
+    x0 = torch.from_numpy(x_h.view(np.int16)).cuda().view(torch.bfloat16)
+    w0 = torch.from_numpy(w_h.view(np.int16)).cuda().view(torch.bfloat16)
+    sets = []
+    for i in range(copies):
+        sets.append((x0 if i == 0 else x0.clone(), w0 if i == 0 else w0.clone(),
+                     torch.zeros((cv["N"], P, Q, cv["K"]), dtype=out_dtype, device="cuda")))
+
+    def step(i):
+        xx, ww, yy = sets[i % copies]
+        g.conv2d(xx, ww, out=yy, **kw)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    st, where = g.gemm_get_device_status(None)
+    if st:
+        raise RuntimeError(f"device fault during warm-up: {where:#x}")
+    gpu_id = getattr(props, "uuid", None)
+    sampler = ClockSampler(f"GPU-{gpu_id}" if gpu_id is not None else str(local))
+    time.sleep(0.3)
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    t_wall1 = time.time()
+    time.sleep(0.25)
+    sampler.stop()
+    st, where = g.gemm_get_device_status(None)
+    if st:
+        raise RuntimeError(f"device fault in the timed region: {where:#x}")
+    total_ms = e0.elapsed_time(e1)
+    flops = 2.0 * cv["N"] * P * Q * cv["K"] * cv["R"] * cv["S"] * cv["C"]
+    max_ms, total_flops = aggregate(total_ms, flops * args.steps)
+    value = total_flops / (max_ms * 1e-3) / 1e12
+    peaks = load_peaks()
+    long_region = (t_wall1 - t_wall0) > 1.0
+    peak = peaks["bf16_sustained"] if long_region else peaks["bf16_burst"]
+    peak_kind = ("sustained" if long_region else "burst") + f" bf16, {peaks['source']}"
+    mean_ms = total_ms / args.steps
+    achieved = flops / (mean_ms * 1e-3) / 1e12
+    result = {
+        "metric": "conv2d TFLOP/s (2 N P Q K R S C / device time) and % of GB300 dense BF16 peak, 1 GPU",
+        "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(max_ms / args.steps, 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": f"synthetic (seeded SplitMix64, N(0,1) input, N(0,1)/sqrt(RSC) filter, seed {seed})",
+        "config": {
+            "workload": w["desc"], **{k: v for k, v in cv.items()}, "P": P, "Q": Q, "out": w["out"],
+            "gemm": {"M": cv["N"] * P * Q, "N": cv["K"], "K": cv["R"] * cv["S"] * cv["C"]},
+            "kernel_variant": g.KERNEL_VARIANTS[plan.kernel_variant], "cluster_size": plan.cluster_size,
+            "tile": f"{plan.tile_m}x{plan.tile_n}x{plan.tile_k}", "split_k": plan.split_k,
+            "stream_k_tiles": plan.stream_k_tiles, "pct_of_peak": round(100.0 * value / world / peak, 2),
+            "peak_tflops": peak, "peak_kind": peak_kind,
+            "l2": f"inputs larger than L2: {copies} rotating sets of {set_bytes / 1e6:.1f} MB vs L2 {l2 / 1e6:.1f} MB",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "roofline": {
+            "bound": "tensor", "kernel": f"{KERNEL_NAME}<{plan.cluster_size},{plan.tile_n}> (im2col A)",
+            "achieved": round(achieved, 3), "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+            "traffic": recorded_traffic(wname), "algorithmic_flops_per_launch": flops,
+            "mean_launch_ms": round(mean_ms, 6), "launch_time_from": "timed region / steps, launches back to back",
+            "peak_source": peak_kind,
+        },
+        "gpu_launches": (1 + (1 if plan.split_k > 1 else 0)) * args.steps,
+        "clocks": sampler.summary(t_wall0, t_wall1),
+    }
+    e2e_steps = min(args.steps, 20)
+    hx = torch.from_numpy(x_h.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hw = torch.from_numpy(w_h.view(np.int16)).view(torch.bfloat16).pin_memory()
+    yy = sets[0][2]
+    hy = torch.empty(tuple(yy.shape), dtype=out_dtype).pin_memory()
+    for _ in range(2):
+        x0.copy_(hx, non_blocking=True)
+        w0.copy_(hw, non_blocking=True)
+        g.conv2d(x0, w0, out=yy, **kw)
+        hy.copy_(yy, non_blocking=True)
+    torch.cuda.synchronize()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    f0.record(stream)
+    for _ in range(e2e_steps):
+        x0.copy_(hx, non_blocking=True)
+        w0.copy_(hw, non_blocking=True)
+        g.conv2d(x0, w0, out=yy, **kw)
+        hy.copy_(yy, non_blocking=True)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms, e2e_flops = aggregate(f0.elapsed_time(f1), flops * e2e_steps)
+    result["e2e"] = {"value": round(e2e_flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
+                     "h2d_bytes_per_step": int(hx.numel() * 2 + hw.numel() * 2),
+                     "d2h_bytes_per_step": int(hy.numel() * hy.element_size()), "steps": e2e_steps}
     return result, rank
 
 
@@ -518,8 +718,11 @@ def main(argv=None):
     try:
         names = sorted(WORKLOADS) if args.all_workloads else [args.workload]
         for name in names:
-            res, rank = run_gpu(args, name, WORKLOADS[name],
-                                cpu_baseline=not args.no_cpu_baseline and not args.all_workloads)
+            if WORKLOADS[name].get("conv"):
+                res, rank = run_gpu_conv(args, name, WORKLOADS[name])
+            else:
+                res, rank = run_gpu(args, name, WORKLOADS[name],
+                                    cpu_baseline=not args.no_cpu_baseline and not args.all_workloads)
             if rank == 0:
                 if args.all_workloads:
                     res["config"]["name"] = name
