@@ -164,22 +164,6 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void *tmap,
         : "memory");
 }
 
-// ---- per-thread asynchronous copies (cp.async) ---------------------------------
-
-// 16 bytes from global to shared memory, of which `src_bytes` (16 or 0) are
-// read and the rest zero-filled.
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-
-// Arrive on `bar` once all of this thread's earlier cp.async copies have
-// landed; the arrival is not pre-counted (the barrier's count includes it).
-__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
 // 2-D tiled store of a shared-memory box to the tensor map's box at (c0, c1);
 // out-of-range elements are not written.  Tracked as a bulk async-group of the
 // issuing thread.
