@@ -418,33 +418,39 @@ def run_gpu(args, wname: str, w: dict, cpu_baseline: bool):
     clocks = sampler.summary(t_wall0, t_wall1)
     result["clocks"] = clocks
 
-    # end to end through the public API: pinned host operands in, C back out, every step
-    e2e_steps = min(args.steps, 20)
-    hA = torch.from_numpy(A_store.view(np.int16)).view(torch.bfloat16).pin_memory()
-    hB = torch.from_numpy(B_store.view(np.int16)).view(torch.bfloat16).pin_memory()
-    hC = torch.empty((M, N), dtype=out_dtype).pin_memory()
-    dA, dB, dC = A0, B0, sets[0][2]     # the storage of set 0
-    for _ in range(2):
-        dA.copy_(hA, non_blocking=True)
-        dB.copy_(hB, non_blocking=True)
-        g.matmul(a_view(dA), b_view(dB), out=dC, **kw)
-        hC.copy_(dC, non_blocking=True)
+    # End to end through the public API: every step copies its A and B from
+    # pinned host memory and its C back, through gemm_bf16_host_batch, which
+    # overlaps one step's copies with another step's product.  Two host sets
+    # alternate so that consecutive steps never share a buffer.
+    e2e_steps = max(min(args.steps, 20), 2)
+    hA = [torch.from_numpy(A_store.view(np.int16)).view(torch.bfloat16).pin_memory() for _ in range(2)]
+    hB = [torch.from_numpy(B_store.view(np.int16)).view(torch.bfloat16).pin_memory() for _ in range(2)]
+    hC = [torch.zeros((M, N), dtype=out_dtype).pin_memory() for _ in range(2)]
+    ha = [a_view(x) for x in hA]
+    hb = [b_view(x) for x in hB]
+    hkw = {k: v for k, v in kw.items() if k in ("split_k", "no_stream_k", "non_persistent", "kernel_variant",
+                                                 "alpha", "beta", "bias", "activation")}
+
+    def e2e_batch(n):
+        idx = [i % 2 for i in range(n)]
+        return g.matmul_host_batch([ha[i] for i in idx], [hb[i] for i in idx], outs=[hC[i] for i in idx],
+                                   stream=stream, **hkw)
+
+    e2e_batch(2)   # grows the staging slots outside the timed region
     torch.cuda.synchronize()
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     f0.record(stream)
-    for _ in range(e2e_steps):
-        dA.copy_(hA, non_blocking=True)
-        dB.copy_(hB, non_blocking=True)
-        g.matmul(a_view(dA), b_view(dB), out=dC, **kw)
-        hC.copy_(dC, non_blocking=True)
+    e2e_batch(e2e_steps)
     f1.record(stream)
     torch.cuda.synchronize()
     e2e_ms, e2e_flops = aggregate(f0.elapsed_time(f1), flops * e2e_steps)
     result["e2e"] = {"value": round(e2e_flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
-                     "h2d_bytes_per_step": int(hA.numel() * 2 + hB.numel() * 2),
-                     "d2h_bytes_per_step": int(hC.numel() * hC.element_size()), "steps": e2e_steps}
+                     "h2d_bytes_per_step": int(hA[0].numel() * 2 + hB[0].numel() * 2),
+                     "d2h_bytes_per_step": int(hC[0].numel() * hC[0].element_size()), "steps": e2e_steps,
+                     "ms_per_step": round(e2e_ms / e2e_steps, 4),
+                     "api": "gemm_bf16_host_batch (host operands; copies overlapped with the products)"}
 
     if cpu_baseline and rank == 0 and world == 1:
         result["cpu_baseline"] = cpu_oracle_baseline(A_h, Bt_h, M, N, K, target_s=args.cpu_seconds)

@@ -27,7 +27,7 @@ __all__ = [
     "gemm_get_device_status", "gemm_status_string", "gemm_limiter_string", "matmul", "lib", "header_functions",
     "gemm_bf16_splitk_noalloc", "GEMM_NOALLOC_SCRATCH_FLOATS", "options",
     "gemm_epilogue_t", "gemm_conv2d_desc_t", "gemm_conv2d_out_dims", "gemm_conv2d_plan", "gemm_conv2d_fprop_bf16",
-    "conv2d",
+    "conv2d", "gemm_host_problem_t", "gemm_bf16_host_batch", "matmul_host_batch",
 ]
 
 GEMM_ROW_MAJOR, GEMM_COL_MAJOR = 0, 1
@@ -92,6 +92,13 @@ class gemm_options_t(ctypes.Structure):
 ACTIVATIONS = {"none": 0, "relu": 1, "gelu": 2}
 
 
+class gemm_host_problem_t(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("A", ctypes.c_void_p), ("lda", ctypes.c_int64), ("layout_a", ctypes.c_int),
+                ("B", ctypes.c_void_p), ("ldb", ctypes.c_int64), ("layout_b", ctypes.c_int),
+                ("C", ctypes.c_void_p), ("ldc", ctypes.c_int64)]
+
+
 class gemm_conv2d_desc_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in ("N", "H", "W", "C", "K", "R", "S")] + \
         [(n, ctypes.c_int) for n in ("pad_h", "pad_w", "stride_h", "stride_w", "dil_h", "dil_w")]
@@ -129,6 +136,8 @@ def lib() -> ctypes.CDLL:
         L.gemm_conv2d_plan.restype = i32
         L.gemm_conv2d_fprop_bf16.argtypes = [P(gemm_conv2d_desc_t), vp, vp, vp, i32, P(gemm_options_t), vp]
         L.gemm_conv2d_fprop_bf16.restype = i32
+        L.gemm_bf16_host_batch.argtypes = [i64, P(gemm_host_problem_t), i32, P(gemm_options_t), vp]
+        L.gemm_bf16_host_batch.restype = i32
         L.gemm_reserve_workspace.argtypes = [ctypes.c_size_t]
         L.gemm_release_workspace.argtypes = []
         L.gemm_release_workspace.restype = None
@@ -246,6 +255,14 @@ def gemm_conv2d_fprop_bf16(desc: gemm_conv2d_desc_t, x, w, y, out_dtype, opts: g
                                         ctypes.byref(opts) if opts is not None else None, stream)
 
 
+def gemm_bf16_host_batch(problems, out_dtype, opts: gemm_options_t | None, stream) -> int:
+    """Status code of the C call; ``problems`` a sequence of gemm_host_problem_t
+    (host pointers as integers)."""
+    arr = (gemm_host_problem_t * max(len(problems), 1))(*problems)
+    return lib().gemm_bf16_host_batch(len(problems), arr, out_dtype,
+                                      ctypes.byref(opts) if opts is not None else None, stream)
+
+
 def gemm_reserve_workspace(nbytes: int) -> int:
     return lib().gemm_reserve_workspace(nbytes)
 
@@ -280,6 +297,33 @@ def _stream_handle(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _layouts(A, B):
+    """(layout_a, lda, layout_b, ldb) from the strides.  A: row-major when K is
+    contiguous (or K <= 1), else column-major when M is contiguous (or M <= 1);
+    B alike, column-major first.  A dimension of extent 1 has no real leading
+    dimension: report the smallest aligned one so the alignment rule does not
+    reject it."""
+    M, K = A.shape
+    N = B.shape[1]
+    if K <= 1 or A.stride(1) == 1:
+        a_layout = GEMM_ROW_MAJOR
+        lda = A.stride(0) if M > 1 else _round_up(K, 8)
+    elif M <= 1 or A.stride(0) == 1:
+        a_layout = GEMM_COL_MAJOR
+        lda = A.stride(1) if K > 1 else _round_up(M, 8)
+    else:
+        raise ValueError("A must be row-major (stride (lda, 1)) or column-major (stride (1, lda))")
+    if K <= 1 or B.stride(0) == 1:
+        b_layout = GEMM_COL_MAJOR
+        ldb = B.stride(1) if N > 1 else _round_up(K, 8)
+    elif N <= 1 or B.stride(1) == 1:
+        b_layout = GEMM_ROW_MAJOR
+        ldb = B.stride(0) if K > 1 else _round_up(N, 8)
+    else:
+        raise ValueError("B must be column-major (stride (1, ldb)) or row-major (stride (ldb, 1))")
+    return a_layout, lda, b_layout, ldb
 
 
 def matmul(A, B, *, out_dtype=None, out=None, split_k: int = 0, non_persistent: bool = False,
@@ -324,26 +368,7 @@ def matmul(A, B, *, out_dtype=None, out=None, split_k: int = 0, non_persistent: 
     odt = {torch.float32: GEMM_OUT_F32, torch.bfloat16: GEMM_OUT_BF16}.get(out.dtype)
     if odt is None:
         raise TypeError("out must be float32 or bfloat16")
-    # Layouts from the strides.  A: row-major when K is contiguous (or K <= 1),
-    # else column-major when M is contiguous (or M <= 1); B alike, column-major
-    # first.  A dimension of extent 1 has no real leading dimension: report the
-    # smallest aligned one so the alignment rule does not reject it.
-    if K <= 1 or A.stride(1) == 1:
-        a_layout = GEMM_ROW_MAJOR
-        lda = A.stride(0) if M > 1 else _round_up(K, 8)
-    elif M <= 1 or A.stride(0) == 1:
-        a_layout = GEMM_COL_MAJOR
-        lda = A.stride(1) if K > 1 else _round_up(M, 8)
-    else:
-        raise ValueError("A must be row-major (stride (lda, 1)) or column-major (stride (1, lda))")
-    if K <= 1 or B.stride(0) == 1:
-        b_layout = GEMM_COL_MAJOR
-        ldb = B.stride(1) if N > 1 else _round_up(K, 8)
-    elif N <= 1 or B.stride(1) == 1:
-        b_layout = GEMM_ROW_MAJOR
-        ldb = B.stride(0) if K > 1 else _round_up(N, 8)
-    else:
-        raise ValueError("B must be column-major (stride (1, ldb)) or row-major (stride (ldb, 1))")
+    a_layout, lda, b_layout, ldb = _layouts(A, B)
     ldc = out.stride(0) if M > 1 else _round_up(N, 8)
     opts = gemm_options_t(split_k=split_k, non_persistent=int(non_persistent), raster_group_m=raster_group_m,
                           mainloop_done_event=(mainloop_done_event.cuda_event if mainloop_done_event is not None
@@ -360,6 +385,63 @@ def matmul(A, B, *, out_dtype=None, out=None, split_k: int = 0, non_persistent: 
     if st:
         raise GemmError(st, "gemm_bf16_ex")
     return out
+
+
+def matmul_host_batch(As, Bs, *, outs=None, out_dtype=None, split_k: int = 0, no_stream_k: bool = False,
+                      non_persistent: bool = False, kernel_variant: int = 0, stream=None, alpha: float = 1.0, beta: float = 0.0, bias=None,
+                      activation: str = "none", timeout_ms: int = 0):
+    """C_i = A_i @ B_i for host-resident operands through ``gemm_bf16_host_batch``.
+
+    ``As``, ``Bs``: sequences of CPU torch.bfloat16 tensors, (M_i, K_i) and
+    (K_i, N_i), each row- or column-major as for :func:`matmul`; pinned
+    (``.pin_memory()``) for the copies to overlap the products.  ``outs``:
+    optional sequence of CPU (M_i, N_i) row-major float32 or bfloat16 tensors
+    (all of one dtype), allocated pinned when omitted.  The work is enqueued on
+    ``stream`` (default: the current stream), which waits for the last result
+    copy: synchronise it before reading ``outs``.  Epilogue arguments as for
+    :func:`matmul`, applied to every problem; ``bias`` is a CUDA tensor.
+    Raises :class:`GemmError` on a non-zero status."""
+    import torch
+    if len(As) != len(Bs):
+        raise ValueError("As and Bs differ in length")
+    if activation not in ACTIVATIONS:
+        raise ValueError(f"activation must be one of {sorted(ACTIVATIONS)}")
+    if beta != 0.0 and outs is None:
+        raise ValueError("beta != 0 reads the previous C: pass outs=")
+    dt = out_dtype if out_dtype is not None else (outs[0].dtype if outs else torch.bfloat16)
+    odt = {torch.float32: GEMM_OUT_F32, torch.bfloat16: GEMM_OUT_BF16}.get(dt)
+    if odt is None:
+        raise TypeError("the output dtype must be float32 or bfloat16")
+    if outs is None:
+        outs = [torch.empty((A.shape[0], B.shape[1]), dtype=dt).pin_memory() for A, B in zip(As, Bs)]
+    if len(outs) != len(As):
+        raise ValueError("outs differs in length from As")
+    problems = []
+    for A, B, C in zip(As, Bs, outs):
+        if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
+            raise TypeError("A and B must be torch.bfloat16")
+        if A.is_cuda or B.is_cuda or C.is_cuda:
+            raise ValueError("matmul_host_batch takes host tensors; use matmul for device tensors")
+        M, K = A.shape
+        K2, N = B.shape
+        if K2 != K:
+            raise ValueError(f"inner dimensions differ: {K} vs {K2}")
+        if tuple(C.shape) != (M, N) or C.dtype != dt or (M and N and C.stride(1) != 1):
+            raise ValueError(f"each out must be a row-major ({M}, {N}) {dt} tensor")
+        a_layout, lda, b_layout, ldb = _layouts(A, B)
+        problems.append(gemm_host_problem_t(M=M, N=N, K=K, A=A.data_ptr(), lda=lda, layout_a=a_layout,
+                                            B=B.data_ptr(), ldb=ldb, layout_b=b_layout, C=C.data_ptr(),
+                                            ldc=C.stride(0) if M > 1 else max(N, 1)))
+    opts = gemm_options_t(split_k=split_k, no_stream_k=int(no_stream_k), non_persistent=int(non_persistent),
+                          kernel_variant=kernel_variant, timeout_ms=timeout_ms)
+    if alpha != 1.0 or beta != 0.0 or bias is not None or activation != "none":
+        epi = gemm_epilogue_t(alpha=alpha, beta=beta, bias=bias.data_ptr() if bias is not None else None,
+                              activation=ACTIVATIONS[activation])
+        opts.epilogue = ctypes.pointer(epi)
+    st = gemm_bf16_host_batch(problems, odt, opts, _stream_handle(stream))
+    if st:
+        raise GemmError(st, "gemm_bf16_host_batch")
+    return outs
 
 
 def conv2d(x, w, *, pad=(0, 0), stride=(1, 1), dil=(1, 1), out_dtype=None, out=None, split_k: int = 0,

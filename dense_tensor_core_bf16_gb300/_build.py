@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libgemm_bf16.so")
 
-SOURCES = ["gemm_bf16.cu", "plan.cpp"]
+SOURCES = ["gemm_bf16.cu", "plan.cpp", "host_pipeline.cpp"]
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-lineinfo", "-O3", "-std=c++17",

@@ -1623,6 +1623,7 @@ gemm_status_t gemm_reserve_workspace(size_t bytes) {
 }
 
 void gemm_release_workspace(void) {
+    release_host_staging();   // takes its own per-device locks, never under g_mutex
     std::lock_guard<std::mutex> lock(g_mutex);
     int current = -1;
     if (cudaGetDevice(&current) != cudaSuccess) {

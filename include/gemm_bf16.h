@@ -381,10 +381,61 @@ gemm_status_t gemm_conv2d_plan(const gemm_conv2d_desc_t *d, gemm_dtype_t out_dty
 gemm_status_t gemm_conv2d_fprop_bf16(const gemm_conv2d_desc_t *d, const void *x, const void *w, void *y,
                                      gemm_dtype_t out_dtype, const gemm_options_t *opts, void *stream);
 
+/*
+ * Host-resident GEMMs, copies overlapped with the Tensor Core work.
+ *
+ * The pages measure the kernel on operands already in device memory; a caller
+ * whose matrices live in host memory also pays the copies over the host link,
+ * which for a 4096^3 problem take several times longer than the product.
+ * gemm_bf16_host_batch runs `count` independent problems whose A, B and C are
+ * HOST pointers.  Each problem's operands are copied into one of two device
+ * staging slots, the product is computed there by the kernels of gemm_bf16_ex,
+ * and C is copied back -- every problem moves its own bytes both ways -- but
+ * the library overlaps problem i's result copy and problem i+1's operand
+ * copies with the products on three streams of its own (operand copies,
+ * products, result copies).
+ *
+ *   problems[i]: sizes, layouts and leading dimensions as for gemm_bf16
+ *      (lda, ldb, ldc in elements of the host arrays; no alignment rule on the
+ *      host side: the staging copies are pitched to 16-byte rows on the
+ *      device, so any M, N, K are accepted).
+ *   out_dtype, opts: as for gemm_bf16_ex, applied to every problem; an
+ *      epilogue's bias stays a DEVICE array.  With an epilogue whose beta is
+ *      non-zero, C is also copied in before the product.
+ *   stream: the copies of problem 0 start after the work enqueued on `stream`
+ *      before the call, and `stream` waits for the last result copy, so a
+ *      cudaStreamSynchronize(stream) later means every C is in host memory.
+ *      The call itself returns once everything is enqueued: the host arrays
+ *      must stay valid and unchanged until then.
+ * Pinned host memory (cudaHostAlloc or cudaHostRegister) is needed for the
+ * copies to be asynchronous and to overlap; pageable memory gives the same
+ * results, with copies the CUDA runtime serialises through its own buffers.
+ * All problems are checked before anything is enqueued (INVALID_VALUE: a NULL
+ * pointer, a leading dimension below its minimum, a bad size, layout, type or
+ * option).  The staging slots grow on demand with cudaMalloc (synchronising
+ * the library's streams first); gemm_release_workspace frees them.  Calls on
+ * one device are serialised by a lock; the products share the split-K
+ * workspace with the other entry points, as usual. */
+typedef struct {
+    int64_t M, N, K;
+    const void *A;               /* host */
+    int64_t lda;
+    gemm_layout_t layout_a;
+    const void *B;               /* host */
+    int64_t ldb;
+    gemm_layout_t layout_b;
+    void *C;                     /* host, M x N row-major */
+    int64_t ldc;
+} gemm_host_problem_t;
+
+gemm_status_t gemm_bf16_host_batch(int64_t count, const gemm_host_problem_t *problems,
+                                   gemm_dtype_t out_dtype, const gemm_options_t *opts, void *stream);
+
 /* Grow the current device's split-K workspace to at least `bytes`. */
 gemm_status_t gemm_reserve_workspace(size_t bytes);
 
-/* Free the split-K workspaces of every device (waits for each device first). */
+/* Free the split-K workspaces and the host-batch staging slots of every
+ * device (waits for each device first). */
 void gemm_release_workspace(void);
 
 /*

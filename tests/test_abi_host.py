@@ -45,7 +45,8 @@ def test_binding_structs_match_the_header(tmp_path):
     import subprocess
     structs = {"gemm_device_desc_t": g.gemm_device_desc_t, "gemm_kernel_desc_t": g.gemm_kernel_desc_t,
                "gemm_plan_t": g.gemm_plan_t, "gemm_options_t": g.gemm_options_t,
-               "gemm_epilogue_t": g.gemm_epilogue_t, "gemm_conv2d_desc_t": g.gemm_conv2d_desc_t}
+               "gemm_epilogue_t": g.gemm_epilogue_t, "gemm_conv2d_desc_t": g.gemm_conv2d_desc_t,
+               "gemm_host_problem_t": g.gemm_host_problem_t}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "gemm_bf16.h"', "int main(void) {"]
     for name, cls in structs.items():
         lines.append(f'  printf("{name} %zu\\n", sizeof({name}));')
@@ -352,3 +353,32 @@ def test_conv2d_argument_checks_before_any_cuda_call():
     assert call(_conv(pad_h=128, H=300)) == 3                   # beyond an im2col pixel box's range
     assert call(_conv(R=65, dil_h=2, H=200)) == 3
     assert call(_conv(), opts=g.options(debug_skip_load=1)) == 1
+
+
+def _host(M=4, N=4, K=8, A=16, lda=8, la=0, B=16, ldb=8, lb=1, C=16, ldc=4):
+    return g.gemm_host_problem_t(M=M, N=N, K=K, A=A, lda=lda, layout_a=la, B=B, ldb=ldb, layout_b=lb, C=C, ldc=ldc)
+
+
+def test_host_batch_argument_checks_before_any_cuda_call():
+    """gemm_bf16_host_batch checks every problem before it enqueues anything;
+    no host-side rule on alignment (the device copies are pitched)."""
+    L = g.lib()
+    assert L.gemm_bf16_host_batch(-1, None, 0, None, None) == 1
+    assert L.gemm_bf16_host_batch(2, None, 0, None, None) == 1
+    assert g.gemm_bf16_host_batch([], 0, None, None) == 0
+    assert g.gemm_bf16_host_batch([_host()], 7, None, None) == 1                 # bad output type
+    assert g.gemm_bf16_host_batch([_host(la=2)], 0, None, None) == 1
+    assert g.gemm_bf16_host_batch([_host(M=-1)], 0, None, None) == 1
+    assert g.gemm_bf16_host_batch([_host(lda=7)], 0, None, None) == 1            # row-major A: lda < K
+    assert g.gemm_bf16_host_batch([_host(la=1, lda=3)], 0, None, None) == 1      # column-major A: lda < M
+    assert g.gemm_bf16_host_batch([_host(lb=0, ldb=3)], 0, None, None) == 1      # row-major B: ldb < N
+    assert g.gemm_bf16_host_batch([_host(ldc=3)], 0, None, None) == 1
+    assert g.gemm_bf16_host_batch([_host(C=0)], 0, None, None) == 1
+    assert g.gemm_bf16_host_batch([_host(A=0)], 0, None, None) == 1
+    assert g.gemm_bf16_host_batch([_host(K=0, A=0, B=0)], 0, g.options(timeout_ms=-1), None) == 1
+    bad = g.gemm_epilogue_t(alpha=1.0, beta=0.0, bias=None, activation=3)
+    assert g.gemm_bf16_host_batch([_host()], 0, g.gemm_options_t(epilogue=ctypes.pointer(bad)), None) == 1
+    # a bad problem anywhere in the batch rejects the whole batch
+    assert g.gemm_bf16_host_batch([_host(M=0), _host(), _host(ldb=2)], 0, None, None) == 1
+    # only empty problems: nothing to do, no device needed
+    assert g.gemm_bf16_host_batch([_host(M=0), _host(N=0, C=0)], 0, None, None) == 0
