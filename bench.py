@@ -450,11 +450,51 @@ def run_gpu(args, wname: str, w: dict, cpu_baseline: bool):
                      "h2d_bytes_per_step": int(hA[0].numel() * 2 + hB[0].numel() * 2),
                      "d2h_bytes_per_step": int(hC[0].numel() * hC[0].element_size()), "steps": e2e_steps,
                      "ms_per_step": round(e2e_ms / e2e_steps, 4),
-                     "api": "gemm_bf16_host_batch (host operands; copies overlapped with the products)"}
+                     "api": "gemm_bf16_host_batch (host operands; copies overlapped with the products)",
+                     "copy_floor": host_link_floor(hA[0], hB[0], hC[0], A0, B0, sets[0][2])}
 
     if cpu_baseline and rank == 0 and world == 1:
         result["cpu_baseline"] = cpu_oracle_baseline(A_h, Bt_h, M, N, K, target_s=args.cpu_seconds)
     return result, rank
+
+
+def host_link_floor(hA, hB, hC, dA, dB, dC, reps: int = 5) -> dict:
+    """What the host link alone allows per step: the step's operand bytes
+    host -> device and its C device -> host, each timed alone and both at once
+    on two streams (plain pinned copies, no product).  An end-to-end step can
+    be no faster than the concurrent figure."""
+    import torch
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    main = torch.cuda.current_stream()
+
+    def timed(do_in: bool, do_out: bool) -> float:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for r in range(reps + 2):
+            if r == 2:
+                e0.record(main)
+            start = torch.cuda.Event()
+            start.record(main)
+            for s, on in ((s_in, do_in), (s_out, do_out)):
+                if not on:
+                    continue
+                s.wait_event(start)
+                with torch.cuda.stream(s):
+                    if s is s_in:
+                        dA.copy_(hA, non_blocking=True)
+                        dB.copy_(hB, non_blocking=True)
+                    else:
+                        hC.copy_(dC, non_blocking=True)
+                done = torch.cuda.Event()
+                done.record(s)
+                main.wait_event(done)
+        e1.record(main)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    bin_, bout = hA.numel() * 2 + hB.numel() * 2, hC.numel() * hC.element_size()
+    t_in, t_out, t_both = timed(True, False), timed(False, True), timed(True, True)
+    return {"h2d_gbs": round(bin_ / (t_in * 1e-3) / 1e9, 1), "d2h_gbs": round(bout / (t_out * 1e-3) / 1e9, 1),
+            "ms_per_step_both_directions": round(t_both, 4)}
 
 
 # ---- the oracle on the host cores ---------------------------------------------------------

@@ -907,9 +907,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // holds row wq*32 + lane, columns chunk*32 + 4v .. +3, where
 // q = ((wq*(bn/32) + chunk)*8 + v)*32 + lane.
 // A CTA of 8 warps takes 32 consecutive float4s of the slots (one per lane);
-// warp w adds slices w, w+8, w+16, ... in increasing order (16 loads in
-// flight), and warp 0 then adds the 8 warp sums in order w = 0 .. 7.  The
-// order is the same on every run.
+// warp w adds slices w, w+8, w+16, ... in increasing order (BATCH loads in
+// flight: the smallest of 2, 4, 8, 16, 24 that covers a warp's slices, else
+// 24 per round), and warp 0 then adds the 8 warp sums in order w = 0 .. 7.  The
+// order is the same on every run, whatever BATCH.
 // With the fused epilogue (ep.epi), the sum of the slices takes the place of
 // the accumulator: C := act(alpha * sum + beta * C + bias[n]).
 constexpr int COMBINE_WARPS = 8;
@@ -921,7 +922,12 @@ struct EpilogueArgs {
     int act;
 };
 
-__global__ void __launch_bounds__(COMBINE_WARPS * 32)
+// Small batches keep to 64 registers (4 CTAs per SM), so that with a few
+// slices the whole grid fits on the SMs the GEMM leaves idle and waits there
+// (programmatic dependent launch); large ones take 128 (2 CTAs per SM) to
+// hold all their loads in flight.
+template <int BATCH>
+__global__ void __launch_bounds__(COMBINE_WARPS * 32, BATCH <= 8 ? 4 : 2)
     splitk_combine_kernel(const float *__restrict__ part, int split, long long tiles, int tiles_n, int tile_m, int bn,
                           int M, int N, void *C, long long ldc, int out_bf16, EpilogueArgs ep) {
     __shared__ float4 warp_sum[COMBINE_WARPS][32];
@@ -946,26 +952,31 @@ __global__ void __launch_bounds__(COMBINE_WARPS * 32)
         const bool live = idx < split_f4 && row < M && col < N;   // padding of the tiles is never read
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         if (live) {
+            // Every load of a round is issued before the first add, the
+            // round's tail included, so a warp's slices cost
+            // ceil(slices / BATCH) memory round trips; the adds then
+            // run in increasing slice order.
             const float4 *src = P + idx;
-            int s = warp;
-            for (; s + 15 * COMBINE_WARPS < split; s += 16 * COMBINE_WARPS) {
-                float4 w[16];
+            for (int s = warp; s < split; s += BATCH * COMBINE_WARPS) {
+                float4 w[BATCH];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) w[j] = __ldcs(src + static_cast<long long>(s + j * COMBINE_WARPS) * split_f4);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    acc.x += w[j].x;
-                    acc.y += w[j].y;
-                    acc.z += w[j].z;
-                    acc.w += w[j].w;
+                for (int j = 0; j < BATCH; ++j) {
+                    // past the last slice: reload the last one (in bounds, not
+                    // added), so the loads stay unconditional and all issue first
+                    const int sj = min(s + j * COMBINE_WARPS, split - 1);
+                    w[j] = __ldcs(src + static_cast<long long>(sj) * split_f4);
                 }
-            }
-            for (; s < split; s += COMBINE_WARPS) {
-                const float4 w1 = __ldcs(src + static_cast<long long>(s) * split_f4);
-                acc.x += w1.x;
-                acc.y += w1.y;
-                acc.z += w1.z;
-                acc.w += w1.w;
+                // A reloaded slice adds +0 instead, which leaves acc unchanged:
+                // acc starts at +0 and a sum of finite values is -0 only when
+                // both terms are -0, so acc is never -0.
+#pragma unroll
+                for (int j = 0; j < BATCH; ++j) {
+                    const bool in = s + j * COMBINE_WARPS < split;
+                    acc.x += in ? w[j].x : 0.0f;
+                    acc.y += in ? w[j].y : 0.0f;
+                    acc.z += in ? w[j].z : 0.0f;
+                    acc.w += in ? w[j].w : 0.0f;
+                }
             }
         }
         warp_sum[warp][lane] = acc;
@@ -1519,7 +1530,12 @@ gemm_status_t launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_
         pdl.val.programmaticStreamSerializationAllowed = 1;
         cc.attrs = &pdl;
         cc.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cc, splitk_combine_kernel, static_cast<const float *>(partials), plan.split_k,
+        const int per_warp = (plan.split_k + COMBINE_WARPS - 1) / COMBINE_WARPS;
+        auto combine = per_warp <= 2 ? splitk_combine_kernel<2>
+                     : per_warp <= 4 ? splitk_combine_kernel<4>
+                     : per_warp <= 8 ? splitk_combine_kernel<8>
+                     : per_warp <= 16 ? splitk_combine_kernel<16> : splitk_combine_kernel<24>;
+        if (cudaLaunchKernelEx(&cc, combine, static_cast<const float *>(partials), plan.split_k,
                                static_cast<long long>(plan.tiles), p.tiles_n, vi.tile_m, vi.bn, static_cast<int>(M),
                                static_cast<int>(N), C, static_cast<long long>(ldc),
                                out_dtype == GEMM_OUT_BF16 ? 1 : 0, ep) != cudaSuccess) {

@@ -34,7 +34,7 @@ def _gpu():
 
 
 def host(bits: np.ndarray, pinned: bool = True):
-    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+    t = torch.from_numpy(np.array(bits, dtype=np.uint16, order="C").view(np.int16)).view(torch.bfloat16)
     return t.pin_memory() if pinned else t.clone()
 
 
