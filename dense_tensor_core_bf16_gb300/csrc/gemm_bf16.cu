@@ -309,12 +309,27 @@ __device__ __forceinline__ float4 load_bias4(const float *bias, int col, int N) 
 // the producer and MMA threads, and a larger epilogue body measurably slows
 // the whole kernel.
 __device__ __forceinline__ void gelu_row_smem(uint32_t row_base, uint32_t sw) {
-#pragma unroll 2
-    for (int g = 0; g < 8; ++g) {
-        const uint32_t addr = row_base + ((static_cast<uint32_t>(g) ^ sw) << 4);
-        const uint4 u = ptx::ld_shared_v4(addr);
-        ptx::st_shared_v4(addr, __float_as_uint(gelu(__uint_as_float(u.x))), __float_as_uint(gelu(__uint_as_float(u.y))),
-                          __float_as_uint(gelu(__uint_as_float(u.z))), __float_as_uint(gelu(__uint_as_float(u.w))));
+    // Two halves of 16 values: every read of a half is issued before its
+    // evaluations and every write after them, so the 16 evaluations are
+    // independent (a read cannot be hoisted above an earlier write to the
+    // same buffer, so a loop that reads, evaluates and writes one piece at a
+    // time runs its pieces one after another).
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+        uint4 u[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            u[q] = ptx::ld_shared_v4(row_base + ((static_cast<uint32_t>(4 * h + q) ^ sw) << 4));
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            u[q].x = __float_as_uint(gelu(__uint_as_float(u[q].x)));
+            u[q].y = __float_as_uint(gelu(__uint_as_float(u[q].y)));
+            u[q].z = __float_as_uint(gelu(__uint_as_float(u[q].z)));
+            u[q].w = __float_as_uint(gelu(__uint_as_float(u[q].w)));
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            ptx::st_shared_v4(row_base + ((static_cast<uint32_t>(4 * h + q) ^ sw) << 4), u[q].x, u[q].y, u[q].z, u[q].w);
     }
 }
 
@@ -791,15 +806,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         asm volatile("prefetch.global.L1 [%0];" ::"l"(nxt));
                         if (!p.out_bf16) asm volatile("prefetch.global.L1 [%0];" ::"l"(nxt + 64));
                     }
-                    float4 cv[8], bv[8];
+                    float4 cv[8];
                     if (read_c) {
                         load_c32(cv, p.out, p.ld_out, p.out_bf16, row, col0, p.N);
                     } else {
 #pragma unroll
                         for (int g = 0; g < 8; ++g) cv[g] = make_float4(0.f, 0.f, 0.f, 0.f);
                     }
-#pragma unroll
-                    for (int g = 0; g < 8; ++g) bv[g] = load_bias4(p.bias, col0 + 4 * g, p.N);
+                    // the chunk's 32 bias values, one per lane (one coalesced load),
+                    // handed to every lane by shuffles below
+                    const float b_lane = p.bias && col0 + lane < p.N ? __ldg(p.bias + col0 + lane) : 0.0f;
                     uint32_t r[32];
                     __syncwarp();
                     ptx::tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r);
@@ -807,10 +823,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (w.kind == KIND_OWNER) add_partials(r, c);
 #pragma unroll
                     for (int g = 0; g < 8; ++g) {
-                        r[4 * g + 0] = __float_as_uint(epilogue_linear(__uint_as_float(r[4 * g + 0]), cv[g].x, bv[g].x, p.alpha, p.beta, p.act));
-                        r[4 * g + 1] = __float_as_uint(epilogue_linear(__uint_as_float(r[4 * g + 1]), cv[g].y, bv[g].y, p.alpha, p.beta, p.act));
-                        r[4 * g + 2] = __float_as_uint(epilogue_linear(__uint_as_float(r[4 * g + 2]), cv[g].z, bv[g].z, p.alpha, p.beta, p.act));
-                        r[4 * g + 3] = __float_as_uint(epilogue_linear(__uint_as_float(r[4 * g + 3]), cv[g].w, bv[g].w, p.alpha, p.beta, p.act));
+                        const float b0 = __shfl_sync(0xffffffffu, b_lane, 4 * g + 0);
+                        const float b1 = __shfl_sync(0xffffffffu, b_lane, 4 * g + 1);
+                        const float b2 = __shfl_sync(0xffffffffu, b_lane, 4 * g + 2);
+                        const float b3 = __shfl_sync(0xffffffffu, b_lane, 4 * g + 3);
+                        r[4 * g + 0] = __float_as_uint(epilogue_linear(__uint_as_float(r[4 * g + 0]), cv[g].x, b0, p.alpha, p.beta, p.act));
+                        r[4 * g + 1] = __float_as_uint(epilogue_linear(__uint_as_float(r[4 * g + 1]), cv[g].y, b1, p.alpha, p.beta, p.act));
+                        r[4 * g + 2] = __float_as_uint(epilogue_linear(__uint_as_float(r[4 * g + 2]), cv[g].z, b2, p.alpha, p.beta, p.act));
+                        r[4 * g + 3] = __float_as_uint(epilogue_linear(__uint_as_float(r[4 * g + 3]), cv[g].w, b3, p.alpha, p.beta, p.act));
                     }
                     stage_store(r, col0, p.act == GEMM_ACT_GELU);
                 }
