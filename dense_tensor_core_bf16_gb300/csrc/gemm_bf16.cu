@@ -44,7 +44,8 @@ enum : unsigned {
     SITE_MMA_ACC = 4u,
     SITE_EPI_ACC = 8u,
     SITE_DRAIN = 16u,
-    SITE_FIXUP = 32u
+    SITE_FIXUP = 32u,
+    SITE_EPI_C = 64u
 };
 
 struct KernelParams {
@@ -273,27 +274,6 @@ __device__ __forceinline__ float4 load_c4(const void *C, long long ldc, int out_
     return make_float4(e[0], e[1], e[2], e[3]);
 }
 
-// The 32 previous values of C at (row, col0 .. col0+31), as fp32; 16-byte
-// loads when the chunk lies inside C, element loads at the ragged edge.
-__device__ __forceinline__ void load_c32(float4 (&cv)[8], const void *C, long long ldc, int out_bf16, int row, int col0,
-                                         int N) {
-    if (out_bf16 && col0 + 32 <= N) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(C) +
-                                                           static_cast<long long>(row) * ldc + col0);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const uint4 u = src[q];
-            cv[2 * q] = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
-                                    __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
-            cv[2 * q + 1] = make_float4(__uint_as_float(u.z << 16), __uint_as_float(u.z & 0xFFFF0000u),
-                                        __uint_as_float(u.w << 16), __uint_as_float(u.w & 0xFFFF0000u));
-        }
-        return;
-    }
-#pragma unroll
-    for (int g = 0; g < 8; ++g) cv[g] = load_c4(C, ldc, out_bf16, row, col0 + 4 * g, N);
-}
-
 // Four bias values for columns col .. col+3 (0 beyond N or without a bias).
 __device__ __forceinline__ float4 load_bias4(const float *bias, int col, int N) {
     if (!bias) return make_float4(0.f, 0.f, 0.f, 0.f);
@@ -394,7 +374,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     constexpr int BAR_ACC_FULL = 2 * STAGES;              // [ACC_BUFS] accumulator complete
     constexpr int BAR_ACC_EMPTY = 2 * STAGES + ACC_BUFS;  // [ACC_BUFS] accumulator drained (leader's)
     constexpr int BAR_DRAIN = 2 * STAGES + 2 * ACC_BUFS;  // all MMAs of this CTA done
-    constexpr int NUM_BARRIERS = 2 * STAGES + 2 * ACC_BUFS + 1;
+    constexpr int BAR_CLOAD = 2 * STAGES + 2 * ACC_BUFS + 1;   // [2 per epilogue warp] previous C landed
+    constexpr int NUM_BARRIERS = 2 * STAGES + 2 * ACC_BUFS + 1 + 2 * EPI_WARPS;
+    static_assert(NUM_BARRIERS_FIXED == 2 * ACC_BUFS + 1 + 2 * EPI_WARPS, "barrier count");
     constexpr uint32_t IDESC = ptx::idesc_bf16_f32(CTA_ROWS * CG, BN);
     constexpr uint32_t TX_BYTES = CG * V.stage;           // bytes both CTAs land per stage
     constexpr bool PAIR = CG == 2;
@@ -438,6 +420,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::mbar_init(bar(BAR_ACC_EMPTY + b), EPI_WARPS * CG); // one lane per epilogue warp of each CTA
         }
         ptx::mbar_init(bar(BAR_DRAIN), 1);
+        for (int i = 0; i < 2 * EPI_WARPS; ++i) ptx::mbar_init(bar(BAR_CLOAD + i), 1);   // lane 0 + the box's bytes
         *abort_flag = 0;
         ptx::fence_barrier_init();
     }
@@ -662,6 +645,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // which also keeps the 32 lanes' writes free of bank conflicts.
         const uint32_t epi_buf0 = sEpi + static_cast<uint32_t>(quarter) * 2u * EPI_BUF_BYTES;
         uint32_t stores_issued = 0;
+        uint32_t c_phase = 0;     // bit b: parity of the next completion of this warp's C-load barrier b
+        uint32_t c_pending = 0;   // bit b: a load of previous C into buffer b not yet waited for
         uint32_t tc = 0;
         Schedule sched(p, cluster);
         Unit w;
@@ -788,27 +773,81 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 ++stores_issued;
             };
+            bool c_ok = true;   // false: a wait for previous C gave up (the CTA aborts)
             if (p.epi && !to_slot) {
                 // Fused epilogue, one chunk at a time in a rolled loop so that the
                 // code stays small: the row's previous C and bias values are
                 // loaded first (their latencies overlap the TMEM read), the
                 // linear part and ReLU run on registers, GELU through the
                 // staging buffer (gelu_row_smem).
-                const int row = warp_row0 + lane;
-                const bool read_c = p.beta != 0.0f && row < p.M;
+                // With beta != 0 the previous C comes in by TMA, one 32 x 32 chunk
+                // ahead, into the staging buffer the chunk's result will leave
+                // from, in the same swizzled layout (rows past M and columns past
+                // N arrive as zeros); each lane then reads its own row of it.
+                const bool read_c = p.beta != 0.0f && warp_row0 < p.M;   // warp-uniform
+                const uint32_t c_bar = bar(BAR_CLOAD + 2 * quarter);
+                const uint32_t c_bytes = 32u * 32u * (p.out_bf16 ? 2u : 4u);
+                const uint32_t s0 = stores_issued;   // chunk c leaves from buffer (s0 + c) & 1
+                auto load_c_chunk = [&](int col0, uint32_t slot) {
+                    c_pending |= 1u << slot;
+                    if (lane == 0) {
+                        ptx::mbar_arrive_expect_tx(c_bar + 8u * slot, c_bytes);
+                        ptx::tma_load_2d(epi_buf0 + slot * EPI_BUF_BYTES, &tmap_c, c_bar + 8u * slot, col0, warp_row0);
+                    }
+                };
+                if (read_c) {
+                    if (s0 >= 2 && lane == 0) ptx::bulk_wait_group_read<1>();   // buffer s0 & 1 read out
+                    __syncwarp();
+                    load_c_chunk(col_base, s0 & 1u);
+                }
 #pragma unroll 1
                 for (int c = 0; c < n_chunks; ++c) {
                     const int col0 = col_base + c * 32;
-                    if (read_c && c + 1 < n_chunks) {
-                        // the next chunk's previous values of C, on their way to L1
-                        const char *nxt = static_cast<const char *>(p.out) +
-                                          (static_cast<long long>(row) * p.ld_out + col0 + 32) * (p.out_bf16 ? 2 : 4);
-                        asm volatile("prefetch.global.L1 [%0];" ::"l"(nxt));
-                        if (!p.out_bf16) asm volatile("prefetch.global.L1 [%0];" ::"l"(nxt + 64));
-                    }
+                    const uint32_t slot = (s0 + static_cast<uint32_t>(c)) & 1u;
                     float4 cv[8];
                     if (read_c) {
-                        load_c32(cv, p.out, p.ld_out, p.out_bf16, row, col0, p.N);
+                        if (c + 1 < n_chunks) {
+                            // the other buffer's last store (the previous chunk's) must
+                            // have been read out before the next chunk's C lands there
+                            if (lane == 0) ptx::bulk_wait_group_read<0>();
+                            __syncwarp();
+                            load_c_chunk(col0 + 32, slot ^ 1u);
+                        }
+                        c_ok = __all_sync(0xffffffffu, wait_phase<false>(c_bar + 8u * slot, (c_phase >> slot) & 1u,
+                                                                         abort_flag, p.timeout_ns, SITE_EPI_C, true));
+                        if (!c_ok) {
+                            // loads may still be landing in the buffers: wait for them
+                            // (bounded) before this warp leaves
+                            for (uint32_t b = 0; b < 2; ++b)
+                                if ((c_pending >> b) & 1u)
+                                    wait_phase<false>(c_bar + 8u * b, (c_phase >> b) & 1u, abort_flag, p.timeout_ns,
+                                                      SITE_EPI_C, false);
+                            break;
+                        }
+                        c_phase ^= 1u << slot;
+                        c_pending &= ~(1u << slot);
+                        const uint32_t cbuf = epi_buf0 + slot * EPI_BUF_BYTES;
+                        if (p.out_bf16) {
+                            const uint32_t row_base = cbuf + static_cast<uint32_t>(lane) * 64u;
+                            const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
+#pragma unroll
+                            for (int v = 0; v < 4; ++v) {
+                                const uint4 u = ptx::ld_shared_v4(row_base + ((static_cast<uint32_t>(v) ^ sw) << 4));
+                                cv[2 * v] = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                                                        __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+                                cv[2 * v + 1] = make_float4(__uint_as_float(u.z << 16), __uint_as_float(u.z & 0xFFFF0000u),
+                                                            __uint_as_float(u.w << 16), __uint_as_float(u.w & 0xFFFF0000u));
+                            }
+                        } else {
+                            const uint32_t row_base = cbuf + static_cast<uint32_t>(lane) * 128u;
+                            const uint32_t sw = static_cast<uint32_t>(lane) & 7u;
+#pragma unroll
+                            for (int v = 0; v < 8; ++v) {
+                                const uint4 u = ptx::ld_shared_v4(row_base + ((static_cast<uint32_t>(v) ^ sw) << 4));
+                                cv[v] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
+                                                    __uint_as_float(u.w));
+                            }
+                        }
                     } else {
 #pragma unroll
                         for (int g = 0; g < 8; ++g) cv[g] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -884,6 +923,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (c + 1 < n_chunks) ptx::tmem_wait_ld(rbuf[(c + 1) & 1]);
             }
             }
+            if (!c_ok) break;
             if (w.kind == KIND_PARTIAL) {
                 // publish: every lane's stores, then one release of the flag
                 __threadfence();

@@ -30,7 +30,9 @@ constexpr int ACC_BUFS = 2;               // accumulators in TMEM (epilogue over
 constexpr int NUM_WARPS = 6;              // 0: TMA producer, 1: TMEM owner + MMA issuer, 2..5: epilogue
 constexpr int NUM_THREADS = NUM_WARPS * 32;
 constexpr int EPI_WARPS = 4;
-constexpr int NUM_BARRIERS_FIXED = 2 * ACC_BUFS + 1;   // + 2 per stage
+// accumulator full/empty, drain, and per epilogue warp two loads of previous
+// C into its staging buffers (the fused epilogue with beta != 0); + 2 per stage
+constexpr int NUM_BARRIERS_FIXED = 2 * ACC_BUFS + 1 + 2 * 4;
 constexpr int SMEM_LIMIT = 232448;        // opt-in dynamic shared memory per CTA on sm_100-class parts
 constexpr int MAX_STAGES = 8;
 // Epilogue staging: per epilogue warp, two buffers of one 32 x 32 chunk of C

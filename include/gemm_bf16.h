@@ -443,7 +443,8 @@ void gemm_release_workspace(void);
  * word: GEMM_OK, GEMM_ERR_DEVICE_TIMEOUT (a pipeline wait ran out of time;
  * if `where` is not NULL it receives the bit set of the waits that gave up:
  * 1 producer slot wait, 2 MMA operand wait, 4 MMA accumulator wait,
- * 8 epilogue accumulator wait, 16 end-of-kernel drain), or GEMM_ERR_LAUNCH
+ * 8 epilogue accumulator wait, 16 end-of-kernel drain, 32 stream-K partial
+ * hand-off, 64 fused epilogue's load of the previous C), or GEMM_ERR_LAUNCH
  * if the synchronisation itself failed.
  */
 gemm_status_t gemm_get_device_status(void *stream, unsigned int *where);
