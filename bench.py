@@ -311,17 +311,19 @@ def run_gpu(args, wname: str, w: dict, cpu_baseline: bool):
         a, b, c = sets[i % copies]
         g.matmul(a, b, out=c, **kw, **extra)
 
+    # The clock sampler starts before the warm-up, so that the GPU does not sit
+    # idle between the warm-up and the timed region (after an idle gap the
+    # first launches of a short step run slower).
+    gpu_id = getattr(props, "uuid", None)
+    gpu_id = f"GPU-{gpu_id}" if gpu_id is not None else str(local)
+    sampler = ClockSampler(gpu_id)
+    time.sleep(0.3)
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
     st, where = g.gemm_get_device_status(None)
     if st:
         raise RuntimeError(f"device fault during warm-up: {where:#x}")
-
-    gpu_id = getattr(props, "uuid", None)
-    gpu_id = f"GPU-{gpu_id}" if gpu_id is not None else str(local)
-    sampler = ClockSampler(gpu_id)
-    time.sleep(0.3)
 
     # The K steps go back to back between two events (events between launches
     # would break the overlap of one launch's prologue with the previous one's
@@ -658,15 +660,15 @@ def run_gpu_conv(args, wname: str, w: dict):
         xx, ww, yy = sets[i % copies]
         g.conv2d(xx, ww, out=yy, **kw)
 
+    gpu_id = getattr(props, "uuid", None)
+    sampler = ClockSampler(f"GPU-{gpu_id}" if gpu_id is not None else str(local))
+    time.sleep(0.3)   # before the warm-up: no idle gap before the timed region
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
     st, where = g.gemm_get_device_status(None)
     if st:
         raise RuntimeError(f"device fault during warm-up: {where:#x}")
-    gpu_id = getattr(props, "uuid", None)
-    sampler = ClockSampler(f"GPU-{gpu_id}" if gpu_id is not None else str(local))
-    time.sleep(0.3)
     stream = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()

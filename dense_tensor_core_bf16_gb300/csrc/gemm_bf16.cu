@@ -924,6 +924,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             }
             if (!c_ok) break;
+            if (w.kind == KIND_OWNER && lane == 0) {
+                // The owner clears the flags it consumed, so that every launch
+                // starts from cleared flags -- also one replayed from a captured
+                // graph, which carries the epoch it was captured with.  (The next
+                // launch in the stream writes flags only after this grid ends.)
+                for (long long c2 = cluster + 1; c2 < contrib_end; ++c2)
+                    if (sk_range_start(p, c2 + 1) != sk_range_start(p, c2))
+                        p.sk_flags[c2 * (CG * EPI_WARPS) + flag_idx] = 0u;
+            }
             if (w.kind == KIND_PARTIAL) {
                 // publish: every lane's stores, then one release of the flag
                 __threadfence();
@@ -1151,7 +1160,7 @@ struct DeviceState {
     VariantState var[VARIANT_COUNT];
     float *workspace = nullptr;
     size_t workspace_bytes = 0;
-    unsigned int *sk_flags = nullptr;   // zeroed once; each launch writes its own epoch
+    unsigned int *sk_flags = nullptr;   // zeroed once; contributors publish the launch's epoch, owners clear
     unsigned int epoch = 0;
 };
 
