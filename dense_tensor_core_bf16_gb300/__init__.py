@@ -292,38 +292,76 @@ def _round_up(x: int, m: int) -> int:
     return max(m, (x + m - 1) // m * m)
 
 
+_OUT_DTYPES: dict = {}
+
+
+def _out_dtypes():
+    import torch
+    if not _OUT_DTYPES:
+        _OUT_DTYPES.update({torch.float32: GEMM_OUT_F32, torch.bfloat16: GEMM_OUT_BF16})
+    return _OUT_DTYPES
+
+
 def _stream_handle(stream):
+    """The raw cudaStream_t of ``stream`` (a torch stream or an integer), or of
+    the current stream when it is None.  torch's raw accessor of the current
+    stream is about a microsecond cheaper per call than building a Stream
+    object; it is used when this torch has it."""
     import torch
     if stream is None:
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is not None:
+            return raw(torch.cuda.current_device())
         stream = torch.cuda.current_stream()
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def _layouts(A, B):
-    """(layout_a, lda, layout_b, ldb) from the strides.  A: row-major when K is
+def _layouts(A, B, sa=None, sb=None):
+    """(layout_a, lda, layout_b, ldb) from the strides (``sa``, ``sb``: the
+    tensors' stride tuples when the caller has them).  A: row-major when K is
     contiguous (or K <= 1), else column-major when M is contiguous (or M <= 1);
     B alike, column-major first.  A dimension of extent 1 has no real leading
     dimension: report the smallest aligned one so the alignment rule does not
     reject it."""
     M, K = A.shape
     N = B.shape[1]
-    if K <= 1 or A.stride(1) == 1:
+    sa = A.stride() if sa is None else sa
+    sb = B.stride() if sb is None else sb
+    if K <= 1 or sa[1] == 1:
         a_layout = GEMM_ROW_MAJOR
-        lda = A.stride(0) if M > 1 else _round_up(K, 8)
-    elif M <= 1 or A.stride(0) == 1:
+        lda = sa[0] if M > 1 else _round_up(K, 8)
+    elif M <= 1 or sa[0] == 1:
         a_layout = GEMM_COL_MAJOR
-        lda = A.stride(1) if K > 1 else _round_up(M, 8)
+        lda = sa[1] if K > 1 else _round_up(M, 8)
     else:
         raise ValueError("A must be row-major (stride (lda, 1)) or column-major (stride (1, lda))")
-    if K <= 1 or B.stride(0) == 1:
+    if K <= 1 or sb[0] == 1:
         b_layout = GEMM_COL_MAJOR
-        ldb = B.stride(1) if N > 1 else _round_up(K, 8)
-    elif N <= 1 or B.stride(1) == 1:
+        ldb = sb[1] if N > 1 else _round_up(K, 8)
+    elif N <= 1 or sb[1] == 1:
         b_layout = GEMM_ROW_MAJOR
-        ldb = B.stride(0) if K > 1 else _round_up(N, 8)
+        ldb = sb[0] if K > 1 else _round_up(N, 8)
     else:
         raise ValueError("B must be column-major (stride (1, ldb)) or row-major (stride (ldb, 1))")
     return a_layout, lda, b_layout, ldb
+
+
+# Option structs without an epilogue or event, by their fields: reused from
+# call to call (the library copies *opts during the call and keeps nothing).
+_OPTS_CACHE: dict = {}
+
+
+def _plain_options(key) -> "gemm_options_t":
+    o = _OPTS_CACHE.get(key)
+    if o is None:
+        if len(_OPTS_CACHE) > 256:
+            _OPTS_CACHE.clear()
+        split_k, non_persistent, raster_group_m, timeout_ms, debug_skip_load, kernel_variant, no_stream_k = key
+        o = gemm_options_t(split_k=split_k, non_persistent=non_persistent, raster_group_m=raster_group_m,
+                           timeout_ms=timeout_ms, debug_skip_load=debug_skip_load, kernel_variant=kernel_variant,
+                           no_stream_k=no_stream_k)
+        _OPTS_CACHE[key] = o
+    return o
 
 
 def matmul(A, B, *, out_dtype=None, out=None, split_k: int = 0, non_persistent: bool = False,
@@ -363,20 +401,26 @@ def matmul(A, B, *, out_dtype=None, out=None, split_k: int = 0, non_persistent: 
         out = torch.empty((M, N), dtype=dt, device=A.device)
     if out.shape != (M, N):
         raise ValueError("out has the wrong shape")
-    if M and N and out.stride(1) != 1:
+    so = out.stride()
+    if M and N and so[1] != 1:
         raise ValueError("out must be row-major")
-    odt = {torch.float32: GEMM_OUT_F32, torch.bfloat16: GEMM_OUT_BF16}.get(out.dtype)
+    odt = _out_dtypes().get(out.dtype)
     if odt is None:
         raise TypeError("out must be float32 or bfloat16")
-    a_layout, lda, b_layout, ldb = _layouts(A, B)
-    ldc = out.stride(0) if M > 1 else _round_up(N, 8)
-    opts = gemm_options_t(split_k=split_k, non_persistent=int(non_persistent), raster_group_m=raster_group_m,
-                          mainloop_done_event=(mainloop_done_event.cuda_event if mainloop_done_event is not None
-                                               else None),
-                          timeout_ms=timeout_ms, debug_skip_load=debug_skip_load, kernel_variant=kernel_variant,
-                          no_stream_k=int(no_stream_k))
+    a_layout, lda, b_layout, ldb = _layouts(A, B, A.stride(), B.stride())
+    ldc = so[0] if M > 1 else _round_up(N, 8)
+    with_epilogue = alpha != 1.0 or beta != 0.0 or bias is not None or activation != "none"
+    if mainloop_done_event is None and not with_epilogue:
+        opts = _plain_options((split_k, int(non_persistent), raster_group_m, timeout_ms, debug_skip_load,
+                               kernel_variant, int(no_stream_k)))
+    else:
+        opts = gemm_options_t(split_k=split_k, non_persistent=int(non_persistent), raster_group_m=raster_group_m,
+                              mainloop_done_event=(mainloop_done_event.cuda_event if mainloop_done_event is not None
+                                                   else None),
+                              timeout_ms=timeout_ms, debug_skip_load=debug_skip_load, kernel_variant=kernel_variant,
+                              no_stream_k=int(no_stream_k))
     epi = None
-    if alpha != 1.0 or beta != 0.0 or bias is not None or activation != "none":
+    if with_epilogue:
         epi = gemm_epilogue_t(alpha=alpha, beta=beta, bias=bias.data_ptr() if bias is not None else None,
                               activation=ACTIVATIONS[activation])
         opts.epilogue = ctypes.pointer(epi)
