@@ -357,6 +357,33 @@ def test_splitk_128x256x65536_all_splits(oracle_lib):
         assert np.array_equal(Ci.astype(np.float64), refi), f"split {split} not exact on integers"
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_combine_every_batch_and_several_rounds(oracle_lib, variant):
+    """The combine loads a warp's slices in batches of 2, 4, 8, 16 or 24 (the
+    smallest that covers ceil(split / 8)), in rounds of 24 past 192 slices:
+    splits that reach every batch and up to three rounds, against the oracle,
+    run to run, and exactly on integers."""
+    M, N, K = 128, 256, 65536
+    A, Bt = operands(M, N, K, "uniform", True, SEED + 12)
+    ref, sabs = oracle_lib.gemm(A, Bt, M, N, K)
+    g = _lib()
+    dA, dBt = to_dev(A), to_dev(Bt)
+    for split in (16, 40, 64, 120, 192, 200, 400):
+        C1 = g.matmul(dA, dBt.t(), out_dtype=torch.float32, split_k=split, kernel_variant=variant)
+        C2 = g.matmul(dA, dBt.t(), out_dtype=torch.float32, split_k=split, kernel_variant=variant)
+        C1, C2 = C1.cpu().numpy(), C2.cpu().numpy()
+        assert np.array_equal(C1, C2), f"split {split} not deterministic"
+        nbad, worst = check_f32(C1, ref, sabs)
+        assert nbad == 0, f"split {split}: {nbad} entries outside the bound ({worst:.3g})"
+    Ki = 32768   # int4 products summed over 32768 stay below 2^24: exact in any order
+    Ai, Bti = operands(M, N, Ki, "int4", False, SEED + 14)
+    refi, _ = oracle_lib.gemm(Ai, Bti, M, N, Ki)
+    dAi, dBti = to_dev(Ai), to_dev(Bti)
+    for split in (40, 200, 400):
+        Ci = g.matmul(dAi, dBti.t(), out_dtype=torch.float32, split_k=split, kernel_variant=variant).cpu().numpy()
+        assert np.array_equal(Ci.astype(np.float64), refi), f"split {split} not exact on integers"
+
+
 def test_large_16384x8192x8192_persistent_and_one_cta_per_tile(oracle_lib):
     M, N, K = 16384, 8192, 8192
     A, Bt = operands(M, N, K, "normal", True, SEED + 14)
