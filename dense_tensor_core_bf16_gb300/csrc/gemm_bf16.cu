@@ -480,14 +480,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             while (ok && sched.next(p, w)) {
                 const int row_a = w.tm * V.tile_m + static_cast<int>(rank) * CTA_ROWS;
                 const int row_b = w.tn * BN + static_cast<int>(rank) * V.b_rows;
-                // convolution: the window origin of this CTA's first output pixel
+                // convolution: the window origin of this CTA's first output pixel,
+                // and the (tap, channel block) of the unit's first box -- stepped
+                // box by box below, so the loop itself divides nothing
                 int cv_n = 0, cv_h = 0, cv_w = 0;
+                int cv_tap = 0, cv_cb = 0, cv_r = 0, cv_s = 0;
                 if (p.conv) {
                     cv_n = row_a / p.cv_PQ;
                     const int pq = row_a - cv_n * p.cv_PQ;
                     const int pp = pq / p.cv_Q;
                     cv_h = pp * p.str_h - p.pad_h;
                     cv_w = (pq - pp * p.cv_Q) * p.str_w - p.pad_w;
+                    const int bi0 = w.kb_begin * V.k_boxes;
+                    cv_tap = bi0 / p.ncb;
+                    cv_cb = bi0 - cv_tap * p.ncb;
+                    cv_r = cv_tap / p.cv_S;
+                    cv_s = cv_tap - cv_r * p.cv_S;
                 }
                 for (int kb = 0; kb < w.kb_count; ++kb, ++it) {
                     const uint32_t s = it % STAGES;
@@ -518,16 +526,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         // the filter.  Boxes past the last tap point at channel
                         // 64 ncb (>= C): both read as zeros.
                         for (int j = 0; j < V.k_boxes; ++j) {
-                            const int bi = (w.kb_begin + kb) * V.k_boxes + j;
-                            int tap = bi / p.ncb;
-                            int c0 = (bi - tap * p.ncb) * TILE_K;
+                            // box (kb_begin + kb) * k_boxes + j is channel block
+                            // cv_cb of tap cv_tap = cv_r * S + cv_s
+                            int tap = cv_tap, c0 = cv_cb * TILE_K, r = cv_r, sx = cv_s;
                             if (tap >= p.cv_taps) {
                                 tap = 0;
                                 c0 = p.ncb * TILE_K;
+                                r = 0;
+                                sx = 0;
                             }
-                            const int r = tap / p.cv_S;
+                            if (++cv_cb == p.ncb) {
+                                cv_cb = 0;
+                                ++cv_tap;
+                                if (++cv_s == p.cv_S) {
+                                    cv_s = 0;
+                                    ++cv_r;
+                                }
+                            }
                             const uint16_t off_h = static_cast<uint16_t>(r * p.dil_h);
-                            const uint16_t off_w = static_cast<uint16_t>((tap - r * p.cv_S) * p.dil_w);
+                            const uint16_t off_w = static_cast<uint16_t>(sx * p.dil_w);
                             const uint32_t dst_a = sA + s * V.a_stage + j * A_BOX;
                             const uint32_t dst_b = sB + s * V.b_stage + j * B_BOX;
                             if constexpr (PAIR) {
