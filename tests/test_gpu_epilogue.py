@@ -153,6 +153,21 @@ def test_epilogue_on_stream_k_tiles(oracle_lib, variant, shape):
     check(oracle_lib, A, Bt, C, "f32", C0, bias, 1.0, 1.0, "relu", exact=True)
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("non_persistent", [False, True])
+def test_previous_c_over_many_tiles_per_cta(oracle_lib, variant, non_persistent):
+    """gelu(A.B + C/2 + bias) with more tiles than resident CTAs: the loads of
+    the previous C alternate between each warp's two staging buffers across
+    tiles (persistent), or start afresh in every CTA (one cluster per tile)."""
+    M, N, K = 2560, 2304, 136
+    A, Bt = operands(M, N, K, "normal", True, SEED + 20)
+    C0, bias = c_old_and_bias(M, N, SEED + 21)
+    for out in ("bf16", "f32"):
+        C = run(A, Bt, out, C0, bias, kernel_variant=variant, non_persistent=non_persistent, no_stream_k=True,
+                alpha=1.0, beta=0.5, activation="gelu")
+        check(oracle_lib, A, Bt, C, out, C0, bias, 1.0, 0.5, "gelu")
+
+
 def test_epilogue_with_row_major_b(oracle_lib):
     M, N, K = 513, 769, 1000
     A, Bt = operands(M, N, K, "normal", True, SEED + 8)
