@@ -151,7 +151,7 @@ gemm_status_t ensure_slots(HostPipe &p, size_t a, size_t b, size_t c) {
 }
 
 // The host-side checks first (no CUDA call), then the plan on the current
-// device, which also rejects what this build cannot run.
+// device, which also rejects what the library cannot run.
 gemm_status_t check_host_problem(const gemm_host_problem_t &p, gemm_dtype_t out, const gemm_options_t *opts) {
     gemm_status_t st = check_problem(p.M, p.N, p.K, p.layout_a, p.layout_b, out, opts ? opts->split_k : 0);
     if (st != GEMM_OK) return st;

@@ -56,7 +56,7 @@ typedef enum {
     GEMM_OK = 0,
     GEMM_ERR_INVALID_VALUE = 1,   /* negative or too large size, bad enum, short ld, NULL */
     GEMM_ERR_MISALIGNED = 2,      /* a pointer or leading dimension breaks the rules above */
-    GEMM_ERR_NOT_SUPPORTED = 3,   /* a request this build cannot run (too many stream-K clusters;
+    GEMM_ERR_NOT_SUPPORTED = 3,   /* a request the library cannot run (too many stream-K clusters;
                                      a convolution beyond an im2col box's range) */
     GEMM_ERR_NO_DEVICE = 4,       /* no usable CUDA device, or not an sm_103 part */
     GEMM_ERR_OUT_OF_MEMORY = 5,   /* the split-K workspace could not be grown */
