@@ -283,36 +283,6 @@ __device__ __forceinline__ float4 load_bias4(const float *bias, int col, int N) 
     return make_float4(e[0], e[1], e[2], e[3]);
 }
 
-// GELU on one lane's row of a 32 x 32 chunk staged as fp32 in the warp's
-// buffer (piece v = columns 4v .. 4v+3 at row_base + ((v ^ sw) << 4)).  The
-// loop stays rolled: the epilogue warps share the SM's instruction cache with
-// the producer and MMA threads, and a larger epilogue body measurably slows
-// the whole kernel.
-__device__ __forceinline__ void gelu_row_smem(uint32_t row_base, uint32_t sw) {
-    // Two halves of 16 values: every read of a half is issued before its
-    // evaluations and every write after them, so the 16 evaluations are
-    // independent (a read cannot be hoisted above an earlier write to the
-    // same buffer, so a loop that reads, evaluates and writes one piece at a
-    // time runs its pieces one after another).
-#pragma unroll 1
-    for (int h = 0; h < 2; ++h) {
-        uint4 u[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            u[q] = ptx::ld_shared_v4(row_base + ((static_cast<uint32_t>(4 * h + q) ^ sw) << 4));
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            u[q].x = __float_as_uint(gelu(__uint_as_float(u[q].x)));
-            u[q].y = __float_as_uint(gelu(__uint_as_float(u[q].y)));
-            u[q].z = __float_as_uint(gelu(__uint_as_float(u[q].z)));
-            u[q].w = __float_as_uint(gelu(__uint_as_float(u[q].w)));
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            ptx::st_shared_v4(row_base + ((static_cast<uint32_t>(4 * h + q) ^ sw) << 4), u[q].x, u[q].y, u[q].z, u[q].w);
-    }
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_bits, uint32_t hi_bits) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(lo_bits), __uint_as_float(hi_bits));
     return *reinterpret_cast<const uint32_t *>(&v);
@@ -745,24 +715,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 __syncwarp();
                 const uint32_t buf = epi_buf0 + (stores_issued & 1u) * EPI_BUF_BYTES;
                 if (with_gelu) {
-                    // GELU through this lane's fp32 row of the buffer (swizzled
-                    // as the fp32 staging below), and back into registers
-                    const uint32_t row_base = buf + static_cast<uint32_t>(lane) * 128u;
-                    const uint32_t sw = static_cast<uint32_t>(lane) & 7u;
+                    // on registers: 32 independent evaluations, and no round trip
+                    // through shared memory, whose bandwidth the main loop's
+                    // copies and MMAs are already using
 #pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        ptx::st_shared_v4(row_base + ((static_cast<uint32_t>(v) ^ sw) << 4), r[4 * v + 0], r[4 * v + 1],
-                                          r[4 * v + 2], r[4 * v + 3]);
-                    gelu_row_smem(row_base, sw);
-#pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        const uint4 u = ptx::ld_shared_v4(row_base + ((static_cast<uint32_t>(v) ^ sw) << 4));
-                        r[4 * v + 0] = u.x;
-                        r[4 * v + 1] = u.y;
-                        r[4 * v + 2] = u.z;
-                        r[4 * v + 3] = u.w;
-                    }
-                    __syncwarp();   // the staging below writes into other lanes' rows
+                    for (int q = 0; q < 32; ++q) r[q] = __float_as_uint(gelu(__uint_as_float(r[q])));
                 }
                 if (p.out_bf16) {
                     const uint32_t row_base = buf + static_cast<uint32_t>(lane) * 64u;
@@ -793,10 +750,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool c_ok = true;   // false: a wait for previous C gave up (the CTA aborts)
             if (p.epi && !to_slot) {
                 // Fused epilogue, one chunk at a time in a rolled loop so that the
-                // code stays small: the row's previous C and bias values are
-                // loaded first (their latencies overlap the TMEM read), the
-                // linear part and ReLU run on registers, GELU through the
-                // staging buffer (gelu_row_smem).
+                // code stays small (the epilogue warps share the instruction
+                // cache with the producer and MMA threads): the linear part, ReLU
+                // and GELU run on the chunk's 32 registers.
                 // With beta != 0 the previous C comes in by TMA, one 32 x 32 chunk
                 // ahead, into the staging buffer the chunk's result will leave
                 // from, in the same swizzled layout (rows past M and columns past
