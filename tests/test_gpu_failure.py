@@ -51,3 +51,37 @@ def test_operand_wait_times_out_and_the_context_survives(oracle_lib, variant):
     assert np.array_equal(C2.cpu().numpy().astype(np.float64), ref)
     st, where = g.gemm_get_device_status(None)
     assert st == 0, f"{where:#x}"
+
+
+def test_host_batch_wait_times_out_and_the_pipeline_recovers(oracle_lib):
+    """The same hook through gemm_bf16_host_batch: the product runs on the
+    library's own stream, the caller's stream waits for its result copy, and
+    the status is read there.  The staging pipeline then serves a correct
+    batch."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import dense_tensor_core_bf16_gb300 as g
+
+    M, N, K = 256, 512, 1024
+    A, Bt = inputs.workload_operands(M, N, K, dist="int4", scaled=False, seed=inputs.DEFAULT_SEED + 61)
+    hA = torch.from_numpy(np.array(A, dtype=np.uint16).view(np.int16)).view(torch.bfloat16).pin_memory()
+    hBt = torch.from_numpy(np.array(Bt, dtype=np.uint16).view(np.int16)).view(torch.bfloat16).pin_memory()
+    hC = torch.zeros(M, N, dtype=torch.float32).pin_memory()
+    st, where = g.gemm_get_device_status(None)
+    assert st == 0, f"fault word not clear before the test: {where:#x}"
+
+    prob = g.gemm_host_problem_t(M=M, N=N, K=K, A=hA.data_ptr(), lda=K, layout_a=g.GEMM_ROW_MAJOR,
+                                 B=hBt.data_ptr(), ldb=K, layout_b=g.GEMM_COL_MAJOR, C=hC.data_ptr(), ldc=N)
+    opts = g.options(split_k=1, kernel_variant=2, timeout_ms=200, debug_skip_load=3)
+    stream = torch.cuda.current_stream().cuda_stream
+    assert g.gemm_bf16_host_batch([prob], g.GEMM_OUT_F32, opts, stream) == 0
+    st, where = g.gemm_get_device_status(None)
+    assert st == 7, g.gemm_status_string(st)            # GEMM_ERR_DEVICE_TIMEOUT
+    assert where & (1 | 2), f"{where:#x}"
+
+    ref, _ = oracle_lib.gemm(A, Bt, M, N, K)
+    (C2,) = g.matmul_host_batch([hA], [hBt.t()], out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert np.array_equal(C2.numpy().astype(np.float64), ref)
+    st, where = g.gemm_get_device_status(None)
+    assert st == 0, f"{where:#x}"
