@@ -4,7 +4,8 @@
 // Method (chapter 10 "Tensor Cores, shapes, and tile alignment"; lesson
 // "The Tensor Core"; post "Grid 24 is not headroom"):
 //   * two-sided tiling: A and B tiles are staged once in shared memory and
-//     reused by every MMA of the tile ("feeding it is the hard part");
+//     reused by every MMA of the tile -- keeping the Tensor Cores supplied
+//     with operands is what limits them;
 //   * the staging is a ring of STAGES slots filled by TMA and guarded by
 //     mbarriers -- at one CTA per SM, pipeline depth is the only way to hide
 //     memory latency, and it is bought with shared memory;
