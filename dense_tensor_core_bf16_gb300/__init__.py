@@ -367,7 +367,8 @@ def _plain_options(key) -> "gemm_options_t":
 def matmul(A, B, *, out_dtype=None, out=None, split_k: int = 0, non_persistent: bool = False,
            raster_group_m: int = 0, stream=None, mainloop_done_event=None, timeout_ms: int = 0,
            debug_skip_load: int = 0, kernel_variant: int = 0, no_stream_k: bool = False,
-           alpha: float = 1.0, beta: float = 0.0, bias=None, activation: str = "none"):
+           force_stream_k: bool = False, alpha: float = 1.0, beta: float = 0.0, bias=None,
+           activation: str = "none"):
     """C = A @ B through ``gemm_bf16_ex``.
 
     ``A``: (M, K) torch.bfloat16 CUDA tensor, row-major (stride (lda, 1)) or
@@ -375,6 +376,9 @@ def matmul(A, B, *, out_dtype=None, out=None, split_k: int = 0, non_persistent: 
     ``B``: (K, N) torch.bfloat16 CUDA tensor, column-major (stride (1, ldb),
     e.g. ``Bt.t()`` for a contiguous (N, K) ``Bt``) or row-major (stride (ldb, 1)).
     ``out``: optional (M, N) row-major float32 or bfloat16 tensor (stride (ldc, 1)).
+    ``no_stream_k`` / ``force_stream_k``: never / always spread a tail of
+    tiles over the clusters (the ``no_stream_k`` option 1 / -1); by default
+    the plan decides.
     ``alpha``, ``beta``, ``bias``, ``activation``: the fused epilogue
     ``out := act(alpha * (A @ B) + beta * out + bias)`` (gemm_epilogue_t);
     ``bias`` is None or a contiguous float32 CUDA tensor of N values;
@@ -410,15 +414,16 @@ def matmul(A, B, *, out_dtype=None, out=None, split_k: int = 0, non_persistent: 
     a_layout, lda, b_layout, ldb = _layouts(A, B, A.stride(), B.stride())
     ldc = so[0] if M > 1 else _round_up(N, 8)
     with_epilogue = alpha != 1.0 or beta != 0.0 or bias is not None or activation != "none"
+    sk_mode = -1 if force_stream_k else int(no_stream_k)
     if mainloop_done_event is None and not with_epilogue:
         opts = _plain_options((split_k, int(non_persistent), raster_group_m, timeout_ms, debug_skip_load,
-                               kernel_variant, int(no_stream_k)))
+                               kernel_variant, sk_mode))
     else:
         opts = gemm_options_t(split_k=split_k, non_persistent=int(non_persistent), raster_group_m=raster_group_m,
                               mainloop_done_event=(mainloop_done_event.cuda_event if mainloop_done_event is not None
                                                    else None),
                               timeout_ms=timeout_ms, debug_skip_load=debug_skip_load, kernel_variant=kernel_variant,
-                              no_stream_k=int(no_stream_k))
+                              no_stream_k=sk_mode)
     epi = None
     if with_epilogue:
         epi = gemm_epilogue_t(alpha=alpha, beta=beta, bias=bias.data_ptr() if bias is not None else None,
@@ -489,8 +494,8 @@ def matmul_host_batch(As, Bs, *, outs=None, out_dtype=None, split_k: int = 0, no
 
 
 def conv2d(x, w, *, pad=(0, 0), stride=(1, 1), dil=(1, 1), out_dtype=None, out=None, split_k: int = 0,
-           no_stream_k: bool = False, stream=None, alpha: float = 1.0, beta: float = 0.0, bias=None,
-           activation: str = "none", timeout_ms: int = 0, kernel_variant: int = 0):
+           no_stream_k: bool = False, force_stream_k: bool = False, stream=None, alpha: float = 1.0,
+           beta: float = 0.0, bias=None, activation: str = "none", timeout_ms: int = 0, kernel_variant: int = 0):
     """y = conv2d(x, w) through ``gemm_conv2d_fprop_bf16`` (an implicit GEMM).
 
     ``x``: (N, H, W, C) contiguous torch.bfloat16 CUDA tensor (NHWC).
@@ -523,8 +528,8 @@ def conv2d(x, w, *, pad=(0, 0), stride=(1, 1), dil=(1, 1), out_dtype=None, out=N
     odt = {torch.float32: GEMM_OUT_F32, torch.bfloat16: GEMM_OUT_BF16}.get(out.dtype)
     if odt is None:
         raise TypeError("out must be float32 or bfloat16")
-    opts = gemm_options_t(split_k=split_k, no_stream_k=int(no_stream_k), timeout_ms=timeout_ms,
-                          kernel_variant=kernel_variant)
+    opts = gemm_options_t(split_k=split_k, no_stream_k=-1 if force_stream_k else int(no_stream_k),
+                          timeout_ms=timeout_ms, kernel_variant=kernel_variant)
     if alpha != 1.0 or beta != 0.0 or bias is not None or activation != "none":
         if bias is not None and (bias.dtype != torch.float32 or bias.numel() != K or not bias.is_contiguous()):
             raise ValueError("bias must be a contiguous float32 tensor of K values")

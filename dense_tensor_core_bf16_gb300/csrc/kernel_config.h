@@ -91,5 +91,14 @@ static_assert(variant_info(VARIANT_2SM_256x128).smem <= SMEM_LIMIT, "fits");
 constexpr int DEFAULT_RASTER_GROUP_M = 16;
 constexpr int DEFAULT_TIMEOUT_MS = 4000;
 constexpr int MIN_K_TILES_PER_SPLIT = 4;  // automatic split-K keeps at least this many k-tiles per slice
+// Handing partial tiles between CTAs (split-K's fp32 slices and combine
+// kernel, stream-K's fix-ups) costs a roughly fixed 5-25 us on GB300, which
+// only a long enough K repays (measured over tile counts 2-256 and K 1k-16k).
+// The plan's own choice therefore splits K only for few tiles: tiles * 8 <=
+// resident clusters with K >= AUTO_SPLIT_MIN_K, or tiles * 4 <= clusters with
+// K >= LONG_K; and spreads a tail of tiles over the clusters (stream-K) only
+// behind at least two full waves, or behind one with K >= LONG_K.
+constexpr long long AUTO_SPLIT_MIN_K = 2048;
+constexpr long long LONG_K = 6144;
 
 }  // namespace gemm

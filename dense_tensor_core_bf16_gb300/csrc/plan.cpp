@@ -80,17 +80,17 @@ gemm_status_t occupancy(const gemm_kernel_desc_t &k, const gemm_device_desc_t &d
     return b > 0 ? GEMM_OK : GEMM_ERR_INVALID_VALUE;
 }
 
-int choose_split(int64_t tiles, int k_tiles, int capacity, int requested) {
+int choose_split(int64_t tiles, int k_tiles, int capacity, int requested, int64_t K) {
     if (k_tiles <= 0) return 1;
     int s;
     if (requested > 0) {
         s = requested;
     } else {
-        // Automatic: only when the tiles alone fill under half the resident
-        // slots; then give each slot a slice of K, keeping slices at least
-        // MIN_K_TILES_PER_SPLIT k-tiles long.
+        // Automatic: only for few tiles and a long enough K (see
+        // AUTO_SPLIT_MIN_K); then give each slot a slice of K, keeping slices
+        // at least MIN_K_TILES_PER_SPLIT k-tiles long.
         s = 1;
-        if (tiles * 2 <= capacity) {
+        if ((tiles * 8 <= capacity && K >= AUTO_SPLIT_MIN_K) || (tiles * 4 <= capacity && K >= LONG_K)) {
             int64_t by_slots = capacity / tiles;
             int64_t by_k = k_tiles / MIN_K_TILES_PER_SPLIT;
             int64_t c = by_slots < by_k ? by_slots : by_k;
@@ -171,15 +171,19 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_layout_t la, gemm_
     plan->k_tiles = (int)cdiv(K, vi.tile_k);
 
     // Stream-K tail: only with the plan's own choice of split, on a persistent
-    // grid (every cluster resident, as the hand-off between clusters needs).
+    // grid (every cluster resident, as the hand-off between clusters needs),
+    // when the tiles do not divide the clusters evenly -- and then when it
+    // pays (two full waves ahead of it, or one with a long K; see LONG_K), or
+    // always when asked (no_stream_k < 0).
     int64_t sk_tiles = 0;
-    if (allow_stream_k && persistent && o.split_k == 0 && o.no_stream_k == 0 && plan->k_tiles >= 2 && T > 0 &&
-        T * 2 > clusters && T % clusters != 0) {
-        sk_tiles = T >= 2 * clusters ? clusters + T % clusters : T;
+    if (allow_stream_k && persistent && o.split_k == 0 && o.no_stream_k <= 0 && plan->k_tiles >= 2 && T > 0 &&
+        T % clusters != 0) {
+        const bool pays = T >= 2 * clusters || (T >= clusters && K >= LONG_K);
+        if (o.no_stream_k < 0 || pays) sk_tiles = T >= 2 * clusters ? clusters + T % clusters : T;
     }
     plan->stream_k_tiles = sk_tiles;
     plan->dp_tiles = T - sk_tiles;
-    plan->split_k = (T > 0 && sk_tiles == 0) ? choose_split(T, plan->k_tiles, (int)clusters, o.split_k) : 1;
+    plan->split_k = (T > 0 && sk_tiles == 0) ? choose_split(T, plan->k_tiles, (int)clusters, o.split_k, K) : 1;
     plan->k_tiles_per_split = plan->k_tiles > 0 ? (int)cdiv(plan->k_tiles, plan->split_k) : 0;
     plan->grid = T * plan->split_k * cs;
     plan->launch_ctas = persistent ? (plan->grid < resident ? plan->grid : resident) : plan->grid;

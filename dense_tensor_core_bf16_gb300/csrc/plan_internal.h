@@ -13,7 +13,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_layout_t la, gemm_
                         const gemm_device_desc_t &dev, const gemm_kernel_desc_t &kern, gemm_plan_t *plan);
 int resolve_variant(int requested);
 int choose_variant(int64_t M, int64_t N, int64_t K, int requested, int split_k, const gemm_device_desc_t &dev);
-int choose_split(int64_t tiles, int k_tiles, int capacity, int requested);
+int choose_split(int64_t tiles, int k_tiles, int capacity, int requested, int64_t K);
 gemm_status_t conv_check(const gemm_conv2d_desc_t *d, int64_t *P, int64_t *Q);
 // Frees the host-batch staging slots of every device (host_pipeline.cpp).
 void release_host_staging();

@@ -205,7 +205,10 @@ typedef struct {
                                     CTA 0) unissued, so its consumer's wait runs out and the call
                                     ends with GEMM_ERR_DEVICE_TIMEOUT on the device */
     int kernel_variant;          /* gemm_kernel_variant_t; 0 = the plan chooses */
-    int no_stream_k;             /* 1: never spread a tail of tiles over the clusters (stream-K) */
+    int no_stream_k;             /* 0: the plan decides on a stream-K tail (see gemm_plan_for_device);
+                                    1: never spread tiles over the clusters (stream-K);
+                                   -1: always, whenever the tile count is not a multiple of the
+                                       resident clusters (all tiles below two waves) */
     const gemm_epilogue_t *epilogue;   /* NULL: C = A.B; else the fused epilogue above (read
                                           during the call, not kept) */
 } gemm_options_t;
@@ -230,15 +233,20 @@ gemm_status_t gemm_occupancy(const gemm_kernel_desc_t *kern, const gemm_device_d
  * describes the footprint of the variant opts selects (GEMM_KERNEL_AUTO
  * resolves to the default variant).
  *
- * Work decomposition, in order:
+ * Work decomposition, in order (T tiles, C resident clusters):
  *   - split_k > 1: split-K as asked (clamped to the k-tile count);
- *   - split_k = 0 and the tiles fill at most half of the resident clusters:
- *     split-K chosen by the plan;
- *   - split_k = 0, a persistent launch, stream-K not disabled, and the tile
- *     count T not a multiple of the resident clusters C: a stream-K tail --
- *     the last C + (T mod C) tiles (all T when T < 2C) have their k-iterations
- *     dealt out evenly over the C clusters, the rest are computed whole;
+ *   - split_k = 0, a persistent launch, no_stream_k <= 0, T not a multiple of
+ *     C, and either no_stream_k < 0 or T >= 2C or (T >= C and K >= 6144): a
+ *     stream-K tail -- the last C + (T mod C) tiles (all T when T < 2C) have
+ *     their k-iterations dealt out evenly over the C clusters, the rest are
+ *     computed whole;
+ *   - split_k = 0, and T * 8 <= C with K >= 2048 or T * 4 <= C with
+ *     K >= 6144: split-K chosen by the plan (C / T slices, each at least 4
+ *     k-tiles long);
  *   - otherwise one cluster per tile.
+ * Handing partial tiles between CTAs costs a roughly fixed few to 25 us on
+ * GB300 (fp32 partials through L2 and a fix-up or a combine kernel), so the
+ * plan spreads or splits the work only where the longer K repays it.
  */
 gemm_status_t gemm_plan_for_device(int64_t M, int64_t N, int64_t K,
                                    gemm_layout_t layout_a, gemm_layout_t layout_b,

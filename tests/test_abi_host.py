@@ -212,34 +212,59 @@ def test_plan_auto_variant():
         assert st == 0 and p.kernel_variant == 2, shape
 
 
+def _want_stream_k(T, C, K, KB, force=False):
+    """The decomposition rule of gemm_plan_for_device for the plan's own split
+    on a persistent grid: a tail of C + (T mod C) tiles (all T below 2C) when
+    T mod C != 0 and it pays -- T >= 2C, or T >= C with K >= 6144 -- or always
+    when forced."""
+    if KB < 2 or T % C == 0:
+        return 0
+    if force or T >= 2 * C or (T >= C and K >= 6144):
+        return C + T % C if T >= 2 * C else T
+    return 0
+
+
 @pytest.mark.parametrize("variant", [1, 2])
-@pytest.mark.parametrize("shape", WORKLOADS + [(4096, 4096, 8192), (2560, 4096, 4096), (1000, 9000, 3000)])
+@pytest.mark.parametrize("shape", WORKLOADS + [(4096, 4096, 8192), (2560, 4096, 4096), (1000, 9000, 3000),
+                                                (2560, 2560, 8192), (3072, 3072, 3072), (1792, 1792, 1792)])
 def test_plan_stream_k_tail(shape, variant):
-    """With the plan's own split on a persistent grid: T tiles on C clusters;
-    a tail of C + (T mod C) tiles (all T if T < 2C) is spread over the
-    clusters when T mod C != 0 and T > C/2; the largest per-cluster share is
-    ceil(dp/C) whole tiles plus ceil(sk k-iterations / C)."""
+    """T tiles on C clusters; the largest per-cluster share of a stream-K plan
+    is ceil(dp/C) whole tiles plus ceil(sk k-iterations / C)."""
     M, N, K = shape
     tm, tn, cs = TILES[variant]
-    p = _plan(M, N, K, split=0, variant=variant)
     C = 152 // cs
     T = pf.grid(M, N, tm, tn)
     KB = math.ceil(K / TILE_K[variant])
-    want_sk = 0
-    if KB >= 2 and 2 * T > C and T % C:
-        want_sk = C + T % C if T >= 2 * C else T
-    assert p.stream_k_tiles == want_sk and p.dp_tiles == T - want_sk
-    if want_sk:
-        assert p.split_k == 1 and p.launch_ctas == C * cs
-        worst = math.ceil((T - want_sk) / C) * KB + math.ceil(want_sk * KB / C)
-        assert p.eta_stream_k == pytest.approx(T * KB / C / worst, rel=1e-12)
-        assert p.workspace_bytes == C * tm * tn * 4
-    else:
-        assert p.eta_stream_k == 0
+    for force in (False, True):
+        p = _plan(M, N, K, split=0, variant=variant, no_sk=-1 if force else 0)
+        want_sk = _want_stream_k(T, C, K, KB, force)
+        assert p.stream_k_tiles == want_sk and p.dp_tiles == T - want_sk, (force, T, C)
+        if want_sk:
+            assert p.split_k == 1 and p.launch_ctas == C * cs
+            worst = math.ceil((T - want_sk) / C) * KB + math.ceil(want_sk * KB / C)
+            assert p.eta_stream_k == pytest.approx(T * KB / C / worst, rel=1e-12)
+            assert p.workspace_bytes == C * tm * tn * 4
+        else:
+            assert p.eta_stream_k == 0
     # off on request, and never on a one-CTA-per-tile grid or with an explicit split
     assert _plan(M, N, K, split=0, variant=variant, no_sk=1).stream_k_tiles == 0
-    assert _plan(M, N, K, split=0, variant=variant, persistent=0).stream_k_tiles == 0
-    assert _plan(M, N, K, split=1, variant=variant).stream_k_tiles == 0
+    assert _plan(M, N, K, split=0, variant=variant, persistent=0, no_sk=-1).stream_k_tiles == 0
+    assert _plan(M, N, K, split=1, variant=variant, no_sk=-1).stream_k_tiles == 0
+
+
+@pytest.mark.parametrize("shape,variant,want", [
+    ((1536, 1536, 1536), 2, 1),      # 36 pair tiles, short K: one tile per cluster
+    ((1024, 1024, 4096), 2, 1),      # 16 tiles, K below 6144: no split
+    ((1024, 1024, 8192), 2, 4),      # 16 tiles (16 * 4 <= 76), long K: 76 / 16 = 4 slices
+    ((512, 512, 2048), 2, 4),        # 4 tiles (4 * 8 <= 76), K >= 2048: 16 k-tiles, 4 per slice
+    ((512, 512, 1024), 2, 1),        # K below 2048
+    ((2048, 1024, 4096), 2, 1),      # 32 tiles: 32 * 4 > 76
+    ((128, 256, 65536), 1, 152),     # the split-K workload: one tile, 152 slices
+])
+def test_plan_automatic_split_rule(shape, variant, want):
+    M, N, K = shape
+    p = _plan(M, N, K, split=0, variant=variant)
+    assert p.split_k == want and p.stream_k_tiles == 0
 
 
 def test_plan_stream_k_hand_values():

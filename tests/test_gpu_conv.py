@@ -98,30 +98,33 @@ def test_conv_small_integers_exact(oracle_lib, case):
 
 @pytest.mark.parametrize("split", [0, 1, 4])
 def test_conv_split_k(oracle_lib, split):
-    """0: the plan's choice (few tiles: it splits K), 1: no split, 4: four slices."""
+    """0: the plan's choice (4 tiles and a GEMM K of 2304: it splits K),
+    1: no split, 4: four slices."""
     import dense_tensor_core_bf16_gb300 as g
-    c = dict(N=4, H=28, W=28, C=128, K=256, R=3, S=3, pad=(1, 1), stride=(1, 1), dil=(1, 1))
+    c = dict(N=1, H=28, W=28, C=256, K=256, R=3, S=3, pad=(1, 1), stride=(1, 1), dil=(1, 1))
     x, w = conv_operands(*(c[k] for k in "N H W C K R S".split()), "int4", SEED + 2)
     y = run(x, w, "f32", split_k=split, **_conv_kw(c))
     check(oracle_lib, x, w, y, "f32", exact=True, **_conv_kw(c))
     if split == 0:
-        d = g.gemm_conv2d_desc_t(N=4, H=28, W=28, C=128, K=256, R=3, S=3, pad_h=1, pad_w=1, stride_h=1, stride_w=1,
+        d = g.gemm_conv2d_desc_t(N=1, H=28, W=28, C=256, K=256, R=3, S=3, pad_h=1, pad_w=1, stride_h=1, stride_w=1,
                                  dil_h=1, dil_w=1)
         st, plan = g.gemm_conv2d_plan(d, g.GEMM_OUT_F32)
         assert st == 0 and plan.split_k > 1
 
 
 def test_conv_stream_k(oracle_lib):
+    """49 pair tiles on 76 clusters, asked for a stream-K tail (below the plan's
+    own threshold)."""
     import dense_tensor_core_bf16_gb300 as g
     c = dict(N=4, H=56, W=56, C=64, K=256, R=3, S=3, pad=(1, 1), stride=(1, 1), dil=(1, 1))
     d = g.gemm_conv2d_desc_t(N=4, H=56, W=56, C=64, K=256, R=3, S=3, pad_h=1, pad_w=1, stride_h=1, stride_w=1,
                              dil_h=1, dil_w=1)
-    st, plan = g.gemm_conv2d_plan(d, g.GEMM_OUT_BF16)
+    st, plan = g.gemm_conv2d_plan(d, g.GEMM_OUT_BF16, g.options(no_stream_k=-1))
     assert st == 0 and plan.stream_k_tiles > 0
     x, w = conv_operands(*(c[k] for k in "N H W C K R S".split()), "normal", SEED + 3)
-    y = run(x, w, "bf16", **_conv_kw(c))
+    y = run(x, w, "bf16", force_stream_k=True, **_conv_kw(c))
     check(oracle_lib, x, w, y, "bf16", **_conv_kw(c))
-    y2 = run(x, w, "bf16", **_conv_kw(c))
+    y2 = run(x, w, "bf16", force_stream_k=True, **_conv_kw(c))
     assert np.array_equal(y, y2), "stream-K result differs run to run"
 
 

@@ -145,11 +145,12 @@ def test_epilogue_in_the_split_k_combine(oracle_lib, split, activation):
 def test_epilogue_on_stream_k_tiles(oracle_lib, variant, shape):
     import dense_tensor_core_bf16_gb300 as g
     M, N, K = shape
-    st, plan = g.gemm_plan(M, N, K, opts=g.options(kernel_variant=variant))
+    st, plan = g.gemm_plan(M, N, K, opts=g.options(kernel_variant=variant, no_stream_k=-1))
     assert st == 0 and plan.stream_k_tiles > 0
     A, Bt = operands(M, N, K, "int4", False, SEED + 6)
     C0, bias = c_old_and_bias(M, N, SEED + 7, dist="int4")
-    C = run(A, Bt, "f32", C0, bias, kernel_variant=variant, alpha=1.0, beta=1.0, activation="relu")
+    C = run(A, Bt, "f32", C0, bias, kernel_variant=variant, force_stream_k=True, alpha=1.0, beta=1.0,
+            activation="relu")
     check(oracle_lib, A, Bt, C, "f32", C0, bias, 1.0, 1.0, "relu", exact=True)
 
 

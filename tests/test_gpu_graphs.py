@@ -42,10 +42,10 @@ def _operands(M, N, K, seed):
 
 CASES = [
     # (M, N, K, options, what the plan must use)
-    (2048, 2048, 2048, {}, "stream_k"),                       # 64 pair tiles < 2 x 76 clusters: all stream-K
-    (4096, 4096, 1024, {}, "stream_k"),                       # a stream-K tail behind whole tiles
-    (128, 256, 16384, {"split_k": 16}, "split_k"),            # partial slices and the combine kernel
-    (2048, 2048, 1024, {"beta": 1.0, "activation": "gelu"}, "stream_k"),  # the fused epilogue reads C
+    (2048, 2048, 2048, {"force_stream_k": True}, "stream_k"),   # 64 pair tiles < 76 clusters: all spread
+    (4096, 4096, 1024, {}, "stream_k"),                         # the plan's own tail behind two waves
+    (128, 256, 16384, {"split_k": 16}, "split_k"),              # partial slices and the combine kernel
+    (2048, 2048, 1024, {"force_stream_k": True, "beta": 1.0, "activation": "gelu"}, "stream_k"),  # reads C
 ]
 
 
@@ -55,7 +55,7 @@ def test_graph_replays_follow_the_operands(case):
     M, N, K, opts, uses = case
     A, Bt = _operands(M, N, K, SEED)
     st, plan = g.gemm_plan(M, N, K, g.GEMM_ROW_MAJOR, g.GEMM_COL_MAJOR, g.GEMM_OUT_F32,
-                           g.options(split_k=opts.get("split_k", 0)))
+                           g.options(split_k=opts.get("split_k", 0), no_stream_k=-1 if opts.get("force_stream_k") else 0))
     assert st == 0
     if uses == "stream_k":
         assert plan.stream_k_tiles > 0, "the case must exercise the stream-K hand-off"

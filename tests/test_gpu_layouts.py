@@ -145,10 +145,10 @@ def test_layouts_stream_k(oracle_lib, layout, variant, shape):
     M, N, K = shape
     la = g.GEMM_COL_MAJOR if layout[0] else g.GEMM_ROW_MAJOR
     lb = g.GEMM_ROW_MAJOR if layout[1] else g.GEMM_COL_MAJOR
-    st, plan = g.gemm_plan(M, N, K, la, lb, opts=g.options(kernel_variant=variant))
+    st, plan = g.gemm_plan(M, N, K, la, lb, opts=g.options(kernel_variant=variant, no_stream_k=-1))
     assert st == 0 and plan.stream_k_tiles > 0
     Ai, Bti = operands(M, N, K, "int4", False, SEED + 4)
-    C = run_layout(Ai, Bti, *layout, torch.float32, kernel_variant=variant)
+    C = run_layout(Ai, Bti, *layout, torch.float32, kernel_variant=variant, force_stream_k=True)
     check(oracle_lib, Ai, Bti, C, torch.float32, exact=True)
 
 

@@ -187,16 +187,18 @@ SK_CASES = [(2, (1792, 1536, 2048)), (2, (3328, 3072, 512)), (1, (1280, 2048, 20
 def test_stream_k_tail(oracle_lib, variant, shape):
     g = _lib()
     M, N, K = shape
-    st, plan = g.gemm_plan(M, N, K, opts=g.options(kernel_variant=variant))
+    # asked for: these shapes are below the plan's own threshold for a tail
+    st, plan = g.gemm_plan(M, N, K, opts=g.options(kernel_variant=variant, no_stream_k=-1))
     assert st == 0 and plan.stream_k_tiles > 0, "shape chosen to exercise the stream-K tail"
     A, Bt = operands(M, N, K, "normal", True, SEED + 20)
-    C1 = full_check(oracle_lib, A, Bt, M, N, K, torch.float32, kernel_variant=variant)
-    C2 = run_gpu(A, Bt, M, N, K, torch.float32, kernel_variant=variant)
+    C1 = full_check(oracle_lib, A, Bt, M, N, K, torch.float32, kernel_variant=variant, force_stream_k=True)
+    C2 = run_gpu(A, Bt, M, N, K, torch.float32, kernel_variant=variant, force_stream_k=True)
     assert np.array_equal(C1, C2), "stream-K result differs run to run"
-    full_check(oracle_lib, A, Bt, M, N, K, torch.bfloat16, kernel_variant=variant)
+    full_check(oracle_lib, A, Bt, M, N, K, torch.bfloat16, kernel_variant=variant, force_stream_k=True)
     # exact on small integers, like the whole-tile path
     Ai, Bti = operands(M, N, K, "int4", False, SEED + 21)
-    Ce = full_check(oracle_lib, Ai, Bti, M, N, K, torch.float32, exact=True, kernel_variant=variant)
+    Ce = full_check(oracle_lib, Ai, Bti, M, N, K, torch.float32, exact=True, kernel_variant=variant,
+                    force_stream_k=True)
     Cd = run_gpu(Ai, Bti, M, N, K, torch.float32, kernel_variant=variant, no_stream_k=True)
     assert np.array_equal(Ce, Cd)
 
