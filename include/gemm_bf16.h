@@ -244,6 +244,8 @@ gemm_status_t gemm_occupancy(const gemm_kernel_desc_t *kern, const gemm_device_d
  *     K >= 6144: split-K chosen by the plan (C / T slices, each at least 4
  *     k-tiles long);
  *   - otherwise one cluster per tile.
+ * With the plan's own variant, a small GEMM (256 x 128 pair tiles filling at
+ * most half the resident pairs, K < 2048) runs on the 256 x 128 pair kernel.
  * Handing partial tiles between CTAs costs a roughly fixed few to 25 us on
  * GB300 (fp32 partials through L2 and a fix-up or a combine kernel), so the
  * plan spreads or splits the work only where the longer K repays it.

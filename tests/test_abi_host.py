@@ -207,9 +207,15 @@ def test_plan_auto_variant():
     assert st == 1     # a footprint that does not match the variant
     st, p = g.gemm_plan_for_device(128, 256, 65536, 0, 1, 0, None, dev(), kern(1))
     assert st == 0 and p.kernel_variant == 1 and p.split_k == 152
-    for shape in [(16384, 8192, 8192), (4097, 4096, 4096), (3968, 4096, 4096), (256, 256, 256)]:
+    for shape in [(16384, 8192, 8192), (4097, 4096, 4096), (3968, 4096, 4096), (2048, 2048, 1024),
+                  (1536, 1536, 1536), (512, 512, 4096)]:
         st, p = g.gemm_plan_for_device(*shape, 0, 1, 1, None, dev(), kern(2))
         assert st == 0 and p.kernel_variant == 2, shape
+    # small GEMMs (256 x 128 pair tiles filling at most half the pairs, K < 2048)
+    # go to the 256 x 128 pair kernel
+    for shape in [(256, 256, 256), (512, 512, 512), (1024, 1024, 1024), (1024, 1024, 2047)]:
+        st, p = g.gemm_plan_for_device(*shape, 0, 1, 1, None, dev(), kern(3))
+        assert st == 0 and p.kernel_variant == 3, shape
 
 
 def _want_stream_k(T, C, K, KB, force=False):
