@@ -97,8 +97,11 @@ constexpr int MIN_K_TILES_PER_SPLIT = 4;  // automatic split-K keeps at least th
 // The plan's own choice therefore splits K only for few tiles: tiles * 8 <=
 // resident clusters with K >= AUTO_SPLIT_MIN_K, or tiles * 4 <= clusters with
 // K >= LONG_K; and spreads a tail of tiles over the clusters (stream-K) only
-// behind at least two full waves, or behind one with K >= LONG_K.
+// with at least one full wave, when the partly filled last wave would leave
+// at least STREAM_K_MIN_WASTE 128-wide k-tiles of a 128 x 256 block per SM
+// idle in the average cluster.
 constexpr long long AUTO_SPLIT_MIN_K = 2048;
 constexpr long long LONG_K = 6144;
+constexpr double STREAM_K_MIN_WASTE = 12.0;
 
 }  // namespace gemm

@@ -178,12 +178,16 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_layout_t la, gemm_
     // Stream-K tail: only with the plan's own choice of split, on a persistent
     // grid (every cluster resident, as the hand-off between clusters needs),
     // when the tiles do not divide the clusters evenly -- and then when it
-    // pays (two full waves ahead of it, or one with a long K; see LONG_K), or
-    // always when asked (no_stream_k < 0).
+    // pays: at least one full wave, and a last wave whose idle share, in
+    // 128-wide k-tiles of a 128 x 256 block per SM, reaches
+    // STREAM_K_MIN_WASTE -- or always when asked (no_stream_k < 0).
     int64_t sk_tiles = 0;
     if (allow_stream_k && persistent && o.split_k == 0 && o.no_stream_k <= 0 && plan->k_tiles >= 2 && T > 0 &&
         T % clusters != 0) {
-        const bool pays = T >= 2 * clusters || (T >= clusters && K >= LONG_K);
+        const double idle_k_tiles =
+            (double)(cdiv(T, clusters) * clusters - T) / (double)clusters * plan->k_tiles;
+        const double waste = idle_k_tiles * (vi.tile_k / 128.0) * ((double)vi.tile_m * vi.bn / cs / (128.0 * 256.0));
+        const bool pays = T >= clusters && waste >= STREAM_K_MIN_WASTE;
         if (o.no_stream_k < 0 || pays) sk_tiles = T >= 2 * clusters ? clusters + T % clusters : T;
     }
     plan->stream_k_tiles = sk_tiles;

@@ -236,10 +236,11 @@ gemm_status_t gemm_occupancy(const gemm_kernel_desc_t *kern, const gemm_device_d
  * Work decomposition, in order (T tiles, C resident clusters):
  *   - split_k > 1: split-K as asked (clamped to the k-tile count);
  *   - split_k = 0, a persistent launch, no_stream_k <= 0, T not a multiple of
- *     C, and either no_stream_k < 0 or T >= 2C or (T >= C and K >= 6144): a
- *     stream-K tail -- the last C + (T mod C) tiles (all T when T < 2C) have
- *     their k-iterations dealt out evenly over the C clusters, the rest are
- *     computed whole;
+ *     C, and either no_stream_k < 0 or (T >= C and the partly filled last
+ *     wave leaves, per cluster on average, at least 12 k-tiles of 128 of a
+ *     128 x 256 block per SM idle): a stream-K tail -- the last C + (T mod C)
+ *     tiles (all T when T < 2C) have their k-iterations dealt out evenly over
+ *     the C clusters, the rest are computed whole;
  *   - split_k = 0, and T * 8 <= C with K >= 2048 or T * 4 <= C with
  *     K >= 6144: split-K chosen by the plan (C / T slices, each at least 4
  *     k-tiles long);

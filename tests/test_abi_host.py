@@ -218,14 +218,18 @@ def test_plan_auto_variant():
         assert st == 0 and p.kernel_variant == 3, shape
 
 
-def _want_stream_k(T, C, K, KB, force=False):
+def _want_stream_k(T, C, K, KB, force=False, variant=2):
     """The decomposition rule of gemm_plan_for_device for the plan's own split
     on a persistent grid: a tail of C + (T mod C) tiles (all T below 2C) when
-    T mod C != 0 and it pays -- T >= 2C, or T >= C with K >= 6144 -- or always
-    when forced."""
+    T mod C != 0 and it pays -- T >= C and the last wave's idle share,
+    (ceil(T/C) C - T) / C k-tiles scaled to 128-wide k-tiles of a 128 x 256
+    block per SM, at least 12 -- or always when forced."""
     if KB < 2 or T % C == 0:
         return 0
-    if force or T >= 2 * C or (T >= C and K >= 6144):
+    tm, tn, cs = TILES[variant]
+    idle = (math.ceil(T / C) * C - T) / C * KB
+    waste = idle * (TILE_K[variant] / 128) * (tm * tn / cs / (128 * 256))
+    if force or (T >= C and waste >= 12.0):
         return C + T % C if T >= 2 * C else T
     return 0
 
@@ -243,7 +247,7 @@ def test_plan_stream_k_tail(shape, variant):
     KB = math.ceil(K / TILE_K[variant])
     for force in (False, True):
         p = _plan(M, N, K, split=0, variant=variant, no_sk=-1 if force else 0)
-        want_sk = _want_stream_k(T, C, K, KB, force)
+        want_sk = _want_stream_k(T, C, K, KB, force, variant)
         assert p.stream_k_tiles == want_sk and p.dp_tiles == T - want_sk, (force, T, C)
         if want_sk:
             assert p.split_k == 1 and p.launch_ctas == C * cs

@@ -43,7 +43,7 @@ def _operands(M, N, K, seed):
 CASES = [
     # (M, N, K, options, what the plan must use)
     (2048, 2048, 2048, {"force_stream_k": True}, "stream_k"),   # 64 pair tiles < 76 clusters: all spread
-    (4096, 4096, 1024, {}, "stream_k"),                         # the plan's own tail behind two waves
+    (4096, 4096, 1024, {"force_stream_k": True}, "stream_k"),   # a tail of 104 tiles behind 152 whole ones
     (128, 256, 16384, {"split_k": 16}, "split_k"),              # partial slices and the combine kernel
     (2048, 2048, 1024, {"force_stream_k": True, "beta": 1.0, "activation": "gelu"}, "stream_k"),  # reads C
 ]

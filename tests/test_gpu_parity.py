@@ -400,10 +400,12 @@ def test_large_16384x8192x8192_persistent_and_one_cta_per_tile(oracle_lib):
         del C3
         sampled_check(oracle_lib, A, Bt, M, N, K, from_dev_bf16(C2), "bf16", n_random=2000, seed=variant)
         del C2
-        # the default persistent launch adds a stream-K tail (tiles mod clusters != 0)
-        st, plan = g.gemm_plan(M, N, K, opts=g.options(kernel_variant=variant))
+        # a persistent launch with a stream-K tail (tiles mod clusters != 0),
+        # asked for: the last wave is nearly full, so the plan's own choice
+        # leaves the tiles whole
+        st, plan = g.gemm_plan(M, N, K, opts=g.options(kernel_variant=variant, no_stream_k=-1))
         assert st == 0 and plan.stream_k_tiles > 0
-        C1 = g.matmul(dA, dBt.t(), out_dtype=torch.bfloat16, kernel_variant=variant)
+        C1 = g.matmul(dA, dBt.t(), out_dtype=torch.bfloat16, kernel_variant=variant, force_stream_k=True)
         sampled_check(oracle_lib, A, Bt, M, N, K, from_dev_bf16(C1), "bf16", n_random=3000, seed=10 + variant)
         # and every row of the last tile row, where the tail tiles lie
         rows = np.repeat(np.arange(M - plan.tile_m, M, 7), 16)
