@@ -59,6 +59,7 @@ struct KernelParams {
     void *out;                   // C
     long long ld_out;            // leading dimension of C, elements
     int out_bf16;                // 1: bf16 stores, 0: fp32 stores
+    int n_tma;                   // columns of C stored by TMA: N rounded down to whole 16-byte pieces
     unsigned long long timeout_ns;
     int skip_load;               // test hook (0 = off)
     int a_mn, b_mn;              // 1: the operand is MN-major in memory (A column-major, B row-major)
@@ -330,7 +331,8 @@ __device__ __forceinline__ bool wait_flag(const unsigned int *flag, unsigned int
 template <int CG, int BN, int TK>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                     const __grid_constant__ CUtensorMap tmap_c, const KernelParams p) {
+                     const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_out,
+                     const KernelParams p) {
     constexpr VariantInfo V = make_variant(CG, BN, TK);
     // Operand boxes.  K-major (A row-major, B column-major): TK/64 boxes of
     // rows x 64 K, each rows x 128 bytes.  MN-major (A column-major, B
@@ -399,6 +401,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::prefetch_tensormap(&tmap_a);
         ptx::prefetch_tensormap(&tmap_b);
         ptx::prefetch_tensormap(&tmap_c);
+        ptx::prefetch_tensormap(&tmap_out);
     }
     if (warp == 1) {
         if constexpr (PAIR) {
@@ -742,8 +745,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 ptx::fence_proxy_async_shared();
                 __syncwarp();
+                // Every chunk commits a bulk group, empty when the chunk lies
+                // wholly past n_tma, so that buffers and groups keep in step.
                 if (lane == 0) {
-                    ptx::tma_store_2d(&tmap_c, buf, col0, warp_row0);
+                    if (col0 < p.n_tma) ptx::tma_store_2d(&tmap_out, buf, col0, warp_row0);
                     ptx::bulk_commit_group();
                 }
                 ++stores_issued;
@@ -898,6 +903,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             }
             if (!c_ok) break;
+            if (!to_slot && warp_row0 < p.M && col_base + n_chunks * 32 > p.n_tma) {
+                // C's columns from n_tma to N, when N is not a whole number of
+                // 16-byte pieces: a TMA store clipped at N would still write
+                // the last piece whole, past N.  They lie in the last chunk,
+                // still in its staging buffer; each lane stores its own row's.
+                const int col0 = col_base + (n_chunks - 1) * 32;
+                const uint32_t sbuf = epi_buf0 + ((stores_issued - 1u) & 1u) * EPI_BUF_BYTES;
+                const int row = warp_row0 + lane;
+                if (row < p.M) {
+                    const long long at = static_cast<long long>(row) * p.ld_out + col0;
+                    const int j1 = min(p.N - col0, 32);
+                    for (int j = max(p.n_tma - col0, 0); j < j1; ++j) {
+                        const uint32_t uj = static_cast<uint32_t>(j);
+                        if (p.out_bf16) {
+                            const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
+                            static_cast<uint16_t *>(p.out)[at + j] = ptx::ld_shared_b16(
+                                sbuf + static_cast<uint32_t>(lane) * 64u + (((uj >> 3) ^ sw) << 4) + (uj & 7u) * 2u);
+                        } else {
+                            const uint32_t sw = static_cast<uint32_t>(lane) & 7u;
+                            static_cast<uint32_t *>(p.out)[at + j] = ptx::ld_shared_b32(
+                                sbuf + static_cast<uint32_t>(lane) * 128u + (((uj >> 2) ^ sw) << 4) + (uj & 3u) * 4u);
+                        }
+                    }
+                }
+            }
             if (w.kind == KIND_OWNER && lane == 0) {
                 // The owner clears the flags it consumed, so that every launch
                 // starts from cleared flags -- also one replayed from a captured
@@ -1111,7 +1141,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
-using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, KernelParams);
+using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, KernelParams);
 
 KernelFn kernel_fn(int variant) {
     switch (variant) {
@@ -1497,6 +1527,15 @@ gemm_status_t launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_
     }
     st = encode_output(&tmap_c, C, N, M, ldc, out_dtype == GEMM_OUT_BF16);
     if (st != GEMM_OK) return st;
+    // Stores by TMA stop at the last whole 16-byte piece of a row (the rest
+    // of the row inside N is stored lane by lane); loads of the previous C
+    // take the exact extent.
+    const int64_t n_tma = N / (out_dtype == GEMM_OUT_BF16 ? 8 : 4) * (out_dtype == GEMM_OUT_BF16 ? 8 : 4);
+    CUtensorMap tmap_out = tmap_c;
+    if (n_tma > 0 && n_tma != N) {
+        st = encode_output(&tmap_out, C, n_tma, M, ldc, out_dtype == GEMM_OUT_BF16);
+        if (st != GEMM_OK) return st;
+    }
 
     KernelParams p{};
     p.M = static_cast<int>(M);
@@ -1511,9 +1550,17 @@ gemm_status_t launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_
     p.out = C;
     p.ld_out = ldc;
     p.out_bf16 = out_dtype == GEMM_OUT_BF16 ? 1 : 0;
+    p.n_tma = static_cast<int>(n_tma);
     p.partials = partials;
-    const int timeout_ms = o.timeout_ms > 0 ? o.timeout_ms : DEFAULT_TIMEOUT_MS;
-    p.timeout_ns = static_cast<unsigned long long>(timeout_ms) * 1000000ull;
+    if (o.timeout_ms > 0) {
+        p.timeout_ns = static_cast<unsigned long long>(o.timeout_ms) * 1000000ull;
+    } else {
+        // k-tiles one wait may span: a work unit, plus a stream-K range
+        const long long span = static_cast<long long>(plan.k_tiles_per_split) +
+                               (plan.stream_k_tiles > 0 ? (plan.stream_k_tiles * plan.k_tiles + clusters - 1) / clusters : 0);
+        p.timeout_ns = static_cast<unsigned long long>(DEFAULT_TIMEOUT_MS) * 1000000ull +
+                       static_cast<unsigned long long>(span) * DEFAULT_TIMEOUT_US_PER_K_TILE * 1000ull;
+    }
     p.skip_load = o.debug_skip_load;
     p.a_mn = a_mn ? 1 : 0;
     p.b_mn = b_mn ? 1 : 0;
@@ -1561,7 +1608,7 @@ gemm_status_t launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_
     attrs[1] = cluster_attr(vi.cta_group);
     cfg.attrs = attrs;
     cfg.numAttrs = vi.cta_group > 1 ? 2 : 1;
-    if (cudaLaunchKernelEx(&cfg, kernel_fn(variant), tmap_a, tmap_b, tmap_c, p) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, kernel_fn(variant), tmap_a, tmap_b, tmap_c, tmap_out, p) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
     }

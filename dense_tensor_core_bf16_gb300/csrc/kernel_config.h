@@ -90,6 +90,11 @@ static_assert(variant_info(VARIANT_2SM_256x128).smem <= SMEM_LIMIT, "fits");
 
 constexpr int DEFAULT_RASTER_GROUP_M = 16;
 constexpr int DEFAULT_TIMEOUT_MS = 4000;
+// The default limit also grows with the longest stretch of main loop a single
+// wait can span (the epilogue's wait for a whole unit's accumulator, a
+// stream-K owner's wait for its contributors): this much per k-tile, about
+// 16 times what a 128-wide k-tile of the pair kernel takes at full clock.
+constexpr int DEFAULT_TIMEOUT_US_PER_K_TILE = 8;
 constexpr int MIN_K_TILES_PER_SPLIT = 4;  // automatic split-K keeps at least this many k-tiles per slice
 // Handing partial tiles between CTAs (split-K's fp32 slices and combine
 // kernel, stream-K's fix-ups) costs a roughly fixed 5-25 us on GB300, which

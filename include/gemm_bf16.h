@@ -199,7 +199,8 @@ typedef struct {
     int raster_group_m;          /* m-tiles per raster group for L2 reuse; 0: default (16) */
     void *mainloop_done_event;   /* cudaEvent_t or NULL: recorded on the stream after the main
                                     kernel, before the split-K combine kernel */
-    int timeout_ms;              /* per-wait device time limit; 0: default (4000 ms) */
+    int timeout_ms;              /* per-wait device time limit; 0: default (4000 ms plus 8 us for
+                                    each k-tile of the longest work unit and stream-K range) */
     int debug_skip_load;         /* test hook; must be 0 in normal use.  k: the producer leaves
                                     the k-th stage load (1-based, counting from the first load of
                                     CTA 0) unissued, so its consumer's wait runs out and the call

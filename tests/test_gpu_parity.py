@@ -242,6 +242,48 @@ def test_padded_leading_dimensions_and_guard_band(oracle_lib):
     assert check_f32(body[:, :N], ref, sabs)[0] == 0
 
 
+@pytest.mark.parametrize("variant", [1, 2, 3])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+@pytest.mark.parametrize("N", [1, 3, 7, 13, 259, 299, 301])
+def test_columns_past_n_keep_their_contents(oracle_lib, variant, out, N):
+    """C is a column slice of a wider buffer: nothing from column N to ldc, nor
+    in the rows around C, may change, whatever the decomposition (whole tiles,
+    a stream-K tail, split-K, the fused epilogue).  N not a whole number of
+    16-byte pieces is the case to watch: a TMA store clipped at N would write
+    the last piece whole.  Small integers make every value exact."""
+    g = _lib()
+    from oracle import epilogue as ep
+    M, K, guard = 200, 136, 3
+    A, Bt = operands(M, N, K, "int4", False, SEED + 70)
+    dA, dB = to_dev_padded(A), to_dev_padded(Bt).t()
+    ldc = _ru(N, 8) + 8
+    tdt = torch.float32 if out == "f32" else torch.bfloat16
+    P, _ = oracle_lib.gemm(A, Bt, M, N, K)
+    rng = np.random.default_rng(SEED + 71)
+    C_old = rng.integers(-8, 9, (M, N)).astype(np.float64)
+    bias = rng.integers(-3, 4, N).astype(np.float32)
+    epi = dict(beta=1.0, bias=torch.from_numpy(bias).cuda(), activation="relu")
+    modes = {"whole_tiles": dict(split_k=1, no_stream_k=True), "stream_k": dict(force_stream_k=True),
+             "split_k": dict(split_k=3), "fused": epi, "fused_stream_k": dict(epi, force_stream_k=True),
+             "fused_split_k": dict(epi, split_k=3)}
+    for mode, kw in modes.items():
+        buf = torch.full(((M + 2 * guard) * ldc,), -7.0, dtype=tdt, device="cuda")
+        C = buf[guard * ldc:(guard + M) * ldc].view(M, ldc)[:, :N]
+        want = P
+        if mode.startswith("fused"):
+            C.copy_(torch.from_numpy(C_old).to(tdt))
+            want = ep.epilogue(P, C_old, bias.astype(np.float64), alpha=1.0, beta=1.0, activation="relu")
+        g.matmul(dA, dB, out=C, kernel_variant=variant, **kw)
+        torch.cuda.synchronize()
+        host = buf.float().cpu().numpy().astype(np.float64)
+        assert np.all(host[:guard * ldc] == -7.0) and np.all(host[(guard + M) * ldc:] == -7.0), mode
+        body = host[guard * ldc:(guard + M) * ldc].reshape(M, ldc)
+        assert np.all(body[:, N:] == -7.0), f"{mode}: columns past N written"
+        if out == "bf16":
+            want = oracle_lib.bf16_to_f64(oracle_lib.f64_to_bf16(want))
+        assert np.array_equal(body[:, :N], want), mode
+
+
 def test_empty_and_zero_k(oracle_lib):
     g = _lib()
     s = torch.cuda.current_stream().cuda_stream
