@@ -24,6 +24,7 @@ the same workload.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import datetime as _dt
 import glob
 import hashlib
@@ -212,6 +213,65 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(inside), "note": note}
 
 
+class NvmlPoller:
+    """SM clock, its maximum and the clock-event reasons read through NVML
+    (read-only queries) while the host waits for a timed region's end event.
+    The region of a short step lasts a few milliseconds, shorter than
+    nvidia-smi's sampling period; these samples fall inside it."""
+    # nvmlClocksEventReasons bits (NVML's public header)
+    REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                   0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+    CLOCK_SM = 1
+
+    def __init__(self, uuid: str | None):
+        self.lib = None
+        if not uuid:
+            return
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            handle = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(handle)) != 0:
+                return
+            reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        except (OSError, AttributeError):
+            return
+        self.lib, self.handle, self.reasons = lib, handle, reasons
+
+    def sample(self):
+        clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        if (self.lib.nvmlDeviceGetClockInfo(self.handle, self.CLOCK_SM, ctypes.byref(clk)) != 0 or
+                self.lib.nvmlDeviceGetMaxClockInfo(self.handle, self.CLOCK_SM, ctypes.byref(mx)) != 0 or
+                self.reasons(self.handle, ctypes.byref(rs)) != 0):
+            return None
+        return float(clk.value), float(mx.value), int(rs.value)
+
+    def poll_until(self, event) -> list:
+        """Samples taken until ``event`` (a torch.cuda.Event) has completed."""
+        rows = []
+        while not event.query():
+            if self.lib is not None:
+                r = self.sample()
+                if r is not None:
+                    rows.append(r)
+            time.sleep(0.0002)
+        return rows
+
+
+def clocks_summary(nvml_rows: list, smi: dict) -> dict:
+    """The bench line's ``clocks``: from the NVML samples inside the timed
+    region when there are any, else nvidia-smi's; nvidia-smi's summary is
+    kept beside them."""
+    if not nvml_rows:
+        return dict(smi)
+    reasons = sorted({name for _, _, bits in nvml_rows for bit, name in NvmlPoller.REASON_BITS.items() if bits & bit})
+    return {"sm_mhz": statistics.median(r[0] for r in nvml_rows), "sm_max_mhz": max(r[1] for r in nvml_rows),
+            "reasons": reasons, "samples": len(nvml_rows),
+            "note": "NVML samples taken inside the timed region", "nvidia_smi": smi}
+
+
 # ---- distributed plumbing (host-side only: barrier and max/sum of scalars) ------------
 
 def dist_env():
@@ -317,6 +377,7 @@ def run_gpu(args, wname: str, w: dict, cpu_baseline: bool):
     gpu_id = getattr(props, "uuid", None)
     gpu_id = f"GPU-{gpu_id}" if gpu_id is not None else str(local)
     sampler = ClockSampler(gpu_id)
+    nvml = NvmlPoller(gpu_id if gpu_id.startswith("GPU-") else None)
     time.sleep(0.3)
     for i in range(args.warmup):
         step(i)
@@ -341,6 +402,7 @@ def run_gpu(args, wname: str, w: dict, cpu_baseline: bool):
     for i in range(args.steps):
         step(i)
     e1.record(stream)
+    nvml_rows = nvml.poll_until(e1)
     torch.cuda.synchronize()
     barrier()
     t_wall1 = time.time()
@@ -417,7 +479,7 @@ def run_gpu(args, wname: str, w: dict, cpu_baseline: bool):
         result["config"]["mainloop_us"] = round(mean_main_ms * 1e3, 3)
         result["config"]["combine_us"] = round(comb * 1e3, 3)
         result["config"]["combine_gbs"] = round(comb_bytes / (comb * 1e-3) / 1e9, 1)
-    clocks = sampler.summary(t_wall0, t_wall1)
+    clocks = clocks_summary(nvml_rows, sampler.summary(t_wall0, t_wall1))
     result["clocks"] = clocks
 
     # End to end through the public API: every step copies its A and B from
@@ -662,6 +724,7 @@ def run_gpu_conv(args, wname: str, w: dict):
 
     gpu_id = getattr(props, "uuid", None)
     sampler = ClockSampler(f"GPU-{gpu_id}" if gpu_id is not None else str(local))
+    nvml = NvmlPoller(f"GPU-{gpu_id}" if gpu_id is not None else None)
     time.sleep(0.3)   # before the warm-up: no idle gap before the timed region
     for i in range(args.warmup):
         step(i)
@@ -678,6 +741,7 @@ def run_gpu_conv(args, wname: str, w: dict):
     for i in range(args.steps):
         step(i)
     e1.record(stream)
+    nvml_rows = nvml.poll_until(e1)
     torch.cuda.synchronize()
     barrier()
     t_wall1 = time.time()
@@ -719,7 +783,7 @@ def run_gpu_conv(args, wname: str, w: dict):
             "launch_time_from": "timed region / steps, launches back to back",
         },
         "gpu_launches": (1 + (1 if plan.split_k > 1 else 0)) * args.steps,
-        "clocks": sampler.summary(t_wall0, t_wall1),
+        "clocks": clocks_summary(nvml_rows, sampler.summary(t_wall0, t_wall1)),
     }
     e2e_steps = min(args.steps, 20)
     hx = torch.from_numpy(x_h.view(np.int16)).view(torch.bfloat16).pin_memory()

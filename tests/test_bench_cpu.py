@@ -36,3 +36,18 @@ def test_reference_arm_prints_one_contract_line():
 def test_warmup_floor():
     r = _bench("--impl", "reference", "--workload", "square256", "--steps", "3", "--warmup", "2", timeout=120)
     assert r.returncode != 0 and "warmup" in r.stderr
+
+
+def test_clocks_summary_prefers_samples_inside_the_region():
+    """NVML samples from inside the timed region decide the clocks entry; the
+    reason bits decode to nvidia-smi's names; without samples the nvidia-smi
+    summary stands."""
+    sys.path.insert(0, ROOT)
+    import bench
+    smi = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 3, "note": "nearest samples"}
+    assert bench.clocks_summary([], smi) == smi
+    rows = [(2070.0, 2070.0, 0x0), (1980.0, 2070.0, 0x4), (2070.0, 2070.0, 0x1), (1500.0, 2070.0, 0x8 | 0x40)]
+    c = bench.clocks_summary(rows, smi)
+    assert c["sm_mhz"] == 2025.0 and c["sm_max_mhz"] == 2070.0 and c["samples"] == 4
+    assert c["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_power_cap"]
+    assert c["nvidia_smi"] == smi
