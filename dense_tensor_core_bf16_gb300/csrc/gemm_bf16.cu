@@ -779,6 +779,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     __syncwarp();
                     load_c_chunk(col_base, s0 & 1u);
                 }
+                if (owner_fast) prefetch(0);
 #pragma unroll 1
                 for (int c = 0; c < n_chunks; ++c) {
                     const int col0 = col_base + c * 32;
@@ -838,7 +839,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     __syncwarp();
                     ptx::tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r);
                     ptx::tmem_wait_ld(r);
-                    if (w.kind == KIND_OWNER) add_partials(r, c);
+                    if (owner_fast) {
+                        // the contributor's partial sums of this chunk, loaded a
+                        // chunk ahead; the next chunk's go out now and land while
+                        // this one is finished and stored
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            r[4 * v + 0] = __float_as_uint(__uint_as_float(r[4 * v + 0]) + pre[v].x);
+                            r[4 * v + 1] = __float_as_uint(__uint_as_float(r[4 * v + 1]) + pre[v].y);
+                            r[4 * v + 2] = __float_as_uint(__uint_as_float(r[4 * v + 2]) + pre[v].z);
+                            r[4 * v + 3] = __float_as_uint(__uint_as_float(r[4 * v + 3]) + pre[v].w);
+                        }
+                        if (c + 1 < n_chunks) prefetch(c + 1);
+                    } else if (w.kind == KIND_OWNER) {
+                        add_partials(r, c);
+                    }
 #pragma unroll
                     for (int g = 0; g < 8; ++g) {
                         const float b0 = __shfl_sync(0xffffffffu, b_lane, 4 * g + 0);
