@@ -31,6 +31,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -130,14 +131,22 @@ def roofline_entry(flops: float, alg_bytes: float, mean_ms: float, peaks: dict, 
             "algorithmic_flops_per_launch": flops}
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without its comments (none of the library's string
+    literals holds a comment marker)."""
+    return re.sub(r"//[^\n]*", "", re.sub(r"/\*.*?\*/", "", text, flags=re.S))
+
+
 def kernel_source_hash() -> str:
+    """sha256 over the library's sources with comments removed: the code the
+    recorded counters were taken on, not its prose."""
     h = hashlib.sha256()
     files = sorted(glob.glob(os.path.join(ROOT, "dense_tensor_core_bf16_gb300", "csrc", "*")))
     files.append(os.path.join(ROOT, "include", "gemm_bf16.h"))
     for fn in files:
-        with open(fn, "rb") as f:
+        with open(fn, encoding="utf-8") as f:
             h.update(os.path.basename(fn).encode())
-            h.update(f.read())
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()
 
 

@@ -36,8 +36,9 @@
  *   - lda and ldb are multiples of 8 (16 bytes of bf16);
  *   - ldc is a multiple of 8 for bf16 C and of 4 for fp32 C.
  * M, N and K themselves need no particular multiple: ragged edges are
- * zero-filled on load and masked on store.  Each of M, N, K must be below
- * 2^31.
+ * zero-filled on load and masked on store.  Nothing outside the M x N block
+ * of C is written (columns N .. ldc-1 keep their contents, so C may be a
+ * column slice of a wider matrix).  Each of M, N, K must be below 2^31.
  */
 #ifndef GEMM_BF16_H
 #define GEMM_BF16_H

@@ -51,3 +51,15 @@ def test_clocks_summary_prefers_samples_inside_the_region():
     assert c["sm_mhz"] == 2025.0 and c["sm_max_mhz"] == 2070.0 and c["samples"] == 4
     assert c["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_power_cap"]
     assert c["nvidia_smi"] == smi
+
+
+def test_source_hash_ignores_comments_only():
+    """The hash that ties a recorded DRAM count to the code changes with the
+    code, not with its comments."""
+    sys.path.insert(0, ROOT)
+    import bench
+    a = "int f(int x) {\n    return x + 1;   // one more\n}\n/* note */\n"
+    b = "int f(int x) {\n    return x + 1;   // one more, reworded\n}\n/* another\n   note */\n"
+    c = "int f(int x) {\n    return x + 2;   // one more\n}\n/* note */\n"
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)
