@@ -137,11 +137,16 @@ def _code_only(text: str) -> str:
     return re.sub(r"//[^\n]*", "", re.sub(r"/\*.*?\*/", "", text, flags=re.S))
 
 
+# The files that decide what the GEMM kernels do and how a problem is cut into
+# launches; the host-batch pipeline (host_pipeline.cpp) only feeds them.
+KERNEL_SOURCES = ("gemm_bf16.cu", "kernel_config.h", "plan.cpp", "plan_internal.h", "ptx.cuh")
+
+
 def kernel_source_hash() -> str:
     """sha256 over the library's sources with comments removed: the code the
     recorded counters were taken on, not its prose."""
     h = hashlib.sha256()
-    files = sorted(glob.glob(os.path.join(ROOT, "dense_tensor_core_bf16_gb300", "csrc", "*")))
+    files = [os.path.join(ROOT, "dense_tensor_core_bf16_gb300", "csrc", f) for f in KERNEL_SOURCES]
     files.append(os.path.join(ROOT, "include", "gemm_bf16.h"))
     for fn in files:
         with open(fn, encoding="utf-8") as f:

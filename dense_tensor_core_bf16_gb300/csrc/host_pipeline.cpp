@@ -287,6 +287,15 @@ extern "C" gemm_status_t gemm_bf16_host_batch(int64_t count, const gemm_host_pro
     // Even after a failure the caller's stream waits for what was enqueued,
     // so that the host arrays it covers are not released under the copies.
     if (last && !ok(cudaStreamWaitEvent(caller, last->out_done, 0))) return GEMM_ERR_LAUNCH;
+    if (st != GEMM_OK || !good) {
+        // A problem that failed before its result copy may still have operand
+        // copies (and part of its product) in flight: wait for every lane and
+        // the product stream too.  `start` is free to record again: each wait
+        // takes the event as last recorded when the wait is enqueued.
+        for (int j = 0; j < kLanes; ++j)
+            if (ok(cudaEventRecord(pipe.start, pipe.lane[j]))) ok(cudaStreamWaitEvent(caller, pipe.start, 0));
+        if (ok(cudaEventRecord(pipe.start, pipe.comp))) ok(cudaStreamWaitEvent(caller, pipe.start, 0));
+    }
     if (st != GEMM_OK) return st;
     return good ? GEMM_OK : GEMM_ERR_LAUNCH;
 }
