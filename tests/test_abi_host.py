@@ -186,6 +186,28 @@ def test_plan_split_k_workload(split, eta):
     assert p.workspace_bytes == (split * 128 * 256 * 4 if split > 1 else 0)
 
 
+def test_plan_at_the_size_limits():
+    """K = 2^31 - 8 for one output, and a C of more than 2^31 elements: the
+    plans the GPU size-limit tests run, by hand.  One tile of 2^25 64-wide
+    k-tiles splits over the 152 single CTAs (each slice at least 4 k-tiles);
+    the pair kernel with a forced tail spreads its one tile over all 76
+    clusters; the large C has 513 x 129 single-CTA tiles of one k-tile."""
+    K = (1 << 31) - 8
+    p = _plan(1, 1, K, split=0, out=g.GEMM_OUT_F32)
+    assert p.k_tiles == (K + 63) // 64 == 1 << 25
+    assert p.split_k == 152 and p.k_tiles_per_split == -(-(1 << 25) // 152)
+    assert p.workspace_bytes == 152 * 128 * 256 * 4
+    p = _plan(1, 1, K, split=0, variant=2, mac=76, no_sk=-1, out=g.GEMM_OUT_F32)
+    assert p.k_tiles == 1 << 24 and p.stream_k_tiles == 1 and p.dp_tiles == 0 and p.split_k == 1
+    assert p.launch_ctas == 152 and p.workspace_bytes == 76 * 256 * 256 * 4
+    p = _plan(1, 1, K, split=1, variant=2, mac=76, out=g.GEMM_OUT_F32)
+    assert p.split_k == 1 and p.stream_k_tiles == 0 and p.launch_ctas == 2
+    M, N = 65605, 32792
+    assert M * N > 1 << 31
+    p = _plan(M, N, 72, split=0)
+    assert (p.tiles, p.k_tiles, p.split_k, p.stream_k_tiles) == (513 * 129, 2, 1, 0)
+
+
 def test_plan_split_k_clamped_and_auto():
     p = _plan(128, 256, 200, split=50)        # 4 k-tiles: at most 4 slices
     assert p.split_k == 4
