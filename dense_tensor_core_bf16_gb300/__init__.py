@@ -228,8 +228,14 @@ GEMM_NOALLOC_SCRATCH_FLOATS = 16 * 1024 * 1024 // 4
 
 def gemm_bf16_splitk_noalloc(M, N, K, A, lda, B, ldb, C, ldc, layout_a, layout_b, out_dtype, split_k, stream) -> int:
     """Status code of the C call: gemm_bf16 for callers that must not allocate
-    device memory; split-K partials go to a fixed 16 MiB array in the library
-    (split * M * round_up(N, 4) must fit in it)."""
+    device memory; split-K partials go to a fixed 16 MiB array in the library.
+
+    The limit counts whole tiles of the kernel the plan picks:
+    split * ceil(M / tile_m) * ceil(N / tile_n) * tile_m * tile_n must be at
+    most GEMM_NOALLOC_SCRATCH_FLOATS (tiles of 128 x 256 or 256 x 256, so a
+    ragged M or N costs a whole padded tile).  To size a call in advance, ask
+    gemm_plan with the same split and no_stream_k=1 (this entry point never
+    uses a stream-K tail) and compare its workspace_bytes with the 16 MiB."""
     return lib().gemm_bf16_splitk_noalloc(M, N, K, A, lda, B, ldb, C, ldc, layout_a, layout_b, out_dtype,
                                           split_k, stream)
 

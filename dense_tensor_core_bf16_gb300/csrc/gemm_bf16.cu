@@ -1177,6 +1177,12 @@ struct DeviceState {
     bool ready = false;
     gemm_device_desc_t desc{};
     VariantState var[VARIANT_COUNT];
+    // The split-K / stream-K workspace and its size, guarded by ws_mutex.  A
+    // launch that uses it holds ws_mutex from the size check until its
+    // kernels are enqueued, so no other host thread can free the buffer in
+    // between (a grower synchronises the device before freeing, which then
+    // waits for those kernels).
+    std::mutex ws_mutex;
     float *workspace = nullptr;
     size_t workspace_bytes = 0;
     unsigned int *sk_flags = nullptr;   // zeroed once; contributors publish the launch's epoch, owners clear
@@ -1338,8 +1344,8 @@ gemm_status_t encode_output(CUtensorMap *map, void *ptr, int64_t cols, int64_t r
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_LAUNCH;
 }
 
+// Grow the workspace to at least `bytes`; the caller holds ds.ws_mutex.
 gemm_status_t ensure_workspace(DeviceState &ds, size_t bytes) {
-    std::lock_guard<std::mutex> lock(g_mutex);
     if (ds.workspace_bytes >= bytes) return GEMM_OK;
     if (ds.workspace) {
         cudaDeviceSynchronize();   // the old buffer may still be read by queued work
@@ -1507,6 +1513,9 @@ gemm_status_t launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_
     if (st != GEMM_OK) return st;
     const int64_t clusters = plan.launch_ctas / vi.cta_group;
     float *partials = nullptr;
+    // held until the kernels that read the workspace are enqueued
+    std::unique_lock<std::mutex> ws_lock(ds.ws_mutex, std::defer_lock);
+    if (plan.stream_k_tiles > 0 || (plan.split_k > 1 && !pb.fixed)) ws_lock.lock();
     if (plan.stream_k_tiles > 0) {
         if (clusters * vi.cta_group * EPI_WARPS > kMaxFlagSlots) return GEMM_ERR_NOT_SUPPORTED;
         st = ensure_flags(ds);
@@ -1748,12 +1757,12 @@ gemm_status_t gemm_reserve_workspace(size_t bytes) {
     DeviceState *ds = nullptr;
     gemm_status_t st = current_device(&device, &ds);
     if (st != GEMM_OK) return st;
+    std::lock_guard<std::mutex> lock(ds->ws_mutex);
     return ensure_workspace(*ds, bytes);
 }
 
 void gemm_release_workspace(void) {
-    release_host_staging();   // takes its own per-device locks, never under g_mutex
-    std::lock_guard<std::mutex> lock(g_mutex);
+    release_host_staging();   // takes its own per-device locks, never under a workspace lock
     int current = -1;
     if (cudaGetDevice(&current) != cudaSuccess) {
         cudaGetLastError();
@@ -1761,6 +1770,7 @@ void gemm_release_workspace(void) {
     }
     for (int d = 0; d < kMaxDevices; ++d) {
         DeviceState &ds = g_devices[d];
+        std::lock_guard<std::mutex> lock(ds.ws_mutex);
         if (!ds.workspace) continue;
         if (cudaSetDevice(d) == cudaSuccess) {
             cudaDeviceSynchronize();

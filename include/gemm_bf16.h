@@ -284,7 +284,10 @@ gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K,
  * call); reserve it beforehand with gemm_reserve_workspace() to keep
  * allocation out of timed regions and stream captures.
  * Calls that share the workspace must not overlap in time on different
- * streams of one device.
+ * streams of one device.  The library's host-side bookkeeping is
+ * thread-safe: while one host thread enqueues work that reads the workspace,
+ * a lock keeps every other thread from growing or freeing it.  Work enqueued
+ * by several host threads must still not overlap on the GPU, as above.
  */
 gemm_status_t gemm_bf16(int64_t M, int64_t N, int64_t K,
                         const void *A, int64_t lda, const void *B, int64_t ldb,
@@ -312,11 +315,13 @@ gemm_status_t gemm_bf16(int64_t M, int64_t N, int64_t K,
  *
  * Arguments, layouts, alignment rules and results are those of gemm_bf16.
  * The split actually used (split_k, or the plan's choice when split_k is 0)
- * must satisfy  split * tiles * tile_m * tile_n <= GEMM_NOALLOC_SCRATCH_FLOATS
- * (the plan's workspace_bytes / 4; with 128 x 256 tiles and M, N multiples
- * of them that is split * M * N); otherwise the call returns
- * GEMM_ERR_INVALID_VALUE and launches nothing.  split_k = 1 uses no scratch
- * at all, and this entry point never uses a stream-K tail.
+ * must satisfy  split * tiles * tile_m * tile_n <= GEMM_NOALLOC_SCRATCH_FLOATS,
+ * counting whole (padded) tiles of the kernel the plan picks; that is the
+ * workspace_bytes / 4 of gemm_plan with the same split_k and no_stream_k = 1
+ * (with 128 x 256 tiles and M, N multiples of them it is split * M * N);
+ * otherwise the call returns GEMM_ERR_INVALID_VALUE and launches nothing.
+ * split_k = 1 uses no scratch at all, and this entry point never uses a
+ * stream-K tail.
  *
  * The first call on a device looks up the array's address on that device
  * (cudaGetSymbolAddress); make that first call before any stream capture.

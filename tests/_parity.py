@@ -11,6 +11,9 @@ Tolerances (stated with the workloads of the BF16 GEMM):
              accumulation can promise one ulp; there C must be the bf16
              rounding of some value within beta of C_ref:
              RN_bf16(C_ref - beta) <= C <= RN_bf16(C_ref + beta);
+    The entries that pass only through that clause are counted, and every
+    check caps the count at cancellation_cap(n) of its n entries: one in
+    10,000, at least 8, the same cap for full and sampled checks;
   * small-integer inputs: bit-exact (every fp32 partial sum is an integer
     below 2^24, so fp32 accumulation is exact in any order);
   * a non-finite output is always a failure.
@@ -22,6 +25,12 @@ import numpy as np
 
 F32_REL = 2.0 ** -16
 F32_ABS = 1e-6
+
+
+def cancellation_cap(n: int) -> int:
+    """Largest number of bf16 entries, out of n checked, that may pass only
+    through the accumulation-bound clause (one in 10,000, at least 8)."""
+    return max(8, int(n) // 10000)
 
 
 def check_f32(C: np.ndarray, ref: np.ndarray, sabs: np.ndarray):

@@ -8,7 +8,7 @@ import pytest
 
 from dense_tensor_core_bf16_gb300 import inputs
 
-from ._parity import check_bf16, check_f32
+from ._parity import cancellation_cap, check_bf16, check_f32
 
 torch = pytest.importorskip("torch")
 pytestmark = [pytest.mark.gpu, pytest.mark.timeout(900)]
@@ -64,6 +64,7 @@ def check(oracle, x, w, y, out, exact=False, **conv):
         if exact:
             assert neq == 0
         assert nbad == 0, detail
+        assert ncanc <= cancellation_cap(y2.size), f"{ncanc} entries needed the cancellation clause"
 
 
 CASES = [

@@ -13,7 +13,7 @@ import pytest
 
 from dense_tensor_core_bf16_gb300 import inputs
 
-from ._parity import check_bf16, check_f32, sample_entries
+from ._parity import cancellation_cap, check_bf16, check_f32, sample_entries
 from .test_gpu_parity import operands, to_dev_padded
 
 torch = pytest.importorskip("torch")
@@ -58,8 +58,9 @@ def check(oracle, A, Bt, C):
         nbad, worst = check_f32(got, ref, sabs)
         assert nbad == 0, f"{nbad} fp32 entries outside the bound (worst {worst:.3g})"
     else:
-        nbad, _, _, detail = check_bf16(got, ref, sabs, oracle)
+        nbad, _, ncanc, detail = check_bf16(got, ref, sabs, oracle)
         assert nbad == 0, detail
+        assert ncanc <= cancellation_cap(ref.size), f"{ncanc} entries needed the cancellation clause"
 
 
 # (M, N, K, A column-major, B row-major): ragged tiles, K not a multiple of 8
@@ -188,6 +189,7 @@ def test_square4096_batch_sampled(oracle_lib):
     for (a, b), C in zip([(A, Bt), (A2, Bt2)], Cs[:2]):
         rows, cols = sample_entries(M, N, 4000, SEED)
         ref, sabs = oracle_lib.gemm_entries(a, b, M, N, K, rows, cols)
-        nbad, _, _, detail = check_bf16(as_numpy(C)[rows, cols], ref, sabs, oracle_lib)
+        nbad, _, ncanc, detail = check_bf16(as_numpy(C)[rows, cols], ref, sabs, oracle_lib)
         assert nbad == 0, detail
+        assert ncanc <= cancellation_cap(ref.size), f"{ncanc} entries needed the cancellation clause"
     assert torch.equal(Cs[0], Cs[2])

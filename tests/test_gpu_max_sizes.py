@@ -17,7 +17,7 @@ import pytest
 
 from dense_tensor_core_bf16_gb300 import inputs
 
-from ._parity import check_bf16, check_f32, sample_entries
+from ._parity import cancellation_cap, check_bf16, check_f32, sample_entries
 
 torch = pytest.importorskip("torch")
 pytestmark = [pytest.mark.gpu, pytest.mark.timeout(900)]
@@ -97,8 +97,9 @@ def test_c_past_2_31_elements(oracle_lib, out, variant):
         nbad, worst = check_f32(got, ref, sabs)
         assert nbad == 0, f"{nbad} fp32 entries outside the bound (worst {worst:.3g})"
     else:
-        nbad, _, _, detail = check_bf16(got, ref, sabs, oracle_lib)
+        nbad, _, ncanc, detail = check_bf16(got, ref, sabs, oracle_lib)
         assert nbad == 0, detail
+        assert ncanc <= cancellation_cap(ref.size), f"{ncanc} entries needed the cancellation clause"
 
 
 @pytest.mark.parametrize("out", [torch.bfloat16, torch.float32])

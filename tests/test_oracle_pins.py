@@ -411,15 +411,16 @@ def test_gelu_against_high_precision():
         assert v == pytest.approx(float(ref), rel=4e-16, abs=1e-300)
 
 
-def test_epilogue_tolerance_shape():
-    """The bound reduces to the plain fp32 accumulation bound (plus the
-    rounding of one sum) when there is nothing to fuse, and grows with the
-    magnitudes that enter the fp32 sum."""
+def test_epilogue_tolerance_grows_with_what_enters_the_sum():
+    """The bound is never below the plain fp32 accumulation bound and grows
+    with the magnitudes that enter the fp32 sum and with the activation.
+    (Its size is pinned from both sides in test_oracle_tolerance_pin.py: an
+    emulated correct fp32 device lands inside it, planted slips outside.)"""
     from oracle import epilogue as ep
     P = np.array([[1.0, -4.0]])
     S = np.array([[2.0, 8.0]])
     t0 = ep.tolerance(P, S)
-    assert np.allclose(t0, 2.0 ** -16 * S + 1e-6 + 2.0 ** -22 * np.abs(P) + 1e-6)
+    assert np.all(t0 >= 2.0 ** -16 * S + 1e-6)
     t1 = ep.tolerance(P, S, np.array([[1e3, 1e3]]), beta=1.0)
     assert np.all(t1 > t0)
     assert np.all(ep.tolerance(P, S, activation="gelu") > t0)
