@@ -2,12 +2,20 @@
 """BF16 Tensor Core GEMM benchmark on GB300: TFLOP/s = 2MNK / device time.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--no-cpu-baseline] [--all-workloads]
+                    [--workload NAME | --m M --n N --k K [--A row|col] [--B row|col]
+                     [--C bf16|f32] [--split-k S] [--persistent 0|1]]
+                    [--no-cpu-baseline] [--sustained-seconds S] [--no-e2e] [--all-workloads]
+                    [--oracle-table]
 
 A step is one GEMM C = A . B over one batch of synthetic input (the whole hot
 path: plan, TMA-fed tcgen05 main loop, epilogue, and the split-K combine when
-the workload uses it).  The default workload is the square 4096^3 GEMM with
-bf16 A (row-major), B (column-major) and C, inputs N(0,1)/sqrt(K).
+the workload uses it).  The default workload is the largest single-GPU one,
+the rectangular 16384 x 8192 x 8192 GEMM with bf16 A (row-major), B
+(column-major) and C, inputs N(0,1)/sqrt(K), on the persistent scheduler.
+--m/--n/--k (with the layout, output and split flags, as a library profiler
+takes them) time any other shape.  After the K timed steps the same GEMM runs
+back to back for --sustained-seconds more (default 4 s) to report the rate
+the part sustains under its power cap, beside the clocks it ran at.
 
 Timing: W untimed warm-up steps, then K steps bracketed by a barrier and
 torch.cuda.synchronize() on both sides, CUDA events on the launching stream
@@ -95,6 +103,58 @@ for _s in (1, 8, 32, 74, 148):
                                          f"split_k={_s}")
 
 KERNEL_NAME = "gemm_bf16_kernel"
+DEFAULT_WORKLOAD = "large"
+# How every timed region keeps its operands out of L2 (the same words on both arms).
+L2_POLICY = ("inputs larger than L2: operand sets rotate so that the bytes touched between two uses of one set "
+             "exceed twice the L2 size")
+
+
+def custom_workload(m: int, n: int, k: int, a: str, b: str, c: str, split_k: int, persistent: int, dist: str):
+    """A workload from profiler-style flags (--m --n --k --A --B --C --split-k --persistent)."""
+    scaled = dist != "int4"
+    return dict(M=m, N=n, K=k, out=c, dist=dist, scaled=scaled, split_k=split_k, a_col=a == "col", b_row=b == "row",
+                non_persistent=not persistent,
+                desc=f"gemm_bf16 {m}x{n}x{k}, A bf16 {a}-major, B bf16 {b}-major, C {c} row-major, "
+                     f"inputs {dist}{'/sqrt(K)' if scaled else ''}, split_k={split_k}, "
+                     f"{'persistent' if persistent else 'one cluster per tile'}")
+
+
+def workload_data(w: dict, seed: int) -> str:
+    """The bench line's ``data`` for a GEMM workload (both arms)."""
+    return f"synthetic (seeded SplitMix64, {w['dist']}{'/sqrt(K)' if w['scaled'] else ''}, seed {seed})"
+
+
+def workload_config(w: dict) -> dict:
+    """The bench line's ``config`` for a GEMM workload: what is computed and
+    how it is timed, the same on both arms (the GPU arm's plan goes under
+    ``plan``)."""
+    return {"workload": w["desc"], "M": w["M"], "N": w["N"], "K": w["K"], "out": w["out"],
+            "layout_a": "column-major" if w.get("a_col") else "row-major",
+            "layout_b": "row-major" if w.get("b_row") else "column-major",
+            "epilogue": w.get("epilogue"), "split_k": w["split_k"],
+            "launch": "one cluster per tile" if w.get("non_persistent") else "persistent",
+            "l2": L2_POLICY, "parallelism": "replicas (one independent GEMM per GPU)"}
+
+
+def conv_out_dims(cv: dict):
+    P = (cv["H"] + 2 * cv["pad"][0] - cv["dil"][0] * (cv["R"] - 1) - 1) // cv["stride"][0] + 1
+    Q = (cv["W"] + 2 * cv["pad"][1] - cv["dil"][1] * (cv["S"] - 1) - 1) // cv["stride"][1] + 1
+    return P, Q
+
+
+CONV_METRIC = "conv2d TFLOP/s (2 N P Q K R S C / device time) and % of GB300 dense BF16 peak, 1 GPU"
+
+
+def conv_data(seed: int) -> str:
+    return f"synthetic (seeded SplitMix64, N(0,1) input, N(0,1)/sqrt(RSC) filter, seed {seed})"
+
+
+def conv_config(w: dict) -> dict:
+    cv = w["conv"]
+    P, Q = conv_out_dims(cv)
+    return {"workload": w["desc"], **{k: v for k, v in cv.items()}, "P": P, "Q": Q, "out": w["out"],
+            "gemm": {"M": cv["N"] * P * Q, "N": cv["K"], "K": cv["R"] * cv["S"] * cv["C"]},
+            "l2": L2_POLICY, "parallelism": "replicas (one independent convolution per GPU)"}
 
 
 def log(*a):
@@ -261,6 +321,28 @@ class NvmlPoller:
                 self.reasons(self.handle, ctypes.byref(rs)) != 0):
             return None
         return float(clk.value), float(mx.value), int(rs.value)
+
+    def sample_in_background(self, period_s: float = 0.002):
+        """(rows, stop): samples appended to ``rows`` by a thread every
+        ``period_s`` until ``stop()`` is called (ctypes releases the GIL
+        during each NVML call)."""
+        rows, done = [], threading.Event()
+
+        def run():
+            while not done.is_set():
+                if self.lib is not None:
+                    r = self.sample()
+                    if r is not None:
+                        rows.append(r)
+                time.sleep(period_s)
+
+        t = threading.Thread(target=run, daemon=True)
+        t.start()
+
+        def stop():
+            done.set()
+            t.join(timeout=5)
+        return rows, stop
 
     def poll_until(self, event) -> list:
         """Samples taken until ``event`` (a torch.cuda.Event) has completed."""
@@ -459,11 +541,9 @@ def run_gpu(args, wname: str, w: dict, cpu_baseline: bool):
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 6), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": f"synthetic (seeded SplitMix64, {w['dist']}{'/sqrt(K)' if w['scaled'] else ''}, seed {seed})",
-        "config": {
-            "workload": w["desc"], "M": M, "N": N, "K": K, "out": w["out"],
-            "layout_a": "column-major" if a_col else "row-major", "layout_b": "row-major" if b_row else "column-major",
-            "epilogue": w.get("epilogue"),
+        "data": workload_data(w, seed),
+        "config": workload_config(w),
+        "plan": {
             "kernel_variant": g.KERNEL_VARIANTS[plan.kernel_variant], "cluster_size": plan.cluster_size,
             "tile": f"{plan.tile_m}x{plan.tile_n}x{plan.tile_k}", "stages": plan.stages,
             "split_k": plan.split_k, "persistent": bool(plan.persistent), "grid_G": plan.grid,
@@ -474,9 +554,8 @@ def run_gpu(args, wname: str, w: dict, cpu_baseline: bool):
             "stream_k_tiles": plan.stream_k_tiles, "dp_tiles": plan.dp_tiles,
             "eta_stream_k": round(plan.eta_stream_k, 5),
             "pct_of_peak": round(100.0 * value / world / peak, 2), "peak_tflops": peak, "peak_kind": peak_kind,
-            "l2": f"inputs larger than L2: {copies} rotating operand sets of {set_bytes / 1e6:.1f} MB "
-                  f"({copies * set_bytes / 1e6:.0f} MB) vs L2 {l2 / 1e6:.1f} MB",
-            "parallelism": "replicas" if world > 1 else "single GPU",
+            "l2_sets": f"{copies} rotating operand sets of {set_bytes / 1e6:.1f} MB "
+                       f"({copies * set_bytes / 1e6:.0f} MB) vs L2 {l2 / 1e6:.1f} MB",
         },
         "roofline": {
             "kernel": f"{KERNEL_NAME}<{plan.cluster_size},{plan.tile_n}>",
@@ -490,11 +569,18 @@ def run_gpu(args, wname: str, w: dict, cpu_baseline: bool):
     if combine_ms is not None:
         comb = statistics.fmean(combine_ms)
         comb_bytes = plan.split_k * M * N * 4 + esize * M * N   # algorithmic: every slice read once, C written once
-        result["config"]["mainloop_us"] = round(mean_main_ms * 1e3, 3)
-        result["config"]["combine_us"] = round(comb * 1e3, 3)
-        result["config"]["combine_gbs"] = round(comb_bytes / (comb * 1e-3) / 1e9, 1)
+        result["plan"]["mainloop_us"] = round(mean_main_ms * 1e3, 3)
+        result["plan"]["combine_us"] = round(comb * 1e3, 3)
+        result["plan"]["combine_gbs"] = round(comb_bytes / (comb * 1e-3) / 1e9, 1)
     clocks = clocks_summary(nvml_rows, sampler.summary(t_wall0, t_wall1))
     result["clocks"] = clocks
+    if args.sustained_seconds > 0:
+        result["sustained"] = sustained_region(args.sustained_seconds, max_ms / args.steps, step, flops, peaks,
+                                               stream, nvml, gpu_id)
+    if args.no_e2e:
+        if cpu_baseline and rank == 0 and world == 1:
+            result["cpu_baseline"] = cpu_oracle_baseline(A_h, Bt_h, M, N, K, target_s=args.cpu_seconds)
+        return result, rank
 
     # End to end through the public API: every step copies its A and B from
     # pinned host memory and its C back, through gemm_bf16_host_batch, which
@@ -575,26 +661,123 @@ def host_link_floor(hA, hB, hC, dA, dB, dC, reps: int = 5) -> dict:
             "ms_per_step_both_directions": round(t_both, 4)}
 
 
+def sustained_region(seconds: float, ms_per_step: float, step, flops: float, peaks: dict, stream, nvml,
+                     smi_id: str) -> dict:
+    """The same step back to back for about ``seconds``: the rate the part
+    sustains under its power cap, against the measured sustained bf16 peak,
+    with the SM clock and clock-event reasons sampled inside the region
+    (NVML every 2 ms, nvidia-smi every 100 ms).  ``cycles_per_step`` is the
+    step time times the median SM clock, and ``tflops_at_max_clock`` the rate
+    those cycles would give at the maximum clock."""
+    import torch
+    n = max(10, int(math.ceil(seconds * 1e3 / max(ms_per_step, 1e-3))))
+    sampler = ClockSampler(smi_id)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    rows, stop = nvml.sample_in_background()
+    t0 = time.time()
+    e0.record(stream)
+    for i in range(n):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    stop()
+    sampler.stop()
+    ms = e0.elapsed_time(e1)
+    value = flops * n / (ms * 1e-3) / 1e12
+    peak = peaks["bf16_sustained"]
+    clocks = clocks_summary(rows, sampler.summary(t0, t1))
+    out = {"value": round(value, 3), "unit": UNIT, "steps": n, "seconds": round(ms * 1e-3, 3),
+           "ms_per_step": round(ms / n, 6), "peak": peak,
+           "peak_source": f"sustained bf16, {peaks['source']}", "frac": round(value / peak, 4), "clocks": clocks}
+    mhz, mx = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+    if mhz and mx:
+        out["cycles_per_step"] = round(ms / n * 1e-3 * mhz * 1e6)
+        out["tflops_at_max_clock"] = round(value * mx / mhz, 3)
+    return out
+
+
 # ---- the oracle on the host cores ---------------------------------------------------------
+
+def host_cpu() -> dict:
+    """Host core count (os.cpu_count) and the CPU model from lscpu, when it runs."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() == "Model name":
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return {"host_cores": os.cpu_count(), "cpu_model": model}
+
+
+def _time_oracle_rows(A_h, Bt_h, M, N, K, target_s: float, threads: int):
+    """(rows, seconds) of the oracle on the first rows of C, sized for about target_s."""
+    import oracle
+    r0 = min(M, 4 * max(threads, 1))
+    t = time.perf_counter()
+    oracle.gemm(A_h[:r0], Bt_h, r0, N, K, with_abs=False, threads=threads)
+    dt0 = max(time.perf_counter() - t, 1e-3)
+    rows = int(min(M, max(1, math.floor(r0 * target_s / dt0))))
+    t = time.perf_counter()
+    oracle.gemm(A_h[:rows], Bt_h, rows, N, K, with_abs=False, threads=threads)
+    return rows, time.perf_counter() - t
+
 
 def cpu_oracle_baseline(A_h, Bt_h, M, N, K, target_s: float):
     """Time the oracle, as it stands, on the first R rows of C (R x N outputs at
-    the workload's K), R sized for about target_s seconds of CPU work."""
+    the workload's K), R sized for about target_s seconds of CPU work with all
+    of OpenMP's threads, and again on one thread for about a third of that."""
     import oracle
     oracle.build()
     cores = oracle.max_threads()
     oracle.gemm(A_h[:cores], Bt_h, cores, N, K, with_abs=False)      # start the thread pool
-    r0 = min(M, 4 * cores)
-    t = time.perf_counter()
-    oracle.gemm(A_h[:r0], Bt_h, r0, N, K, with_abs=False)
-    dt0 = max(time.perf_counter() - t, 1e-3)
-    rows = int(min(M, max(1, math.floor(r0 * target_s / dt0))))
-    t = time.perf_counter()
-    oracle.gemm(A_h[:rows], Bt_h, rows, N, K, with_abs=False)
-    dt = time.perf_counter() - t
+    rows, dt = _time_oracle_rows(A_h, Bt_h, M, N, K, target_s, cores)
+    rows1, dt1 = _time_oracle_rows(A_h, Bt_h, M, N, K, target_s / 3.0, 1)
     return {"value": round(2.0 * rows * N * K / dt / 1e12, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"rows 0..{rows - 1} of C ({rows}x{N} outputs, K={K}), binary64 triple loop, "
-                      f"{cores} OpenMP threads, {dt:.1f} s"}
+                      f"{cores} OpenMP threads, {dt:.1f} s",
+            "single_thread": {"value": round(2.0 * rows1 * N * K / dt1 / 1e12, 6), "unit": UNIT,
+                              "sample": f"rows 0..{rows1 - 1} of C, one thread, {dt1:.1f} s"},
+            **host_cpu()}
+
+
+def oracle_table(one_thread_budget_s: float = 4.0):
+    """The oracle alone on the host cores, for the correctness and square,
+    neighbour and split-K workloads: every output of C with all of OpenMP's
+    threads, and one thread on the first rows of C (all of them when that
+    takes at most about 10 s; otherwise a row sample, scaled to the whole C and
+    marked as such).  Yields one dict per workload."""
+    import oracle
+    oracle.build()
+    cores = oracle.max_threads()
+    names = ["square256", "square4096", "n4095", "n4097", "k4088", "n4104", "m3968", "splitk148"]
+    for name in names:
+        w = WORKLOADS[name]
+        (A_h, Bt_h), seed = make_host_operands(w)
+        M, N, K = w["M"], w["N"], w["K"]
+        oracle.gemm(A_h[:min(M, cores)], Bt_h, min(M, cores), N, K, with_abs=False)   # thread pool up
+        t = time.perf_counter()
+        oracle.gemm(A_h, Bt_h, M, N, K, with_abs=False)
+        dt_all = time.perf_counter() - t
+        rows1, dt1 = _time_oracle_rows(A_h, Bt_h, M, N, K, one_thread_budget_s, 1)
+        full1 = dt1 * M / rows1
+        if rows1 < M and full1 <= 10.0:
+            t = time.perf_counter()
+            oracle.gemm(A_h, Bt_h, M, N, K, with_abs=False, threads=1)
+            dt1, rows1 = time.perf_counter() - t, M
+            full1 = dt1
+        flops = 2.0 * M * N * K
+        yield {"oracle_table": name, "workload": w["desc"], "M": M, "N": N, "K": K, "flops": flops,
+               "all_threads": {"threads": cores, "seconds": round(dt_all, 3), "tflops": round(flops / dt_all / 1e12, 6),
+                               "outputs": "all of C"},
+               "one_thread": {"seconds": round(full1, 3), "tflops": round(flops / full1 / 1e12, 6),
+                              "outputs": "all of C" if rows1 == M else
+                              f"rows 0..{rows1 - 1} of C in {dt1:.1f} s, scaled to all {M} rows (extrapolated)"},
+               "kind": "oracle", **host_cpu()}
 
 
 def run_reference_conv(args, w: dict, oracle, cores: int):
@@ -628,11 +811,11 @@ def run_reference_conv(args, w: dict, oracle, cores: int):
     desc = (f"each step: one image cut to its first {rows} input rows ({y.shape[1]}x{y.shape[2]} output pixels x "
             f"K={cv['K']}), direct binary64 convolution, {cores} OpenMP threads")
     return {
-        "impl": "reference", "metric": "conv2d TFLOP/s (2 N P Q K R S C / device time) and % of GB300 dense BF16 peak, 1 GPU",
+        "impl": "reference", "metric": CONV_METRIC,
         "value": round(value, 6), "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": f"synthetic (seeded SplitMix64, seed {seed})",
-        "config": {"workload": w["desc"], **cv},
+        "vs_baseline": None, "dtype": "f64", "data": conv_data(seed),
+        "config": conv_config(w),
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -671,8 +854,8 @@ def run_reference(args, wname: str, w: dict):
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": f"synthetic (seeded SplitMix64, {w['dist']}, seed {seed})",
-        "config": {"workload": w["desc"], "M": M, "N": N, "K": K, "out": w["out"]},
+        "data": workload_data(w, seed),
+        "config": workload_config(w),
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -775,20 +958,18 @@ def run_gpu_conv(args, wname: str, w: dict):
     mean_ms = total_ms / args.steps
     achieved = flops / (mean_ms * 1e-3) / 1e12
     result = {
-        "metric": "conv2d TFLOP/s (2 N P Q K R S C / device time) and % of GB300 dense BF16 peak, 1 GPU",
+        "metric": CONV_METRIC,
         "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(max_ms / args.steps, 6), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16",
-        "data": f"synthetic (seeded SplitMix64, N(0,1) input, N(0,1)/sqrt(RSC) filter, seed {seed})",
-        "config": {
-            "workload": w["desc"], **{k: v for k, v in cv.items()}, "P": P, "Q": Q, "out": w["out"],
-            "gemm": {"M": cv["N"] * P * Q, "N": cv["K"], "K": cv["R"] * cv["S"] * cv["C"]},
+        "data": conv_data(seed),
+        "config": conv_config(w),
+        "plan": {
             "kernel_variant": g.KERNEL_VARIANTS[plan.kernel_variant], "cluster_size": plan.cluster_size,
             "tile": f"{plan.tile_m}x{plan.tile_n}x{plan.tile_k}", "split_k": plan.split_k,
             "stream_k_tiles": plan.stream_k_tiles, "pct_of_peak": round(100.0 * value / world / peak, 2),
             "peak_tflops": peak, "peak_kind": peak_kind,
-            "l2": f"inputs larger than L2: {copies} rotating sets of {set_bytes / 1e6:.1f} MB vs L2 {l2 / 1e6:.1f} MB",
-            "parallelism": "replicas" if world > 1 else "single GPU",
+            "l2_sets": f"{copies} rotating sets of {set_bytes / 1e6:.1f} MB vs L2 {l2 / 1e6:.1f} MB",
         },
         "roofline": {
             "kernel": f"{KERNEL_NAME}<{plan.cluster_size},{plan.tile_n}> (im2col A)",
@@ -799,6 +980,8 @@ def run_gpu_conv(args, wname: str, w: dict):
         "gpu_launches": (1 + (1 if plan.split_k > 1 else 0)) * args.steps,
         "clocks": clocks_summary(nvml_rows, sampler.summary(t_wall0, t_wall1)),
     }
+    if args.no_e2e:
+        return result, rank
     e2e_steps = min(args.steps, 20)
     hx = torch.from_numpy(x_h.view(np.int16)).view(torch.bfloat16).pin_memory()
     hw = torch.from_numpy(w_h.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -834,9 +1017,26 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="square4096")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    # an ad-hoc GEMM, flags as a library profiler takes them (all of --m --n --k, or none)
+    ap.add_argument("--m", type=int)
+    ap.add_argument("--n", type=int)
+    ap.add_argument("--k", type=int)
+    ap.add_argument("--A", choices=["row", "col"], default="row", help="layout of A (with --m --n --k)")
+    ap.add_argument("--B", choices=["row", "col"], default="col", help="layout of B (with --m --n --k)")
+    ap.add_argument("--C", choices=["bf16", "f32"], default="bf16", help="type of C (with --m --n --k)")
+    ap.add_argument("--split-k", type=int, default=0, help="0: the plan chooses (with --m --n --k)")
+    ap.add_argument("--persistent", type=int, choices=[0, 1], default=1, help="0: one cluster per tile")
+    ap.add_argument("--dist", choices=["normal", "uniform", "int4"], default="normal",
+                    help="input values (with --m --n --k): N(0,1)/sqrt(K), uniform[-1,1)/sqrt(K) or integers")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--sustained-seconds", type=float, default=None,
+                    help="seconds of back-to-back steps after the timed region (default 4; 0: none)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
+    ap.add_argument("--oracle-table", action="store_true",
+                    help="time the oracle alone on the host cores (configs 1-4 in full, all threads, and a "
+                         "one-thread sample); one JSON line per configuration")
     ap.add_argument("--no-stream-k", action="store_true", help="never spread a tail of tiles over the clusters")
     ap.add_argument("--variant", type=int, default=0, choices=[0, 1, 2, 3],
                     help="kernel variant: 0 auto, 1 one-SM 128x256, 2 two-SM 256x256, 3 two-SM 256x128")
@@ -845,6 +1045,20 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    shape = (args.m, args.n, args.k)
+    if any(v is not None for v in shape):
+        if any(v is None or v < 1 for v in shape):
+            ap.error("--m, --n and --k go together, each at least 1")
+        name = f"custom_{args.m}x{args.n}x{args.k}"
+        WORKLOADS[name] = custom_workload(args.m, args.n, args.k, args.A, args.B, args.C, args.split_k,
+                                          args.persistent, args.dist)
+        args.workload = name
+    if args.sustained_seconds is None:
+        args.sustained_seconds = 0.0 if args.all_workloads else 4.0
+    if args.oracle_table:
+        for line in oracle_table():
+            print(json.dumps(line), flush=True)
+        return 0
 
     world, rank, local = dist_env()
     if args.impl == "reference":

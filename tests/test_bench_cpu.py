@@ -63,3 +63,31 @@ def test_source_hash_ignores_comments_only():
     c = "int f(int x) {\n    return x + 2;   // one more\n}\n/* note */\n"
     assert bench._code_only(a) == bench._code_only(b)
     assert bench._code_only(a) != bench._code_only(c)
+
+
+def test_profiler_style_shape_flags():
+    """--m --n --k (with --A --B --C --split-k --persistent) time an ad-hoc GEMM;
+    the reference arm takes the same flags and labels the line with them."""
+    r = _bench("--impl", "reference", "--m", "64", "--n", "48", "--k", "40", "--A", "col", "--B", "row",
+               "--C", "f32", "--split-k", "2", "--persistent", "0", "--steps", "3", "--warmup", "3")
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads([l for l in r.stdout.splitlines() if l.strip()][-1])
+    c = d["config"]
+    assert (c["M"], c["N"], c["K"], c["out"], c["split_k"]) == (64, 48, 40, "f32", 2)
+    assert c["layout_a"] == "column-major" and c["layout_b"] == "row-major"
+    assert c["launch"] == "one cluster per tile"
+    r = _bench("--impl", "reference", "--m", "64", "--steps", "3", "--warmup", "3", timeout=120)
+    assert r.returncode != 0 and "--m, --n and --k go together" in r.stderr
+
+
+def test_both_arms_label_a_workload_alike():
+    """The reference arm's data and config come from the same builders as the
+    GPU arm's, so the two lines name the same workload."""
+    sys.path.insert(0, ROOT)
+    import bench
+    w = bench.WORKLOADS[bench.DEFAULT_WORKLOAD]
+    assert bench.DEFAULT_WORKLOAD == "large" and (w["M"], w["N"], w["K"]) == (16384, 8192, 8192)
+    src = open(os.path.join(ROOT, "bench.py")).read()
+    assert src.count('"config": workload_config(w)') == 2
+    assert src.count('"data": workload_data(w, seed)') == 2
+    assert src.count('"config": conv_config(w)') == 2

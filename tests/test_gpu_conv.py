@@ -163,3 +163,24 @@ def test_conv_fused_bias_relu(oracle_lib):
     D = ep.epilogue(ref.reshape(-1, K), bias=bias, activation="relu")
     tol = ep.tolerance(ref.reshape(-1, K), sabs.reshape(-1, K), bias=bias, activation="relu")
     assert np.all(np.abs(y.reshape(-1, K) - D) <= tol)
+
+
+@pytest.mark.parametrize("name", ["conv3x3_n32_56x56_c256_k256", "conv3x3_n32_28x28_c512_k512"])
+def test_benched_conv_layers_at_full_size(oracle_lib, name):
+    """The two convolutions bench.py times, at full size (N = 32) and in its
+    launch configuration (the plan's own kernel and stream-K tail), with the
+    bench's operands.  Three whole images are checked against the direct
+    convolution: the first, image 17 (whose first GEMM rows share a 256-row
+    tile with the end of image 16) and the last (the last tile row)."""
+    import bench
+    cv = bench.WORKLOADS[name]["conv"]
+    x, w = bench.conv_host_operands(cv, inputs.DEFAULT_SEED + 400)
+    y = run(x, w, "bf16", **_conv_kw(cv))
+    assert y.shape[0] == cv["N"] == 32
+    for n in (0, 17, cv["N"] - 1):
+        ref, sabs = oracle_lib.conv2d(x[n:n + 1], w, **_conv_kw(cv))
+        K = cv["K"]
+        nbad, _, ncanc, detail = check_bf16(y[n].reshape(-1, K), ref.reshape(-1, K), sabs.reshape(-1, K),
+                                            oracle_lib)
+        assert nbad == 0, f"image {n}: {detail}"
+        assert ncanc <= cancellation_cap(ref.size), f"image {n}: {ncanc} entries needed the cancellation clause"

@@ -14,7 +14,7 @@ import pytest
 
 from dense_tensor_core_bf16_gb300 import inputs
 
-from ._parity import bf16_ulp
+from ._parity import bf16_ulp, sample_entries
 from .test_gpu_parity import VARIANTS, from_dev_bf16, operands, to_dev, _ru
 
 torch = pytest.importorskip("torch")
@@ -82,6 +82,12 @@ def check(oracle, A, Bt, C, out, C0_bits, bias, alpha, beta, activation, exact=F
     C_old = oracle.bf16_to_f64(C0_bits)
     ref = ep.epilogue(P, C_old, bias, alpha=alpha, beta=beta, activation=activation)
     tol = ep.tolerance(P, S, C_old, bias, alpha=alpha, beta=beta, activation=activation)
+    compare(oracle, C, out, ref, tol, exact)
+
+
+def compare(oracle, C, out, ref, tol, exact=False):
+    """C (fp32 values or bf16 bit patterns) against the binary64 reference
+    under the epilogue bound ``tol``."""
     if out == "f32":
         got = C.astype(np.float64)
         assert np.all(np.isfinite(got))
@@ -228,3 +234,31 @@ def test_epilogue_argument_errors():
     off = g.gemm_epilogue_t(alpha=1.0, beta=0.0, bias=bias.data_ptr() + 4, activation=0)
     o = g.options(epilogue=__import__("ctypes").pointer(off))
     assert g.gemm_bf16_ex(64, 64, 64, p, 64, p, 64, C.data_ptr(), 64, 0, 1, 0, o, s) == 2
+
+
+def test_benched_residual_bias_gelu_square4096_sampled(oracle_lib):
+    """square4096_residual_bias_gelu exactly as bench.py times it -- 4096^3,
+    C := gelu(A.B + C + bias), bf16 C, the bench's operands and bias, the
+    plan's own choice (the 2-SM kernel with a stream-K tail) -- with a random
+    previous C, checked on sampled entries: every pairing of the tile-edge
+    rows and columns and 6000 random entries, which fall on whole tiles and
+    on stream-K tiles alike."""
+    import bench
+    import dense_tensor_core_bf16_gb300 as g
+    from oracle import epilogue as ep
+    w = bench.WORKLOADS["square4096_residual_bias_gelu"]
+    M, N, K = w["M"], w["N"], w["K"]
+    (A, Bt), seed = bench.make_host_operands(w)
+    bias_bits = inputs.matrix(1, N, dist="normal", seed=seed, stream=8)[0]
+    bias = (bias_bits.astype(np.uint32) << 16).view(np.float32)
+    C0 = inputs.matrix(M, N, dist="normal", seed=seed, stream=7)
+    st, plan = g.gemm_plan(M, N, K)
+    assert st == 0 and plan.stream_k_tiles > 0, "the benched plan has a stream-K tail"
+    C = run(A, Bt, "bf16", C0, bias, alpha=1.0, beta=1.0, activation="gelu")
+    rows, cols = sample_entries(M, N, 6000, seed=5, tile_m=plan.tile_m, tile_n=plan.tile_n)
+    P, S = oracle_lib.gemm_entries(A, Bt, M, N, K, rows, cols)
+    C_old = oracle_lib.bf16_to_f64(C0[rows, cols])[None, :]
+    b = bias[cols].astype(np.float64)
+    ref = ep.epilogue(P[None, :], C_old, b, alpha=1.0, beta=1.0, activation="gelu")
+    tol = ep.tolerance(P[None, :], S[None, :], C_old, b, alpha=1.0, beta=1.0, activation="gelu")
+    compare(oracle_lib, C[rows, cols][None, :], "bf16", ref, tol)
