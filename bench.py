@@ -418,7 +418,7 @@ def run_gpu(args, wname: str, w: dict, cpu_baseline: bool):
     (A_h, Bt_h), seed = make_host_operands(w)
 
     kw = dict(split_k=w["split_k"], non_persistent=w.get("non_persistent", False), kernel_variant=args.variant,
-              no_stream_k=args.no_stream_k)
+              no_stream_k=args.no_stream_k, raster_group_m=args.raster_group)
     epi = w.get("epilogue")
     if epi:
         from dense_tensor_core_bf16_gb300 import inputs
@@ -1038,8 +1038,11 @@ def main(argv=None):
                     help="time the oracle alone on the host cores (configs 1-4 in full, all threads, and a "
                          "one-thread sample); one JSON line per configuration")
     ap.add_argument("--no-stream-k", action="store_true", help="never spread a tail of tiles over the clusters")
-    ap.add_argument("--variant", type=int, default=0, choices=[0, 1, 2, 3],
-                    help="kernel variant: 0 auto, 1 one-SM 128x256, 2 two-SM 256x256, 3 two-SM 256x128")
+    ap.add_argument("--raster-group", type=int, default=0,
+                    help="m-tiles per raster group of the tile order (0: the library's default, 16)")
+    ap.add_argument("--variant", type=int, default=0, choices=[0, 1, 2, 3, 4],
+                    help="kernel variant: 0 auto, 1 one-SM 128x256, 2 two-SM 256x256, 3 two-SM 256x128, "
+                         "4 one-SM 128x64")
     ap.add_argument("--all-workloads", action="store_true",
                     help="run every workload (one JSON line each, no CPU baseline)")
     args = ap.parse_args(argv)

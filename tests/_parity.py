@@ -12,8 +12,10 @@ Tolerances (stated with the workloads of the BF16 GEMM):
              rounding of some value within beta of C_ref:
              RN_bf16(C_ref - beta) <= C <= RN_bf16(C_ref + beta);
     The entries that pass only through that clause are counted, and every
-    check caps the count at cancellation_cap(n) of its n entries: one in
-    10,000, at least 8, the same cap for full and sampled checks;
+    check (full or sampled) caps the count at cancellation_cap(): one in 100
+    of the entries where the clause is wider than one ulp (beta > ulp of
+    RN_bf16(C_ref)), and at least 8.  How many entries that is depends on
+    the inputs' conditioning sum|ab| / |C|, not on the entry count alone;
   * small-integer inputs: bit-exact (every fp32 partial sum is an integer
     below 2^24, so fp32 accumulation is exact in any order);
   * a non-finite output is always a failure.
@@ -27,10 +29,16 @@ F32_REL = 2.0 ** -16
 F32_ABS = 1e-6
 
 
-def cancellation_cap(n: int) -> int:
-    """Largest number of bf16 entries, out of n checked, that may pass only
-    through the accumulation-bound clause (one in 10,000, at least 8)."""
-    return max(8, int(n) // 10000)
+def cancellation_cap(ref: np.ndarray, sabs: np.ndarray, oracle) -> int:
+    """Largest number of bf16 entries that may pass only through the
+    accumulation-bound clause: one in 100 of the entries where that clause
+    admits more than one ulp (beta > ulp of RN_bf16(C_ref)), at least 8.
+    (Measured on GB300: about 1 in 7,000 such entries for the 4096^3 GEMM,
+    1 in 600 for the benched 3x3 convolutions.)"""
+    r = oracle.bf16_to_f64(oracle.f64_to_bf16(np.asarray(ref, dtype=np.float64)))
+    beta = F32_REL * np.asarray(sabs, dtype=np.float64) + F32_ABS
+    eligible = int(np.count_nonzero(beta > bf16_ulp(np.abs(r))))
+    return max(8, eligible // 100)
 
 
 def check_f32(C: np.ndarray, ref: np.ndarray, sabs: np.ndarray):
