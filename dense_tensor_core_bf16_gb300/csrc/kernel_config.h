@@ -45,8 +45,7 @@ enum Variant : int {
     VARIANT_1SM_128x256 = 1,
     VARIANT_2SM_256x256 = 2,
     VARIANT_2SM_256x128 = 3,
-    VARIANT_1SM_128x64 = 4,
-    VARIANT_COUNT = 5
+    VARIANT_COUNT = 4
 };
 
 GEMM_HD constexpr int pow2_at_least(int x, int p = 32) { return p >= x ? p : pow2_at_least(x, p * 2); }
@@ -81,7 +80,6 @@ GEMM_HD constexpr VariantInfo make_variant(int cg, int bn, int tk) {
 GEMM_HD constexpr VariantInfo variant_info(int v) {
     return v == VARIANT_2SM_256x256 ? make_variant(2, 256, 128)
          : v == VARIANT_2SM_256x128 ? make_variant(2, 128, 64)
-         : v == VARIANT_1SM_128x64  ? make_variant(1, 64, 64)
                                     : make_variant(1, 256, 64);
 }
 
@@ -89,8 +87,6 @@ static_assert(variant_info(VARIANT_1SM_128x256).stages == 4, "1-SM 128x256: four
 static_assert(variant_info(VARIANT_2SM_256x256).stages == 3, "2-SM 256x256: three 64 KiB stages");
 static_assert(variant_info(VARIANT_2SM_256x256).smem <= SMEM_LIMIT, "fits");
 static_assert(variant_info(VARIANT_2SM_256x128).smem <= SMEM_LIMIT, "fits");
-static_assert(variant_info(VARIANT_1SM_128x64).stages == 8, "1-SM 128x64: eight 24 KiB stages");
-static_assert(variant_info(VARIANT_1SM_128x64).smem <= SMEM_LIMIT, "fits");
 
 constexpr int DEFAULT_RASTER_GROUP_M = 16;
 constexpr int DEFAULT_TIMEOUT_MS = 4000;

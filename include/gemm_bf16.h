@@ -67,10 +67,6 @@ typedef enum {
 
 /* Kernel variants.  A tile is the block of C one work unit produces.
  *   1SM_128x256: one CTA per tile, tcgen05.mma.cta_group::1 with M = 128.
- *   1SM_128x64: the same with 64-column tiles (N = 64 per MMA): four times
- *     the work units of 1SM_128x256 along N, so a few tiles with a long K
- *     split into fewer slices (and fewer fp32 partial bytes) for the same
- *     number of CTAs.
  *   2SM_256x256, 2SM_256x128: a cluster of two CTAs on a pair of SMs per
  *     tile, tcgen05.mma.cta_group::2 with M = 256; each CTA stages its own
  *     128 rows of A and half of the tile's columns of B, and holds its 128
@@ -84,8 +80,7 @@ typedef enum {
     GEMM_KERNEL_AUTO = 0,
     GEMM_KERNEL_1SM_128x256 = 1,
     GEMM_KERNEL_2SM_256x256 = 2,
-    GEMM_KERNEL_2SM_256x128 = 3,
-    GEMM_KERNEL_1SM_128x64 = 4
+    GEMM_KERNEL_2SM_256x128 = 3
 } gemm_kernel_variant_t;
 
 /* Which resource sets the number of resident CTAs per SM. */
