@@ -780,6 +780,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     load_c_chunk(col_base, s0 & 1u);
                 }
                 if (owner_fast) prefetch(0);
+                float b_next = p.bias && col_base + lane < p.N ? __ldg(p.bias + col_base + lane) : 0.0f;
 #pragma unroll 1
                 for (int c = 0; c < n_chunks; ++c) {
                     const int col0 = col_base + c * 32;
@@ -834,7 +835,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     // the chunk's 32 bias values, one per lane (one coalesced load),
                     // handed to every lane by shuffles below
-                    const float b_lane = p.bias && col0 + lane < p.N ? __ldg(p.bias + col0 + lane) : 0.0f;
+                    const float b_lane = b_next;
+                    if (c + 1 < n_chunks)
+                        b_next = p.bias && col0 + 32 + lane < p.N ? __ldg(p.bias + col0 + 32 + lane) : 0.0f;
                     uint32_t r[32];
                     __syncwarp();
                     ptx::tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r);
