@@ -33,7 +33,8 @@ __all__ = [
 GEMM_ROW_MAJOR, GEMM_COL_MAJOR = 0, 1
 GEMM_OUT_F32, GEMM_OUT_BF16 = 0, 1
 GEMM_KERNEL_AUTO, GEMM_KERNEL_1SM_128x256, GEMM_KERNEL_2SM_256x256, GEMM_KERNEL_2SM_256x128 = 0, 1, 2, 3
-KERNEL_VARIANTS = {1: "1sm_128x256", 2: "2sm_256x256", 3: "2sm_256x128"}
+GEMM_KERNEL_1SM_128x128 = 4
+KERNEL_VARIANTS = {1: "1sm_128x256", 2: "2sm_256x256", 3: "2sm_256x128", 4: "1sm_128x128"}
 STATUS_NAMES = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_VALUE", 2: "GEMM_ERR_MISALIGNED", 3: "GEMM_ERR_NOT_SUPPORTED",
                 4: "GEMM_ERR_NO_DEVICE", 5: "GEMM_ERR_OUT_OF_MEMORY", 6: "GEMM_ERR_LAUNCH",
                 7: "GEMM_ERR_DEVICE_TIMEOUT"}

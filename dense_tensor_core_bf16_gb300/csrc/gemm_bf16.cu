@@ -1165,6 +1165,7 @@ KernelFn kernel_fn(int variant) {
     switch (variant) {
         case VARIANT_2SM_256x256: return gemm_bf16_kernel<2, 256, 128>;
         case VARIANT_2SM_256x128: return gemm_bf16_kernel<2, 128, 64>;
+        case VARIANT_1SM_128x128: return gemm_bf16_kernel<1, 128, 64>;
         default: return gemm_bf16_kernel<1, 256, 64>;
     }
 }

@@ -45,7 +45,8 @@ enum Variant : int {
     VARIANT_1SM_128x256 = 1,
     VARIANT_2SM_256x256 = 2,
     VARIANT_2SM_256x128 = 3,
-    VARIANT_COUNT = 4
+    VARIANT_1SM_128x128 = 4,
+    VARIANT_COUNT = 5
 };
 
 GEMM_HD constexpr int pow2_at_least(int x, int p = 32) { return p >= x ? p : pow2_at_least(x, p * 2); }
@@ -80,6 +81,7 @@ GEMM_HD constexpr VariantInfo make_variant(int cg, int bn, int tk) {
 GEMM_HD constexpr VariantInfo variant_info(int v) {
     return v == VARIANT_2SM_256x256 ? make_variant(2, 256, 128)
          : v == VARIANT_2SM_256x128 ? make_variant(2, 128, 64)
+         : v == VARIANT_1SM_128x128 ? make_variant(1, 128, 64)
                                     : make_variant(1, 256, 64);
 }
 

@@ -122,6 +122,20 @@ int choose_variant(int64_t M, int64_t N, int64_t K, int requested, int split_k, 
     // tiles spread it over more SMs and shorten each CTA's epilogue
     // (measured: 512^3 7.8 against 9.2 us, 1024^3 10.4 against 11.4 us).
     if (split_k <= 1 && K < AUTO_SPLIT_MIN_K && cdiv(M, 256) * cdiv(N, 128) * 2 <= c2) return VARIANT_2SM_256x128;
+    // One tile row (M <= 128) with a long K: 128 x 128 tiles give twice the
+    // work units of 128 x 256 tiles, so the split that fills the SMs has half
+    // the slices, each CTA stores half a partial tile, and the combine reads
+    // half as much; taken when every unit of the split (given, or the plan's
+    // own for these tiles) fits in one wave.  Measured at 128 x 256 x 65536:
+    // split 74 15.9 against 19.2 us, 32 18.0 against 20.1, 1 324 against
+    // 385, the plan's own 76 at 15.9 against 148 slices of 128 x 256 at 16.4;
+    // equal at 8.
+    if (M <= 128 && N > 128 && K >= AUTO_SPLIT_MIN_K) {
+        const int64_t t4 = cdiv(N, 128);
+        const int64_t s4 = split_k > 0 ? (split_k < kb ? split_k : kb)
+                                       : choose_split(t4, static_cast<int>(kb), static_cast<int>(c1), 0, K);
+        if (t4 * s4 <= c1) return VARIANT_1SM_128x128;
+    }
     const int64_t t1 = cdiv(M, 128) * cdiv(N, 256), t2 = cdiv(M, 256) * cdiv(N, 256);
     int64_t w1, w2;
     if (split_k > 1) {   // a given split: rounds of work units times k-tiles per unit

@@ -67,6 +67,10 @@ typedef enum {
 
 /* Kernel variants.  A tile is the block of C one work unit produces.
  *   1SM_128x256: one CTA per tile, tcgen05.mma.cta_group::1 with M = 128.
+ *   1SM_128x128: the same with 128-column tiles (N = 128 per MMA), for a
+ *     single row of tiles (M <= 128) with a long K: twice the work units of
+ *     1SM_128x256, so the split that fills the SMs takes half the slices and
+ *     half the fp32 partial bytes per CTA.
  *   2SM_256x256, 2SM_256x128: a cluster of two CTAs on a pair of SMs per
  *     tile, tcgen05.mma.cta_group::2 with M = 256; each CTA stages its own
  *     128 rows of A and half of the tile's columns of B, and holds its 128
@@ -80,7 +84,8 @@ typedef enum {
     GEMM_KERNEL_AUTO = 0,
     GEMM_KERNEL_1SM_128x256 = 1,
     GEMM_KERNEL_2SM_256x256 = 2,
-    GEMM_KERNEL_2SM_256x128 = 3
+    GEMM_KERNEL_2SM_256x128 = 3,
+    GEMM_KERNEL_1SM_128x128 = 4
 } gemm_kernel_variant_t;
 
 /* Which resource sets the number of resident CTAs per SM. */
@@ -248,7 +253,10 @@ gemm_status_t gemm_occupancy(const gemm_kernel_desc_t *kern, const gemm_device_d
  *     k-tiles long);
  *   - otherwise one cluster per tile.
  * With the plan's own variant, a small GEMM (256 x 128 pair tiles filling at
- * most half the resident pairs, K < 2048) runs on the 256 x 128 pair kernel.
+ * most half the resident pairs, K < 2048) runs on the 256 x 128 pair kernel,
+ * and a single row of tiles (M <= 128, N > 128) with K >= 2048 runs on the
+ * 128 x 128 single-CTA kernel when all its work units (tiles times the split
+ * asked for, or the plan's own split for those tiles) fit in one wave.
  * Handing partial tiles between CTAs costs a roughly fixed few to 25 us on
  * GB300 (fp32 partials through L2 and a fix-up or a combine kernel), so the
  * plan spreads or splits the work only where the longer K repays it.

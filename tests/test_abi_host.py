@@ -106,8 +106,8 @@ def _plan(M, N, K, split=1, persistent=1, d=None, regs=64, out=g.GEMM_OUT_BF16, 
 WORKLOADS = [(256, 256, 256), (4096, 4096, 4096), (4095, 4096, 4096), (4097, 4096, 4096),
              (4096, 4096, 4088), (4096, 4104, 4096), (3968, 4096, 4096), (16384, 8192, 8192),
              (128, 256, 65536), (1, 1, 1), (129, 257, 65)]
-TILES = {1: (128, 256, 1), 2: (256, 256, 2), 3: (256, 128, 2)}
-TILE_K = {1: 64, 2: 128, 3: 64}
+TILES = {1: (128, 256, 1), 2: (256, 256, 2), 3: (256, 128, 2), 4: (128, 128, 1)}
+TILE_K = {1: 64, 2: 128, 3: 64, 4: 64}
 
 
 def test_kernel_desc_without_a_device():
@@ -118,7 +118,7 @@ def test_kernel_desc_without_a_device():
         assert k.tmem_cols_per_cta == 2 * tn      # two accumulators of tn fp32 columns (a power of two)
 
 
-@pytest.mark.parametrize("variant", [1, 2, 3])
+@pytest.mark.parametrize("variant", [1, 2, 3, 4])
 @pytest.mark.parametrize("S,mac", [(148, 0), (152, 0), (152, 72)])
 @pytest.mark.parametrize("shape", WORKLOADS)
 def test_plan_matches_oracle_closed_forms(shape, S, mac, variant):
@@ -221,14 +221,14 @@ def test_plan_split_k_clamped_and_auto():
 
 def test_plan_auto_variant():
     """Equal balanced work (4096^3: 216 k-tiles per cluster either way) goes to
-    the pair kernel; M = 128 with a long K goes to the single-CTA kernel
-    (ceil(1024/152) = 7 k-tiles per CTA against ceil(1024/76) = 14 per pair)."""
+    the pair kernel; M = 128 with a long K goes to the 128 x 128 single-CTA
+    kernel: two tiles, the plan's own split 152 / 2 = 76, 152 CTAs in one wave."""
     st, p = g.gemm_plan_for_device(4096, 4096, 4096, 0, 1, 1, None, dev(), kern(2))
     assert st == 0 and p.kernel_variant == 2
     st, _ = g.gemm_plan_for_device(4096, 4096, 4096, 0, 1, 1, None, dev(), kern(1))
     assert st == 1     # a footprint that does not match the variant
-    st, p = g.gemm_plan_for_device(128, 256, 65536, 0, 1, 0, None, dev(), kern(1))
-    assert st == 0 and p.kernel_variant == 1 and p.split_k == 152
+    st, p = g.gemm_plan_for_device(128, 256, 65536, 0, 1, 0, None, dev(), kern(4))
+    assert st == 0 and p.kernel_variant == 4 and p.split_k == 76
     for shape in [(16384, 8192, 8192), (4097, 4096, 4096), (3968, 4096, 4096), (2048, 2048, 1024),
                   (1536, 1536, 1536), (512, 512, 4096)]:
         st, p = g.gemm_plan_for_device(*shape, 0, 1, 1, None, dev(), kern(2))
@@ -238,6 +238,28 @@ def test_plan_auto_variant():
     for shape in [(256, 256, 256), (512, 512, 512), (1024, 1024, 1024), (1024, 1024, 2047)]:
         st, p = g.gemm_plan_for_device(*shape, 0, 1, 1, None, dev(), kern(3))
         assert st == 0 and p.kernel_variant == 3, shape
+
+
+@pytest.mark.parametrize("shape,split,want_variant,want_split", [
+    ((128, 256, 65536), 0, 4, 76),     # the plan's own split for two 128 x 128 tiles
+    ((128, 256, 65536), 74, 4, 74),    # 2 x 74 = 148 units: one wave
+    ((128, 256, 65536), 32, 4, 32),
+    ((128, 256, 65536), 8, 4, 8),
+    ((128, 256, 65536), 1, 4, 1),      # two CTAs instead of one
+    ((128, 256, 65536), 148, 1, 148),  # 2 x 148 > 152: the 128 x 256 kernel, one wave of 148
+    ((100, 300, 8192), 0, 4, 32),      # ragged: three 128 x 128 tiles, 128 k-tiles at 4 per slice
+    ((129, 256, 65536), 0, 2, 76),     # two tile rows: the rule does not apply (the pair kernel)
+    ((128, 128, 65536), 0, 1, 152),    # N <= 128: one tile either way
+    ((128, 256, 1024), 1, 3, 1),       # short K: the small-GEMM pair kernel
+])
+def test_plan_one_tile_row_with_a_long_k(shape, split, want_variant, want_split):
+    """The automatic variant for a single row of tiles (M <= 128, N > 128,
+    K >= 2048): the 128 x 128 single-CTA kernel whenever every work unit of
+    the split fits in one wave of the S = 152 SMs."""
+    M, N, K = shape
+    o = g.options(split_k=split)
+    st, p = g.gemm_plan_for_device(M, N, K, 0, 1, 0, o, dev(), kern(want_variant))
+    assert st == 0 and p.kernel_variant == want_variant and p.split_k == want_split, (p.kernel_variant, p.split_k)
 
 
 def _want_stream_k(T, C, K, KB, force=False, variant=2):

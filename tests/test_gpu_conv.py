@@ -129,7 +129,7 @@ def test_conv_stream_k(oracle_lib):
     assert np.array_equal(y, y2), "stream-K result differs run to run"
 
 
-@pytest.mark.parametrize("variant", [0, 1, 2, 3])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4])
 def test_conv_one_by_one_equals_the_gemm_bitwise(variant):
     """A 1 x 1 convolution is the GEMM of pixels and filters: under the same
     kernel variant the plan and the order of every sum are the same."""
@@ -142,7 +142,7 @@ def test_conv_one_by_one_equals_the_gemm_bitwise(variant):
     assert np.array_equal(yc.reshape(N * H * W, K), yg)
 
 
-@pytest.mark.parametrize("variant", [1, 2, 3])
+@pytest.mark.parametrize("variant", [1, 2, 3, 4])
 @pytest.mark.parametrize("case", CASES, ids=IDS)
 def test_conv_every_variant_exact(oracle_lib, case, variant):
     x, w = conv_operands(*(case[k] for k in "N H W C K R S".split()), "int4", SEED + 7)

@@ -129,7 +129,7 @@ SMALL_SHAPES = [
 ]
 
 
-VARIANTS = [1, 2, 3]   # 1-SM 128x256, 2-SM 256x256, 2-SM 256x128
+VARIANTS = [1, 2, 3, 4]   # 1-SM 128x256, 2-SM 256x256, 2-SM 256x128, 1-SM 128x128
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
