@@ -734,7 +734,7 @@ def cpu_oracle_baseline(A_h, Bt_h, M, N, K, target_s: float):
     import oracle
     oracle.build()
     cores = oracle.max_threads()
-    oracle.gemm(A_h[:cores], Bt_h, cores, N, K, with_abs=False)      # start the thread pool
+    oracle.gemm(A_h[:cores], Bt_h, cores, N, K, with_abs=False, threads=cores)   # start the thread pool
     rows, dt = _time_oracle_rows(A_h, Bt_h, M, N, K, target_s, cores)
     rows1, dt1 = _time_oracle_rows(A_h, Bt_h, M, N, K, target_s / 3.0, 1)
     return {"value": round(2.0 * rows * N * K / dt / 1e12, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
@@ -759,9 +759,11 @@ def oracle_table(one_thread_budget_s: float = 4.0):
         w = WORKLOADS[name]
         (A_h, Bt_h), seed = make_host_operands(w)
         M, N, K = w["M"], w["N"], w["K"]
-        oracle.gemm(A_h[:min(M, cores)], Bt_h, min(M, cores), N, K, with_abs=False)   # thread pool up
+        # the thread count is passed every time: the OpenMP runtime keeps the
+        # last count it was given, and the one-thread timing below sets 1
+        oracle.gemm(A_h[:min(M, cores)], Bt_h, min(M, cores), N, K, with_abs=False, threads=cores)   # pool up
         t = time.perf_counter()
-        oracle.gemm(A_h, Bt_h, M, N, K, with_abs=False)
+        oracle.gemm(A_h, Bt_h, M, N, K, with_abs=False, threads=cores)
         dt_all = time.perf_counter() - t
         rows1, dt1 = _time_oracle_rows(A_h, Bt_h, M, N, K, one_thread_budget_s, 1)
         full1 = dt1 * M / rows1
