@@ -1041,7 +1041,7 @@ def main(argv=None):
                          "one-thread sample); one JSON line per configuration")
     ap.add_argument("--no-stream-k", action="store_true", help="never spread a tail of tiles over the clusters")
     ap.add_argument("--raster-group", type=int, default=0,
-                    help="m-tiles per raster group of the tile order (0: the library's default, 16)")
+                    help="m-tiles per raster group of the tile order (0: the library's default)")
     ap.add_argument("--variant", type=int, default=0, choices=[0, 1, 2, 3, 4],
                     help="kernel variant: 0 auto, 1 one-SM 128x256, 2 two-SM 256x256, 3 two-SM 256x128, "
                          "4 one-SM 128x128")

@@ -91,6 +91,8 @@ static_assert(variant_info(VARIANT_2SM_256x256).smem <= SMEM_LIMIT, "fits");
 static_assert(variant_info(VARIANT_2SM_256x128).smem <= SMEM_LIMIT, "fits");
 
 constexpr int DEFAULT_RASTER_GROUP_M = 16;
+constexpr int MANY_WAVES = 8;                  // tiles >= this many waves of clusters ...
+constexpr int MANY_WAVES_RASTER_GROUP_M = 8;   // ... take raster groups of 8 m-tiles
 constexpr int DEFAULT_TIMEOUT_MS = 4000;
 // The default limit also grows with the longest stretch of main loop a single
 // wait can span (the epilogue's wait for a whole unit's accumulator, a

@@ -202,7 +202,8 @@ typedef struct {
 typedef struct {
     int split_k;                 /* 0: the plan chooses; 1: off; >1: clamped to [1, k_tiles] */
     int non_persistent;          /* 1: one CTA per work unit (grid G) instead of a persistent grid */
-    int raster_group_m;          /* m-tiles per raster group for L2 reuse; 0: default (16) */
+    int raster_group_m;          /* m-tiles per raster group for L2 reuse; 0: default (8 when the tiles
+                                    make at least eight waves of the resident clusters, else 16) */
     void *mainloop_done_event;   /* cudaEvent_t or NULL: recorded on the stream after the main
                                     kernel, before the split-K combine kernel */
     int timeout_ms;              /* per-wait device time limit; 0: default (4000 ms plus 8 us for
