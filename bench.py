@@ -565,7 +565,7 @@ def run_gpu(args, wname: str, w: dict, cpu_baseline: bool):
             "occupancy_limiter": g.LIMITERS[plan.occupancy_limiter],
             "eta_wave": round(plan.eta_wave, 5), "eta_pad": round(plan.eta_pad, 5),
             "stream_k_tiles": plan.stream_k_tiles, "dp_tiles": plan.dp_tiles,
-            "eta_stream_k": round(plan.eta_stream_k, 5),
+            "eta_stream_k": round(plan.eta_stream_k, 5), "raster_group_m": plan.raster_group_m,
             "pct_of_peak": round(100.0 * value / world / peak, 2), "peak_tflops": peak, "peak_kind": peak_kind,
             "l2_sets": f"{copies} rotating operand sets of {set_bytes / 1e6:.1f} MB "
                        f"({copies * set_bytes / 1e6:.0f} MB) vs L2 {l2 / 1e6:.1f} MB",

@@ -70,7 +70,8 @@ class gemm_plan_t(ctypes.Structure):
         [(n, ctypes.c_double) for n in ("eta_wave", "eta_pad", "flops")] + \
         [("smem_bytes", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64), ("tmem_cols", ctypes.c_int),
          ("kernel_variant", ctypes.c_int), ("cluster_size", ctypes.c_int), ("resident_ctas", ctypes.c_int64),
-         ("stream_k_tiles", ctypes.c_int64), ("dp_tiles", ctypes.c_int64), ("eta_stream_k", ctypes.c_double)]
+         ("stream_k_tiles", ctypes.c_int64), ("dp_tiles", ctypes.c_int64), ("eta_stream_k", ctypes.c_double),
+         ("raster_group_m", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         d = {n: getattr(self, n) for n, _ in self._fields_}

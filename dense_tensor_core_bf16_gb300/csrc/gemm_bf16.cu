@@ -1573,13 +1573,7 @@ gemm_status_t launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_
     p.tiles_n = static_cast<int>((N + vi.bn - 1) / vi.bn);
     p.k_tiles = plan.k_tiles;
     p.split_k = plan.split_k;
-    // Raster groups of 16 m-tiles; with at least eight waves of tiles, groups
-    // of 8: the 76 tiles in flight then span about 8 m-tiles and 10 n-tiles
-    // instead of 16 and 5, fewer operand bytes per wave (at 16384 x 8192 x
-    // 8192, 2.16 against 2.59 GB read from DRAM, about 1 % faster).
-    p.group_m = o.raster_group_m > 0                          ? o.raster_group_m
-              : plan.tiles >= MANY_WAVES * (plan.launch_ctas / vi.cta_group) ? MANY_WAVES_RASTER_GROUP_M
-                                                                : DEFAULT_RASTER_GROUP_M;
+    p.group_m = plan.raster_group_m;
     p.num_units = plan.tiles * plan.split_k;
     p.out = C;
     p.ld_out = ldc;

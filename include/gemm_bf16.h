@@ -165,6 +165,9 @@ typedef struct {
     int64_t dp_tiles;            /* tiles computed whole, one cluster each */
     double eta_stream_k;         /* with a stream-K tail: ideal / actual per-cluster work
                                     (tiles*k_tiles/clusters over the largest share); 0 without */
+    int raster_group_m;          /* m-tiles per raster group of the tile order: the option's value, or
+                                    8 when the tiles make at least eight waves of the resident
+                                    clusters on a persistent grid, else 16 */
 } gemm_plan_t;
 
 /* Elementwise work fused into the store of C (gemm_bf16_ex with

@@ -321,6 +321,19 @@ def test_plan_automatic_split_rule(shape, variant, want):
     assert p.split_k == want and p.stream_k_tiles == 0
 
 
+def test_plan_raster_group():
+    """Raster groups of 8 m-tiles when the tiles make at least eight waves of
+    the resident clusters on a persistent grid, else 16; an option wins."""
+    assert _plan(16384, 8192, 8192, split=0, variant=2, mac=76).raster_group_m == 8    # 2048 tiles >= 8 x 76
+    assert _plan(8192, 4864, 4096, split=0, variant=2, mac=76).raster_group_m == 8     # 32 x 19 = 608 tiles
+    assert _plan(8192, 4608, 4096, split=0, variant=2, mac=76).raster_group_m == 16    # 32 x 18 = 576 tiles
+    assert _plan(4096, 4096, 4096, split=0, variant=2, mac=76).raster_group_m == 16
+    assert _plan(16384, 8192, 8192, split=0, variant=2, mac=76, persistent=0).raster_group_m == 16
+    o = g.options(split_k=0, kernel_variant=2, raster_group_m=5)
+    st, p = g.gemm_plan_for_device(16384, 8192, 8192, 0, 1, 1, o, dev(), kern(2, 64, 76))
+    assert st == 0 and p.raster_group_m == 5
+
+
 def test_plan_stream_k_hand_values():
     """4096^3 on 76 pairs of 256x256 tiles with 128-wide k-tiles: T = 256,
     256 mod 76 = 28, a tail of 104 tiles (3328 k-iterations, 43.8 per
