@@ -34,7 +34,6 @@ from __future__ import annotations
 import argparse
 import ctypes
 import datetime as _dt
-import glob
 import hashlib
 import json
 import math
