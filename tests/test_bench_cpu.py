@@ -91,3 +91,33 @@ def test_both_arms_label_a_workload_alike():
     assert src.count('"config": workload_config(w)') == 2
     assert src.count('"data": workload_data(w, seed)') == 2
     assert src.count('"config": conv_config(w)') == 2
+
+
+def test_conv_labels_agree_with_the_library():
+    """The conv line's P, Q (the reference arm computes them without a GPU)
+    agree with the library's own gemm_conv2d_out_dims for every benched
+    convolution."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import dense_tensor_core_bf16_gb300 as g
+    for name, w in bench.WORKLOADS.items():
+        cv = w.get("conv")
+        if not cv:
+            continue
+        d = g.gemm_conv2d_desc_t(N=cv["N"], H=cv["H"], W=cv["W"], C=cv["C"], K=cv["K"], R=cv["R"], S=cv["S"],
+                                 pad_h=cv["pad"][0], pad_w=cv["pad"][1], stride_h=cv["stride"][0],
+                                 stride_w=cv["stride"][1], dil_h=cv["dil"][0], dil_w=cv["dil"][1])
+        st, P, Q = g.gemm_conv2d_out_dims(d)
+        assert st == 0 and (P, Q) == bench.conv_out_dims(cv), name
+        c = bench.conv_config(w)
+        assert c["gemm"] == {"M": cv["N"] * P * Q, "N": cv["K"], "K": cv["R"] * cv["S"] * cv["C"]}
+
+
+def test_custom_workload_descriptor():
+    sys.path.insert(0, ROOT)
+    import bench
+    w = bench.custom_workload(300, 520, 264, "col", "row", "f32", 3, 0, "int4")
+    assert (w["M"], w["N"], w["K"], w["out"], w["split_k"]) == (300, 520, 264, "f32", 3)
+    assert w["a_col"] and w["b_row"] and w["non_persistent"] and not w["scaled"]
+    c = bench.workload_config(w)
+    assert c["layout_a"] == "column-major" and c["layout_b"] == "row-major" and c["launch"] == "one cluster per tile"
