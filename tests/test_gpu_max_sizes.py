@@ -81,7 +81,7 @@ def bias_values(cols) -> np.ndarray:
     return (np.asarray(cols) % 5 - 2).astype(np.float64)
 
 
-@pytest.mark.parametrize("variant", [0, 1, 3])
+@pytest.mark.parametrize("variant", [0, 1, 3, 4])
 @pytest.mark.parametrize("out", [torch.bfloat16, torch.float32])
 def test_c_past_2_31_elements(oracle_lib, out, variant):
     import dense_tensor_core_bf16_gb300 as g

@@ -178,9 +178,11 @@ def test_non_persistent_matches_persistent_bitwise(oracle_lib, variant):
 #  v2 1792x1536x2048: 7x6 = 42 tiles, all spread (32 k-tiles over ~18-iteration shares: 2-3 clusters per tile)
 #  v2 3328x3072x512: 13x12 = 156 tiles = 76 whole + a tail of 80
 #  v1 1280x2048x2048: 10x8 = 80 tiles on 152 CTAs, all spread
-#  v1/v2/v3 1800x1500x2000: ragged in every dimension
+#  v1/v2/v3/v4 1800x1500x2000: ragged in every dimension
+#  v4 1280x1024x2048: 10x8 = 80 tiles of 128x128 on 152 CTAs, all spread
 SK_CASES = [(2, (1792, 1536, 2048)), (2, (3328, 3072, 512)), (1, (1280, 2048, 2048)),
-            (1, (1800, 1500, 2000)), (2, (1800, 1500, 2000)), (3, (1800, 1500, 2000))]
+            (1, (1800, 1500, 2000)), (2, (1800, 1500, 2000)), (3, (1800, 1500, 2000)),
+            (4, (1800, 1500, 2000)), (4, (1280, 1024, 2048))]
 
 
 @pytest.mark.parametrize("variant,shape", SK_CASES)
@@ -242,7 +244,7 @@ def test_padded_leading_dimensions_and_guard_band(oracle_lib):
     assert check_f32(body[:, :N], ref, sabs)[0] == 0
 
 
-@pytest.mark.parametrize("variant", [1, 2, 3])
+@pytest.mark.parametrize("variant", [1, 2, 3, 4])
 @pytest.mark.parametrize("out", ["f32", "bf16"])
 @pytest.mark.parametrize("N", [1, 3, 7, 13, 259, 299, 301])
 def test_columns_past_n_keep_their_contents(oracle_lib, variant, out, N):
