@@ -123,18 +123,42 @@ int choose_variant(int64_t M, int64_t N, int64_t K, int requested, int split_k, 
     // (measured: 512^3 7.8 against 9.2 us, 1024^3 10.4 against 11.4 us).
     if (split_k <= 1 && K < AUTO_SPLIT_MIN_K && cdiv(M, 256) * cdiv(N, 128) * 2 <= c2) return VARIANT_2SM_256x128;
     // One tile row (M <= 128) with a long K: 128 x 128 tiles give twice the
-    // work units of 128 x 256 tiles, so the split that fills the SMs has half
-    // the slices, each CTA stores half a partial tile, and the combine reads
-    // half as much; taken when every unit of the split (given, or the plan's
-    // own for these tiles) fits in one wave.  Measured at 128 x 256 x 65536:
-    // split 74 15.9 against 19.2 us, 32 18.0 against 20.1, 1 324 against
-    // 385, the plan's own 76 at 15.9 against 148 slices of 128 x 256 at 16.4;
-    // equal at 8.
+    // work units of 128 x 256 tiles, so a split that fills the SMs takes half
+    // the slices, each CTA stores half a partial tile and the combine reads
+    // half as much -- but each tile of the row reads A again.  The two plans
+    // (each with its own split: the one asked for, or the plan's own) are
+    // compared by an estimate of their time: the operand bytes one CTA
+    // streams at about 100 GB/s per SM, at least the unique operand bytes at
+    // about 6.8 TB/s, plus, when K is split, about 6 us (the combine kernel,
+    // a kernel boundary) and the fp32 partial tiles written and read back at
+    // about 2 TB/s.  Within 0.5 us the plan with more work units wins.  The
+    // 128 x 128 plan must fit in one wave.  (Measured, us, 128 x 128 against
+    // 128 x 256 or the pair kernel: 128 x 256 x 65536 with the plan's split
+    // 15.9 against 16.4, split 74 15.9 against 19.2, split 1 324 against 385;
+    // 128 x 1024 x 4096 11.3 against 12.4; 100 x 3000 x 2048 15.1 against
+    // 16.6; the other way, where the 128 x 128 plan cannot split:
+    // 64 x 4096 x 4096 24.8 against 19.9, 128 x 8192 x 8192 46.7 against
+    // 46.0.)
     if (M <= 128 && N > 128 && K >= AUTO_SPLIT_MIN_K) {
-        const int64_t t4 = cdiv(N, 128);
-        const int64_t s4 = split_k > 0 ? (split_k < kb ? split_k : kb)
-                                       : choose_split(t4, static_cast<int>(kb), static_cast<int>(c1), 0, K);
-        if (t4 * s4 <= c1) return VARIANT_1SM_128x128;
+        const int64_t t4 = cdiv(N, 128), t1 = cdiv(N, 256);
+        auto split_for = [&](int64_t tiles) -> int64_t {
+            return split_k > 0 ? (split_k < kb ? split_k : kb)
+                               : choose_split(tiles, static_cast<int>(kb), static_cast<int>(c1), 0, K);
+        };
+        const int64_t s4 = split_for(t4), s1 = split_for(t1);
+        const double unique_us = 2.0 * static_cast<double>(M * K + N * K) / 6.8e6;
+        auto estimate_us = [&](int64_t bn, int64_t tiles, int64_t s) {
+            const int64_t units = tiles * s;
+            const int64_t waves = cdiv(units, c1);
+            const double cta_bytes = (128.0 + static_cast<double>(bn)) * 2.0 * TILE_K *
+                                     static_cast<double>(cdiv(kb, s) * waves);
+            const double stream_us = cta_bytes / 1.0e5;
+            const double split_us = s > 1 ? 6.0 + static_cast<double>(units) * 128.0 * bn * 4.0 / 2.0e6 : 0.0;
+            return (stream_us > unique_us ? stream_us : unique_us) + split_us;
+        };
+        const double e4 = estimate_us(128, t4, s4), e1 = estimate_us(256, t1, s1);
+        const bool tie = e4 - e1 < 0.5 && e1 - e4 < 0.5;
+        if (t4 * s4 <= c1 && (tie ? t4 * s4 >= t1 * s1 : e4 < e1)) return VARIANT_1SM_128x128;
     }
     const int64_t t1 = cdiv(M, 128) * cdiv(N, 256), t2 = cdiv(M, 256) * cdiv(N, 256);
     int64_t w1, w2;

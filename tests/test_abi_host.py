@@ -241,21 +241,32 @@ def test_plan_auto_variant():
 
 
 @pytest.mark.parametrize("shape,split,want_variant,want_split", [
-    ((128, 256, 65536), 0, 4, 76),     # the plan's own split for two 128 x 128 tiles
+    ((128, 256, 65536), 0, 4, 76),     # the plan's own split for two 128 x 128 tiles: 152 units
     ((128, 256, 65536), 74, 4, 74),    # 2 x 74 = 148 units: one wave
     ((128, 256, 65536), 32, 4, 32),
     ((128, 256, 65536), 8, 4, 8),
     ((128, 256, 65536), 1, 4, 1),      # two CTAs instead of one
     ((128, 256, 65536), 148, 1, 148),  # 2 x 148 > 152: the 128 x 256 kernel, one wave of 148
+    ((128, 1024, 4096), 0, 4, 16),     # both plans split by 16: 128 units against 64
     ((100, 300, 8192), 0, 4, 32),      # ragged: three 128 x 128 tiles, 128 k-tiles at 4 per slice
+    ((100, 3000, 2048), 0, 4, 1),      # 24 unsplit 128 x 128 tiles beat 12 tiles split by 8
+    ((128, 4096, 2048), 0, 4, 1),      # 32 unsplit tiles: 15.3 against 19.4 us split by 8
+    ((96, 512, 16384), 0, 4, 38),      # 11.4 against 12.8 us
+    ((64, 1536, 4096), 0, 4, 12),
+    ((128, 2048, 8192), 0, 4, 9),
+    ((64, 4096, 4096), 0, 1, 9),       # only the 128 x 256 plan splits (16 tiles x 9)
+    ((128, 8192, 8192), 0, 1, 4),      # likewise: 32 tiles x 4
     ((129, 256, 65536), 0, 2, 76),     # two tile rows: the rule does not apply (the pair kernel)
     ((128, 128, 65536), 0, 1, 152),    # N <= 128: one tile either way
     ((128, 256, 1024), 1, 3, 1),       # short K: the small-GEMM pair kernel
 ])
 def test_plan_one_tile_row_with_a_long_k(shape, split, want_variant, want_split):
     """The automatic variant for a single row of tiles (M <= 128, N > 128,
-    K >= 2048): the 128 x 128 single-CTA kernel whenever every work unit of
-    the split fits in one wave of the S = 152 SMs."""
+    K >= 2048): the 128 x 128 single-CTA kernel when all its units fit in one
+    wave and its estimated time (operand bytes per CTA at the per-SM feed,
+    unique bytes at HBM rate, the split-K round trip) beats the 128 x 256
+    plan's, with more units winning a near tie.  The expected choices are the
+    faster plans measured on GB300 (S = 152)."""
     M, N, K = shape
     o = g.options(split_k=split)
     st, p = g.gemm_plan_for_device(M, N, K, 0, 1, 0, o, dev(), kern(want_variant))
