@@ -70,7 +70,7 @@ typedef enum {
  *   1SM_128x128: the same with 128-column tiles (N = 128 per MMA), for a
  *     single row of tiles (M <= 128) with a long K: twice the work units of
  *     1SM_128x256, so the split that fills the SMs takes half the slices and
- *     half the fp32 partial bytes per CTA.
+ *     half the fp32 partial bytes per CTA (see gemm_plan_for_device).
  *   2SM_256x256, 2SM_256x128: a cluster of two CTAs on a pair of SMs per
  *     tile, tcgen05.mma.cta_group::2 with M = 256; each CTA stages its own
  *     128 rows of A and half of the tile's columns of B, and holds its 128
@@ -257,10 +257,14 @@ gemm_status_t gemm_occupancy(const gemm_kernel_desc_t *kern, const gemm_device_d
  *     k-tiles long);
  *   - otherwise one cluster per tile.
  * With the plan's own variant, a small GEMM (256 x 128 pair tiles filling at
- * most half the resident pairs, K < 2048) runs on the 256 x 128 pair kernel,
- * and a single row of tiles (M <= 128, N > 128) with K >= 2048 runs on the
- * 128 x 128 single-CTA kernel when all its work units (tiles times the split
- * asked for, or the plan's own split for those tiles) fit in one wave.
+ * most half the resident pairs, K < 2048) runs on the 256 x 128 pair kernel.
+ * A single row of tiles (M <= 128, N > 128) with K >= 2048 runs on the
+ * 128 x 128 single-CTA kernel when its work units (tiles times the split
+ * asked for, or the plan's own split for those tiles) fit in one wave and an
+ * estimate of its time beats the 128 x 256 plan's: the operand bytes one CTA
+ * streams at about 100 GB/s per SM, at least the unique operand bytes at
+ * about 6.8 TB/s, plus, with split-K, about 6 us and the fp32 partial bytes
+ * at about 2 TB/s; within 0.5 us the plan with more work units wins.
  * Handing partial tiles between CTAs costs a roughly fixed few to 25 us on
  * GB300 (fp32 partials through L2 and a fix-up or a combine kernel), so the
  * plan spreads or splits the work only where the longer K repays it.
