@@ -225,19 +225,63 @@ struct Schedule {
 // the rational approximation of Abramowitz & Stegun, Handbook of Mathematical
 // Functions, formula 7.1.26 (after Hastings): for z >= 0,
 //     erfc(z) = t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-z^2) + e(z),
-//     t = 1 / (1 + p z),  |e(z)| <= 1.5e-7,
-// and erfc(-z) = 2 - erfc(z).  With the fp32 evaluation (fast reciprocal and
-// exp within a few ulp) the error of Phi stays below 3e-7, i.e. below 2^-20 |v| on
-// v * Phi(v) -- inside the stated tolerance -- at about twenty branch-free
-// instructions per value.
+//     t = 1 / (1 + p z),  |e(z)| <= 1.5e-7.
+// With z = |v| / sqrt 2 and E = erfc(z) / 2 (the a_k halved, which is exact):
+//     v >= 0:  v Phi(v) = v - v E = v (1 - E)      v < 0:  v Phi(v) = v E,
+// and as 0 < E <= 1/2, both cases are max(v E, v (1 - E)): no branch, no
+// select on the sign.  1 + p z is fma(|v|, p / sqrt 2, 1), and exp(-z^2) is
+// 2^(v^2 * (-log2(e) / 2)).  With the reciprocal and the power of two each
+// within a few ulps, Phi is within about 5e-7, so v Phi(v) is within 2^-20 |v| --
+// inside the stated tolerance.  gelu2 evaluates two values with the paired
+// instructions; gelu is the same operations on one value, so both give the
+// same bits.
+namespace gelu_as {
+constexpr float P_SQRT1_2 = static_cast<float>(0.3275911 / 1.4142135623730951);   // p / sqrt 2
+constexpr float HALF_A1 = 0.5f * 0.254829592f, HALF_A2 = 0.5f * -0.284496736f, HALF_A3 = 0.5f * 1.421413741f,
+                HALF_A4 = 0.5f * -1.453152027f, HALF_A5 = 0.5f * 1.061405429f;
+constexpr float NEG_HALF_LOG2E = static_cast<float>(-0.5 * 1.4426950408889634);
+}  // namespace gelu_as
+
 __device__ __forceinline__ float gelu(float v) {
-    const float z = fabsf(v) * 0.70710678118654752f;
-    const float t = __fdividef(1.0f, fmaf(0.3275911f, z, 1.0f));   // within 2 ulp
-    const float poly = t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, 1.061405429f, -1.453152027f), 1.421413741f), -0.284496736f),
-                                0.254829592f);
-    const float e = poly * __expf(-z * z);          // erfc(|v| / sqrt 2)
-    const float phi = v >= 0.0f ? fmaf(-0.5f, e, 1.0f) : 0.5f * e;
-    return v * phi;
+    using namespace gelu_as;
+    const float t = ptx::rcp_approx(fmaf(fabsf(v), P_SQRT1_2, 1.0f));
+    float q = fmaf(t, HALF_A5, HALF_A4);
+    q = fmaf(t, q, HALF_A3);
+    q = fmaf(t, q, HALF_A2);
+    q = fmaf(t, q, HALF_A1);
+    q = __fmul_rn(q, t);
+    const float e = __fmul_rn(q, ptx::ex2_approx(__fmul_rn(__fmul_rn(v, v), NEG_HALF_LOG2E)));   // E
+    const float one_minus_e = fmaf(e, -1.0f, 1.0f);
+    return fmaxf(__fmul_rn(v, e), __fmul_rn(v, one_minus_e));
+}
+
+// gelu of both halves of a pair
+__device__ __forceinline__ uint64_t gelu2(uint64_t v) {
+    using namespace gelu_as;
+    uint32_t v0, v1;
+    ptx::f2_unpack(v, v0, v1);
+    const uint64_t d = ptx::f2_fma(ptx::f2_pack(v0 & 0x7FFFFFFFu, v1 & 0x7FFFFFFFu), ptx::f2_splat(P_SQRT1_2),
+                                   ptx::f2_splat(1.0f));
+    uint32_t d0, d1;
+    ptx::f2_unpack(d, d0, d1);
+    const uint64_t t = ptx::f2_pack(__float_as_uint(ptx::rcp_approx(__uint_as_float(d0))),
+                                    __float_as_uint(ptx::rcp_approx(__uint_as_float(d1))));
+    uint64_t q = ptx::f2_fma(t, ptx::f2_splat(HALF_A5), ptx::f2_splat(HALF_A4));
+    q = ptx::f2_fma(t, q, ptx::f2_splat(HALF_A3));
+    q = ptx::f2_fma(t, q, ptx::f2_splat(HALF_A2));
+    q = ptx::f2_fma(t, q, ptx::f2_splat(HALF_A1));
+    q = ptx::f2_mul(q, t);
+    const uint64_t w = ptx::f2_mul(ptx::f2_mul(v, v), ptx::f2_splat(NEG_HALF_LOG2E));
+    uint32_t w0, w1;
+    ptx::f2_unpack(w, w0, w1);
+    const uint64_t e = ptx::f2_mul(q, ptx::f2_pack(__float_as_uint(ptx::ex2_approx(__uint_as_float(w0))),
+                                                   __float_as_uint(ptx::ex2_approx(__uint_as_float(w1)))));
+    const uint64_t one_minus_e = ptx::f2_fma(e, ptx::f2_splat(-1.0f), ptx::f2_splat(1.0f));
+    uint32_t h0, h1, y0, y1;
+    ptx::f2_unpack(ptx::f2_mul(v, e), h0, h1);
+    ptx::f2_unpack(ptx::f2_mul(v, one_minus_e), y0, y1);
+    return ptx::f2_pack(__float_as_uint(fmaxf(__uint_as_float(h0), __uint_as_float(y0))),
+                        __float_as_uint(fmaxf(__uint_as_float(h1), __uint_as_float(y1))));
 }
 
 // alpha * acc + beta * c + b, then ReLU when asked (GELU is applied apart).
@@ -713,18 +757,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             };
             // stage the chunk and hand it to TMA, which clips rows >= M and
             // columns >= N
-            auto stage_store = [&](uint32_t (&r)[32], int col0, bool with_gelu) {
+            auto stage_store = [&](uint32_t (&r)[32], int col0) {
                 if (warp_row0 >= p.M) return;
                 if (stores_issued >= 2 && lane == 0) ptx::bulk_wait_group_read<1>();   // this buffer read out
                 __syncwarp();
                 const uint32_t buf = epi_buf0 + (stores_issued & 1u) * EPI_BUF_BYTES;
-                if (with_gelu) {
-                    // on registers: 32 independent evaluations, and no round trip
-                    // through shared memory, whose bandwidth the main loop's
-                    // copies and MMAs are already using
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) r[q] = __float_as_uint(gelu(__uint_as_float(r[q])));
-                }
                 if (p.out_bf16) {
                     const uint32_t row_base = buf + static_cast<uint32_t>(lane) * 64u;
                     const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
@@ -753,12 +790,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 ++stores_issued;
             };
+            // The fused path's results go from registers straight to C: each lane
+            // writes its own row's 32 values with 16-byte stores (a row of C
+            // starts on a 16-byte boundary, ldc being a whole number of 16-byte
+            // pieces), which keeps them off shared memory, busy with the main
+            // loop's operands.  Columns past N are not written.
+            auto direct_store = [&](uint32_t (&r)[32], int col0) {
+                const int row = warp_row0 + lane;
+                if (row >= p.M) return;
+                const long long at = static_cast<long long>(row) * p.ld_out + col0;
+                if (p.out_bf16) {
+                    uint16_t *dst = static_cast<uint16_t *>(p.out) + at;
+                    if (col0 + 32 <= p.N) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            *reinterpret_cast<uint4 *>(dst + 8 * v) =
+                                make_uint4(pack_bf16x2(r[8 * v + 0], r[8 * v + 1]), pack_bf16x2(r[8 * v + 2], r[8 * v + 3]),
+                                           pack_bf16x2(r[8 * v + 4], r[8 * v + 5]), pack_bf16x2(r[8 * v + 6], r[8 * v + 7]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (col0 + j < p.N) dst[j] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[j])));
+                    }
+                } else {
+                    uint32_t *dst = static_cast<uint32_t *>(p.out) + at;
+                    if (col0 + 32 <= p.N) {
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            *reinterpret_cast<uint4 *>(dst + 4 * v) = make_uint4(r[4 * v + 0], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (col0 + j < p.N) dst[j] = r[j];
+                    }
+                }
+            };
             bool c_ok = true;   // false: a wait for previous C gave up (the CTA aborts)
             if (p.epi && !to_slot) {
                 // Fused epilogue, one chunk at a time in a rolled loop so that the
                 // code stays small (the epilogue warps share the instruction
-                // cache with the producer and MMA threads): the linear part, ReLU
-                // and GELU run on the chunk's 32 registers.
+                // cache with the producer and MMA threads).  The linear part and
+                // the activation run on the chunk's 32 registers, two values per
+                // paired instruction, with no round trip through shared memory,
+                // whose bandwidth the main loop's copies and MMAs are using.
                 // With beta != 0 the previous C comes in by TMA, one 32 x 32 chunk
                 // ahead, into the staging buffer the chunk's result will leave
                 // from, in the same swizzled layout (rows past M and columns past
@@ -780,12 +854,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     load_c_chunk(col_base, s0 & 1u);
                 }
                 if (owner_fast) prefetch(0);
-                float b_next = p.bias && col_base + lane < p.N ? __ldg(p.bias + col_base + lane) : 0.0f;
+                const uint64_t alpha2 = ptx::f2_splat(p.alpha), beta2 = ptx::f2_splat(p.beta);
+                // A chunk's 32 bias values are the same for every lane: eight
+                // 16-byte loads of one address per warp (bias is 16-byte aligned).
+                // The next chunk's go out as soon as this chunk's linear part has
+                // used them, and land during its activation and store.  Columns
+                // past N read as 0.
+                float4 bq[8];
+                auto load_bias = [&](int col0) {
+                    if (p.bias == nullptr) {
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) bq[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    } else if (col0 + 32 <= p.N) {
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) bq[v] = __ldg(reinterpret_cast<const float4 *>(p.bias + col0) + v);
+                    } else {
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            const int j = col0 + 4 * v;
+                            bq[v] = make_float4(j < p.N ? __ldg(p.bias + j) : 0.f, j + 1 < p.N ? __ldg(p.bias + j + 1) : 0.f,
+                                                j + 2 < p.N ? __ldg(p.bias + j + 2) : 0.f,
+                                                j + 3 < p.N ? __ldg(p.bias + j + 3) : 0.f);
+                        }
+                    }
+                };
+                load_bias(col_base);
 #pragma unroll 1
                 for (int c = 0; c < n_chunks; ++c) {
                     const int col0 = col_base + c * 32;
                     const uint32_t slot = (s0 + static_cast<uint32_t>(c)) & 1u;
-                    float4 cv[8];
+                    // previous C of this lane's row, as 16 pairs of fp32 bit patterns
+                    uint64_t cp[16];
                     if (read_c) {
                         if (c + 1 < n_chunks) {
                             // the other buffer's last store (the previous chunk's) must
@@ -809,15 +908,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         c_pending &= ~(1u << slot);
                         const uint32_t cbuf = epi_buf0 + slot * EPI_BUF_BYTES;
                         if (p.out_bf16) {
+                            // a bf16 is the high half of the fp32 with the same value
                             const uint32_t row_base = cbuf + static_cast<uint32_t>(lane) * 64u;
                             const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
 #pragma unroll
                             for (int v = 0; v < 4; ++v) {
                                 const uint4 u = ptx::ld_shared_v4(row_base + ((static_cast<uint32_t>(v) ^ sw) << 4));
-                                cv[2 * v] = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
-                                                        __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
-                                cv[2 * v + 1] = make_float4(__uint_as_float(u.z << 16), __uint_as_float(u.z & 0xFFFF0000u),
-                                                            __uint_as_float(u.w << 16), __uint_as_float(u.w & 0xFFFF0000u));
+                                cp[4 * v + 0] = ptx::f2_pack(u.x << 16, u.x & 0xFFFF0000u);
+                                cp[4 * v + 1] = ptx::f2_pack(u.y << 16, u.y & 0xFFFF0000u);
+                                cp[4 * v + 2] = ptx::f2_pack(u.z << 16, u.z & 0xFFFF0000u);
+                                cp[4 * v + 3] = ptx::f2_pack(u.w << 16, u.w & 0xFFFF0000u);
                             }
                         } else {
                             const uint32_t row_base = cbuf + static_cast<uint32_t>(lane) * 128u;
@@ -825,19 +925,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                             for (int v = 0; v < 8; ++v) {
                                 const uint4 u = ptx::ld_shared_v4(row_base + ((static_cast<uint32_t>(v) ^ sw) << 4));
-                                cv[v] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
-                                                    __uint_as_float(u.w));
+                                cp[2 * v + 0] = ptx::f2_pack(u.x, u.y);
+                                cp[2 * v + 1] = ptx::f2_pack(u.z, u.w);
                             }
                         }
                     } else {
 #pragma unroll
-                        for (int g = 0; g < 8; ++g) cv[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (int j = 0; j < 16; ++j) cp[j] = 0;
                     }
-                    // the chunk's 32 bias values, one per lane (one coalesced load),
-                    // handed to every lane by shuffles below
-                    const float b_lane = b_next;
-                    if (c + 1 < n_chunks)
-                        b_next = p.bias && col0 + 32 + lane < p.N ? __ldg(p.bias + col0 + 32 + lane) : 0.0f;
                     uint32_t r[32];
                     __syncwarp();
                     ptx::tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r);
@@ -857,18 +952,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     } else if (w.kind == KIND_OWNER) {
                         add_partials(r, c);
                     }
+                    // alpha * acc + beta * c + bias, each product and sum rounded
+                    // on its own, as epilogue_linear does
 #pragma unroll
-                    for (int g = 0; g < 8; ++g) {
-                        const float b0 = __shfl_sync(0xffffffffu, b_lane, 4 * g + 0);
-                        const float b1 = __shfl_sync(0xffffffffu, b_lane, 4 * g + 1);
-                        const float b2 = __shfl_sync(0xffffffffu, b_lane, 4 * g + 2);
-                        const float b3 = __shfl_sync(0xffffffffu, b_lane, 4 * g + 3);
-                        r[4 * g + 0] = __float_as_uint(epilogue_linear(__uint_as_float(r[4 * g + 0]), cv[g].x, b0, p.alpha, p.beta, p.act));
-                        r[4 * g + 1] = __float_as_uint(epilogue_linear(__uint_as_float(r[4 * g + 1]), cv[g].y, b1, p.alpha, p.beta, p.act));
-                        r[4 * g + 2] = __float_as_uint(epilogue_linear(__uint_as_float(r[4 * g + 2]), cv[g].z, b2, p.alpha, p.beta, p.act));
-                        r[4 * g + 3] = __float_as_uint(epilogue_linear(__uint_as_float(r[4 * g + 3]), cv[g].w, b3, p.alpha, p.beta, p.act));
+                    for (int v = 0; v < 8; ++v) {
+                        uint64_t lo = ptx::f2_mul(alpha2, ptx::f2_pack(r[4 * v + 0], r[4 * v + 1]));
+                        uint64_t hi = ptx::f2_mul(alpha2, ptx::f2_pack(r[4 * v + 2], r[4 * v + 3]));
+                        lo = ptx::f2_add(lo, ptx::f2_mul(beta2, cp[2 * v + 0]));
+                        hi = ptx::f2_add(hi, ptx::f2_mul(beta2, cp[2 * v + 1]));
+                        lo = ptx::f2_add(lo, ptx::f2_pack(__float_as_uint(bq[v].x), __float_as_uint(bq[v].y)));
+                        hi = ptx::f2_add(hi, ptx::f2_pack(__float_as_uint(bq[v].z), __float_as_uint(bq[v].w)));
+                        ptx::f2_unpack(lo, r[4 * v + 0], r[4 * v + 1]);
+                        ptx::f2_unpack(hi, r[4 * v + 2], r[4 * v + 3]);
                     }
-                    stage_store(r, col0, p.act == GEMM_ACT_GELU);
+                    if (c + 1 < n_chunks) load_bias(col0 + 32);
+                    if (p.act == GEMM_ACT_GELU) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const uint64_t y = gelu2(ptx::f2_pack(r[2 * j], r[2 * j + 1]));
+                            ptx::f2_unpack(y, r[2 * j], r[2 * j + 1]);
+                        }
+                    }
+                    if (p.act == GEMM_ACT_RELU) {
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) r[q] = __float_as_uint(fmaxf(__uint_as_float(r[q]), 0.0f));
+                    }
+                    direct_store(r, col0);
                 }
             } else {
             if (owner_fast) prefetch(0);
@@ -916,12 +1025,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         add_partials(r, c);
                     }
                 }
-                stage_store(r, col0, false);
+                stage_store(r, col0);
                 if (c + 1 < n_chunks) ptx::tmem_wait_ld(rbuf[(c + 1) & 1]);
             }
             }
             if (!c_ok) break;
-            if (!to_slot && warp_row0 < p.M && col_base + n_chunks * 32 > p.n_tma) {
+            if (!to_slot && !p.epi && warp_row0 < p.M && col_base + n_chunks * 32 > p.n_tma) {
                 // C's columns from n_tma to N, when N is not a whole number of
                 // 16-byte pieces: a TMA store clipped at N would still write
                 // the last piece whole, past N.  They lie in the last chunk,

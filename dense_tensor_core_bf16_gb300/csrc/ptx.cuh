@@ -385,5 +385,57 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
            (static_cast<uint32_t>(m >> 4) << 24);
 }
 
+// ---- paired fp32 arithmetic ---------------------------------------------------
+//
+// Two fp32 values in one 64-bit register (low half first).  The paired
+// instructions of the sm_100 family round each half exactly as the scalar
+// instruction with the same rounding mode does, so a result computed in pairs
+// equals, bit for bit, the same operations done one value at a time.
+
+__device__ __forceinline__ uint64_t f2_pack(uint32_t lo, uint32_t hi) {
+    uint64_t v;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "r"(lo), "r"(hi));
+    return v;
+}
+
+__device__ __forceinline__ uint64_t f2_splat(float x) {
+    return f2_pack(__float_as_uint(x), __float_as_uint(x));
+}
+
+__device__ __forceinline__ void f2_unpack(uint64_t v, uint32_t &lo, uint32_t &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// 1 / x and 2^x to within a few ulps (flushing subnormal inputs and results to 0).
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 }  // namespace ptx
 }  // namespace gemm

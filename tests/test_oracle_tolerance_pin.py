@@ -51,23 +51,27 @@ def _ulps(x, n):
 
 
 def device_gelu(v, erfc_scale=1.0):
-    """x Phi(x) as an fp32 kernel evaluates it: A&S 7.1.26 for erfc(|x|/sqrt 2),
-    a reciprocal 2 ulp off and an exp (2 + 1.16 |arg|) ulp off (the fast
-    intrinsics' documented bounds), each in the direction that enlarges erfc."""
+    """x Phi(x) as an fp32 kernel evaluates it, from A&S 7.1.26 with the
+    coefficients halved: E = erfc(|x| / sqrt 2) / 2 = t (a1/2 + ... ) exp(-x^2/2),
+    t = 1 / fma(|x|, p / sqrt 2, 1) from a reciprocal 2 ulp off, exp(-x^2/2) as
+    2^(x^2 * (-log2(e) / 2)) with its two products rounded and the power 2 ulp
+    off (results below 2^-126 flushed to 0), both errors in the direction that
+    enlarges E; then x Phi(x) = max(x E, x (1 - E))."""
     v = np.asarray(v, f32)
-    z = (np.abs(v) * f32(0.70710678118654752)).astype(f32)
-    t = _ulps((f32(1.0) / _fma32(f32(AS_P), z, f32(1.0))).astype(f32), 2.0)
-    a1, a2, a3, a4, a5 = (f32(a) for a in AS_A)
-    q = _fma32(t, a5, a4)
-    q = _fma32(t, q, a3)
-    q = _fma32(t, q, a2)
-    q = _fma32(t, q, a1)
-    poly = (t * q).astype(f32)
-    arg = (-(z * z)).astype(f32)
-    ex = _ulps(np.exp(arg.astype(np.float64)).astype(f32), 2.0 + 1.16 * np.abs(arg.astype(np.float64)))
-    e = (poly * ex * f32(erfc_scale)).astype(f32)
-    phi = np.where(v >= 0, _fma32(f32(-0.5), e, f32(1.0)), (f32(0.5) * e).astype(f32))
-    return (v * phi).astype(f32)
+    d = _fma32(np.abs(v), f32(AS_P / math.sqrt(2.0)), f32(1.0))
+    t = _ulps((f32(1.0) / d).astype(f32), 2.0)
+    h1, h2, h3, h4, h5 = (f32(0.5) * f32(a) for a in AS_A)
+    q = _fma32(t, h5, h4)
+    q = _fma32(t, q, h3)
+    q = _fma32(t, q, h2)
+    q = _fma32(t, q, h1)
+    q = (q * t).astype(f32)
+    w = ((v * v).astype(f32) * f32(-0.5 * math.log2(math.e))).astype(f32)
+    ex = _ulps(np.exp2(w.astype(np.float64)).astype(f32), 2.0)
+    ex = np.where(ex < f32(2.0 ** -126), f32(0.0), ex).astype(f32)
+    e = (((q * ex).astype(f32)).astype(np.float64) * erfc_scale).astype(f32)
+    one_minus_e = _fma32(e, f32(-1.0), f32(1.0))
+    return np.maximum((v * e).astype(f32), (v * one_minus_e).astype(f32))
 
 
 def device_accumulate(A_bits, Bt_bits, oracle):
