@@ -435,10 +435,18 @@ def run_gpu(args, wname: str, w: dict, cpu_baseline: bool):
     b_view = (lambda t: t) if b_row else (lambda t: t.t())
     A_store = np.ascontiguousarray(A_h.T) if a_col else A_h
     B_store = np.ascontiguousarray(Bt_h.T) if b_row else Bt_h
+    # the plan the timed call makes: the same options, epilogue included (a
+    # long epilogue changes how a stream-K tail is dealt out)
+    plan_epi = None
+    if epi:
+        plan_epi = g.gemm_epilogue_t(alpha=epi["alpha"], beta=epi["beta"], bias=None,
+                                     activation=g.ACTIVATIONS[epi["activation"]])
     st, plan = g.gemm_plan(M, N, K, layout_a, layout_b,
                            g.GEMM_OUT_BF16 if w["out"] == "bf16" else g.GEMM_OUT_F32,
                            g.options(split_k=kw["split_k"], non_persistent=int(kw["non_persistent"]),
-                                     kernel_variant=kw["kernel_variant"], no_stream_k=int(kw["no_stream_k"])))
+                                     kernel_variant=kw["kernel_variant"], no_stream_k=int(kw["no_stream_k"]),
+                                     raster_group_m=kw["raster_group_m"] or 0,
+                                     epilogue=ctypes.pointer(plan_epi) if plan_epi is not None else None))
     if st:
         raise g.GemmError(st, "gemm_plan")
     if plan.workspace_bytes:

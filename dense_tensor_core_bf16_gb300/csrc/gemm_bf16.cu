@@ -91,6 +91,9 @@ struct KernelParams {
     float *partials;
     unsigned int *sk_flags;      // [num_clusters][CTA group][4 epilogue warps]
     unsigned int epoch;          // value the flags of this launch carry (never 0)
+    // first stream-K iteration of cluster c (c = 0 .. num_clusters; the last
+    // is sk_iters), as the plan deals them out
+    long long sk_bounds[SK_MAX_CLUSTERS + 1];
 };
 
 // Wait for the phase of `bar` with parity `parity`.  Gives up after
@@ -167,13 +170,8 @@ __device__ __forceinline__ void tile_coords(long long tile, const KernelParams &
     tn = r / gsize;
 }
 
-// First stream-K iteration of cluster c: the sk_iters iterations are dealt out
-// in contiguous ranges, the first (sk_iters mod clusters) ranges one longer.
-__device__ __forceinline__ long long sk_range_start(const KernelParams &p, long long c) {
-    const long long base = p.sk_iters / p.num_clusters;
-    const long long rem = p.sk_iters - base * p.num_clusters;
-    return c * base + min(c, rem);
-}
+// First stream-K iteration of cluster c (c = num_clusters: the end).
+__device__ __forceinline__ long long sk_range_start(const KernelParams &p, long long c) { return p.sk_bounds[c]; }
 
 // The work of one cluster, in the order every role of its CTAs walks it:
 // its stream-K range (cut at tile boundaries), then its whole tiles.
@@ -376,7 +374,7 @@ template <int CG, int BN, int TK>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                      const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_out,
-                     const KernelParams p) {
+                     const __grid_constant__ KernelParams p) {
     constexpr VariantInfo V = make_variant(CG, BN, TK);
     // Operand boxes.  K-major (A row-major, B column-major): TK/64 boxes of
     // rows x 64 K, each rows x 128 bytes.  MN-major (A column-major, B
@@ -1727,6 +1725,10 @@ gemm_status_t launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_
     p.sk_tiles = static_cast<int>(plan.stream_k_tiles);
     p.sk_iters = plan.stream_k_tiles * plan.k_tiles;
     if (plan.stream_k_tiles > 0) {
+        if (clusters > SK_MAX_CLUSTERS) return GEMM_ERR_NOT_SUPPORTED;   // the plan never asks for this
+        int64_t bounds[SK_MAX_CLUSTERS + 1];
+        stream_k_bounds(p.sk_iters, clusters, plan.k_tiles, o, bounds);
+        for (int64_t c = 0; c <= clusters; ++c) p.sk_bounds[c] = bounds[c];
         p.partials = ds.workspace;
         p.sk_flags = ds.sk_flags;
         p.epoch = next_epoch(ds);

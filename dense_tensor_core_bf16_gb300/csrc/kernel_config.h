@@ -112,5 +112,8 @@ constexpr int MIN_K_TILES_PER_SPLIT = 4;  // automatic split-K keeps at least th
 constexpr long long AUTO_SPLIT_MIN_K = 2048;
 constexpr long long LONG_K = 6144;
 constexpr double STREAM_K_MIN_WASTE = 12.0;
+// The stream-K tail's range boundaries travel in the kernel's parameters, one
+// per cluster; a launch with more clusters than this takes no tail.
+constexpr int SK_MAX_CLUSTERS = 160;
 
 }  // namespace gemm

@@ -14,6 +14,9 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_layout_t la, gemm_
 int resolve_variant(int requested);
 int choose_variant(int64_t M, int64_t N, int64_t K, int requested, int split_k, const gemm_device_desc_t &dev);
 int choose_split(int64_t tiles, int k_tiles, int capacity, int requested, int64_t K);
+// First stream-K iteration of each cluster, bounds[0 .. clusters] (the last is
+// sk_iters), for the tail a plan with these options runs.
+void stream_k_bounds(int64_t sk_iters, int64_t clusters, int64_t k_tiles, const gemm_options_t &o, int64_t *bounds);
 gemm_status_t conv_check(const gemm_conv2d_desc_t *d, int64_t *P, int64_t *Q);
 // Frees the host-batch staging slots of every device (host_pipeline.cpp).
 void release_host_staging();

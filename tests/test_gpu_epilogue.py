@@ -160,6 +160,26 @@ def test_epilogue_on_stream_k_tiles(oracle_lib, variant, shape):
     check(oracle_lib, A, Bt, C, "f32", C0, bias, 1.0, 1.0, "relu", exact=True)
 
 
+@pytest.mark.parametrize("variant,shape", [(2, (3328, 3072, 512)), (2, (1800, 1500, 2000)), (1, (1800, 1500, 2000)),
+                                           (0, (2200, 2600, 4100))])
+def test_gelu_on_snapped_stream_k_ranges(oracle_lib, variant, shape):
+    """With a GELU epilogue (or one that reads C) the stream-K boundaries that
+    fall within a quarter tile of a tile's edge move to the edge: ranges grow,
+    shrink or vanish, and owners and contributors change.  A partial sum lost or counted twice would
+    move entries by far more than the bound."""
+    import dense_tensor_core_bf16_gb300 as g
+    M, N, K = shape
+    opts = g.options(kernel_variant=variant, no_stream_k=-1)
+    st, plan = g.gemm_plan(M, N, K, opts=opts)
+    assert st == 0 and plan.stream_k_tiles > 0
+    A, Bt = operands(M, N, K, "normal", True, SEED + 22)
+    C0, bias = c_old_and_bias(M, N, SEED + 23)
+    for out in ("bf16", "f32"):
+        C = run(A, Bt, out, C0, bias, kernel_variant=variant, force_stream_k=True, alpha=1.0, beta=1.0,
+                activation="gelu")
+        check(oracle_lib, A, Bt, C, out, C0, bias, 1.0, 1.0, "gelu")
+
+
 @pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("non_persistent", [False, True])
 def test_previous_c_over_many_tiles_per_cta(oracle_lib, variant, non_persistent):
