@@ -832,13 +832,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // paired instruction, with no round trip through shared memory,
                 // whose bandwidth the main loop's copies and MMAs are using.
                 // With beta != 0 the previous C comes in by TMA, one 32 x 32 chunk
-                // ahead, into the staging buffer the chunk's result will leave
-                // from, in the same swizzled layout (rows past M and columns past
-                // N arrive as zeros); each lane then reads its own row of it.
+                // ahead, into the warp's two staging buffers (no store leaves
+                // from them in a fused launch), in the swizzled layout of a store
+                // (rows past M and columns past N arrive as zeros); each lane then
+                // reads its own row of it.  Chunk c lands in buffer c & 1.
                 const bool read_c = p.beta != 0.0f && warp_row0 < p.M;   // warp-uniform
                 const uint32_t c_bar = bar(BAR_CLOAD + 2 * quarter);
                 const uint32_t c_bytes = 32u * 32u * (p.out_bf16 ? 2u : 4u);
-                const uint32_t s0 = stores_issued;   // chunk c leaves from buffer (s0 + c) & 1
                 auto load_c_chunk = [&](int col0, uint32_t slot) {
                     c_pending |= 1u << slot;
                     if (lane == 0) {
@@ -847,9 +847,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 };
                 if (read_c) {
-                    if (s0 >= 2 && lane == 0) ptx::bulk_wait_group_read<1>();   // buffer s0 & 1 read out
-                    __syncwarp();
-                    load_c_chunk(col_base, s0 & 1u);
+                    __syncwarp();   // the previous unit's reads of buffer 0 are done
+                    load_c_chunk(col_base, 0u);
                 }
                 if (owner_fast) prefetch(0);
                 const uint64_t alpha2 = ptx::f2_splat(p.alpha), beta2 = ptx::f2_splat(p.beta);
@@ -880,14 +879,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll 1
                 for (int c = 0; c < n_chunks; ++c) {
                     const int col0 = col_base + c * 32;
-                    const uint32_t slot = (s0 + static_cast<uint32_t>(c)) & 1u;
+                    const uint32_t slot = static_cast<uint32_t>(c) & 1u;
                     // previous C of this lane's row, as 16 pairs of fp32 bit patterns
                     uint64_t cp[16];
                     if (read_c) {
                         if (c + 1 < n_chunks) {
-                            // the other buffer's last store (the previous chunk's) must
-                            // have been read out before the next chunk's C lands there
-                            if (lane == 0) ptx::bulk_wait_group_read<0>();
+                            // every lane has used the previous chunk's C: the next
+                            // chunk's lands in its buffer
                             __syncwarp();
                             load_c_chunk(col0 + 32, slot ^ 1u);
                         }
