@@ -203,6 +203,41 @@ def test_epilogue_with_row_major_b(oracle_lib):
     check(oracle_lib, A, Bt, C, "bf16", C0, bias, 1.0, 1.0, "gelu")
 
 
+def test_device_gelu_on_a_sweep(oracle_lib):
+    """GELU alone: with A = 0 the product is exactly 0, so C := gelu(C) with
+    fp32 C evaluates the device's GELU on the values C holds.  The main
+    kernel (two values per paired instruction), the split-K combine kernel
+    and the K = 0 kernel (one value at a time) run the same operations, so
+    they agree bit for bit; each lies within 2^-20 |x| of x Phi(x)."""
+    import dense_tensor_core_bf16_gb300 as g
+    from oracle import epilogue as ep
+    M, N, K = 256, 1024, 256
+    x = np.linspace(-14.0, 14.0, M * N - 64).astype(np.float32)
+    special = np.array([0.0, -0.0, 1e-30, -1e-30, 1e-7, -1e-7, 2 ** -126, -(2 ** -126), 1e30, -1e30,
+                        np.sqrt(2.0), -np.sqrt(2.0), 13.2, -13.2, 40.0, -40.0], dtype=np.float32)
+    x = np.concatenate([x, np.tile(special, 4)]).reshape(M, N)
+    A = torch.zeros(M, K, dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros(N, K, dtype=torch.bfloat16, device="cuda").t()
+    got = {}
+    for mode, kw in (("main", dict(split_k=1)), ("combine", dict(split_k=2)), ("k_zero", {})):
+        C = torch.from_numpy(x.copy()).cuda()
+        if mode == "k_zero":
+            Az = torch.zeros(M, 8, dtype=torch.bfloat16, device="cuda")[:, :0]
+            Bz = torch.zeros(N, 8, dtype=torch.bfloat16, device="cuda")[:, :0].t()
+            g.matmul(Az, Bz, out=C, beta=1.0, activation="gelu")
+        else:
+            g.matmul(A, B, out=C, beta=1.0, activation="gelu", **kw)
+        torch.cuda.synchronize()
+        got[mode] = C.cpu().numpy()
+    assert np.array_equal(got["main"].view(np.uint32), got["combine"].view(np.uint32))
+    assert np.array_equal(got["main"].view(np.uint32), got["k_zero"].view(np.uint32))
+    xd = x.astype(np.float64)
+    ref = ep.epilogue(np.zeros_like(xd), xd, None, alpha=1.0, beta=1.0, activation="gelu")
+    err = np.abs(got["main"].astype(np.float64) - ref)
+    assert np.all(np.isfinite(got["main"]))
+    assert np.all(err <= 2.0 ** -20 * np.abs(xd) + 1e-37), f"worst {np.max(err / np.maximum(np.abs(xd), 1e-30)):.3g} |x|"
+
+
 @pytest.mark.parametrize("out", ["f32", "bf16"])
 def test_k_zero_epilogue(oracle_lib, out):
     """K == 0: the product is the empty sum, so C := act(beta * C + bias)."""
