@@ -3,7 +3,7 @@
 The fused epilogue C := act(alpha * A.B + beta * C + bias[n]) is the
 Tensor Core's D = A x B + C with the ordinary lanes' work after it (lesson
 "The Tensor Core", its opening and the paragraph on what the Tensor Cores
-speed up).  Every fused-epilogue parity verdict rests on the bound
+speed up).  Every fused-epilogue parity check rests on the bound
 ``tolerance`` returns, so it is checked from both sides here:
 
 * from below -- a correct fp32 device, emulated in numpy float32 (bf16
