@@ -80,11 +80,12 @@ struct KernelParams {
     int act;                     // gemm_activation_t
     // Stream-K tail (sk_tiles > 0; split_k is then 1): tiles [0, dp_tiles) are
     // computed whole, round robin over the clusters; the k-iterations of tiles
-    // [dp_tiles, tiles) are spread evenly over the clusters, which run them first.
+    // [dp_tiles, tiles) are dealt out to the clusters in the contiguous ranges
+    // of sk_bounds, which the clusters run first.
     int num_clusters;            // clusters launched (gridDim.x / CTA group)
     int dp_tiles;
     int sk_tiles;
-    long long sk_iters;          // sk_tiles * k_tiles
+    long long sk_iters;          // sk_tiles * k_tiles (the last of sk_bounds)
     // fp32 partial tiles, one slot of tile rows x BN each: with split-K,
     // [split][tile] (slot split * tiles + tile); with a stream-K tail, one
     // slot per cluster.  Slots are laid out warp-major (see the epilogue).
