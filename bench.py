@@ -192,8 +192,10 @@ def roofline_entry(flops: float, alg_bytes: float, mean_ms: float, peaks: dict, 
 
 def _code_only(text: str) -> str:
     """C/C++ source without its comments (none of the library's string
-    literals holds a comment marker)."""
-    return re.sub(r"//[^\n]*", "", re.sub(r"/\*.*?\*/", "", text, flags=re.S))
+    literals holds a comment marker), its whitespace collapsed: a change to
+    the prose or the layout alone leaves the hash as it was."""
+    code = re.sub(r"//[^\n]*", "", re.sub(r"/\*.*?\*/", "", text, flags=re.S))
+    return " ".join(code.split())
 
 
 # The files that decide what the GEMM kernels do and how a problem is cut into

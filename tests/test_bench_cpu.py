@@ -63,6 +63,9 @@ def test_source_hash_ignores_comments_only():
     c = "int f(int x) {\n    return x + 2;   // one more\n}\n/* note */\n"
     assert bench._code_only(a) == bench._code_only(b)
     assert bench._code_only(a) != bench._code_only(c)
+    # a comment grown by a line, or code re-wrapped, leaves the code as it was
+    d = "int f(int x) {\n    // one\n    // more\n    return x +\n        1;\n}\n"
+    assert bench._code_only(a) == bench._code_only(d)
 
 
 def test_profiler_style_shape_flags():
