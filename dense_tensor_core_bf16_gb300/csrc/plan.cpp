@@ -278,31 +278,42 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, gemm_layout_t la, gemm_
 }
 
 // The sk_iters iterations are dealt out in contiguous ranges, the first
-// (sk_iters mod clusters) ranges one longer.  With a long epilogue -- GELU, or
-// any that reads the previous C -- a boundary that falls within k_tiles / 4 of
-// a tile's edge moves to the edge.  Otherwise the cluster before it would own
-// that tile for a few k-tiles of MMAs and still run its whole epilogue, or the
-// cluster after it would start with a sliver; such an epilogue is long enough
-// next to a tile's main loop to hold up the next tile's MMAs.  At 4096^3:
-// GELU(A.B + C + bias) 91.2 -> 87.5 us, A.B + C + bias 85.6 -> 84.4; with bias
-// and ReLU alone 80.9 -> 81.2 and for the plain GEMM 77.7 -> 79.3, so those
-// keep the even ranges.  The boundaries stay in order: a moved boundary never
-// passes a neighbour, as the move is less than half a tile.
+// (sk_iters mod clusters) ranges one longer.  A long epilogue -- GELU, or any
+// that reads the previous C -- changes this:
+//   - with k_tiles even (and at least 8) the ranges are made of whole half
+//     tiles.  Every range then starts at k = 0 or k_tiles / 2 of a tile, so
+//     clusters reading the same operand panels start on the same slices and
+//     share them in L2, and no cluster runs a whole epilogue for a piece
+//     shorter than half a tile.  The longest range may grow (4096^3: 48
+//     iterations against 44; M = 4097: 64 against 51), and still: 4096^3
+//     GELU(A.B + C + bias) 89.2 -> 87.2 us and A.B + C + bias 85.6 -> 83.6
+//     against the tile-edge moves below; M = 4097 GELU 95.8 -> 94.6; the 3 x 3
+//     convolutions with bias and GELU 76.7 -> 76.3 (28 x 28) and 80.0 -> 79.8
+//     (56 x 56).  For the plain GEMM half tiles do not pay (4096^3 -0.7 %,
+//     K = 4088 +0.6 %, M = 4097 +2.8 %, 28 x 28 convolution +5.5 %);
+//   - otherwise a boundary within k_tiles / 4 of a tile's edge moves to the
+//     edge, so that no cluster owns a tile for a few k-tiles of MMAs and still
+//     runs its whole epilogue, nor starts with a sliver (4096^3 with even
+//     ranges before: GELU(A.B + C + bias) 91.2 -> 87.5 us, A.B + C + bias
+//     85.6 -> 84.4; for bias and ReLU alone 80.9 -> 81.2 and for the plain
+//     GEMM 77.7 -> 79.3, so those keep even ranges).  A moved boundary never
+//     passes a neighbour, as the move is less than half a tile.
 void stream_k_bounds(int64_t sk_iters, int64_t clusters, int64_t k_tiles, const gemm_options_t &o, int64_t *bounds) {
-    const int64_t base = sk_iters / clusters, rem = sk_iters % clusters;
-    const bool snap = o.epilogue != nullptr && (o.epilogue->activation == GEMM_ACT_GELU || o.epilogue->beta != 0.0f);
+    const bool long_epilogue =
+        o.epilogue != nullptr && (o.epilogue->activation == GEMM_ACT_GELU || o.epilogue->beta != 0.0f);
+    // contiguous ranges of whole units (sk_iters is a multiple of the unit), as even as they go
+    const int64_t unit = long_epilogue && k_tiles >= 8 && k_tiles % 2 == 0 ? k_tiles / 2 : 1;
+    const int64_t n = sk_iters / unit, base = n / clusters, rem = n % clusters;
+    for (int64_t c = 0; c <= clusters; ++c) bounds[c] = unit * (c * base + (c < rem ? c : rem));
     const int64_t reach = k_tiles / 4;
-    for (int64_t c = 0; c <= clusters; ++c) {
-        int64_t x = c * base + (c < rem ? c : rem);
-        if (snap && reach > 0) {
-            const int64_t lo = x / k_tiles * k_tiles;
-            if (x - lo <= reach) {
-                x = lo;
-            } else if (lo + k_tiles - x <= reach && lo + k_tiles <= sk_iters) {
-                x = lo + k_tiles;
-            }
+    if (!long_epilogue || unit > 1 || reach == 0) return;
+    for (int64_t c = 1; c < clusters; ++c) {
+        const int64_t x = bounds[c], lo = x / k_tiles * k_tiles;
+        if (x - lo <= reach) {
+            bounds[c] = lo;
+        } else if (lo + k_tiles - x <= reach && lo + k_tiles <= sk_iters) {
+            bounds[c] = lo + k_tiles;
         }
-        bounds[c] = x;
     }
 }
 

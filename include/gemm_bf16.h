@@ -252,9 +252,10 @@ gemm_status_t gemm_occupancy(const gemm_kernel_desc_t *kern, const gemm_device_d
  *     128 x 256 block per SM idle): a stream-K tail -- the last C + (T mod C)
  *     tiles (all T when T < 2C) have their k-iterations dealt out evenly over
  *     the C clusters in contiguous ranges, the rest are computed whole; with a
- *     GELU epilogue or one that reads C, a range boundary within k_tiles / 4
- *     of a tile's edge moves to the edge (a long epilogue should not follow a
- *     few k-tiles of MMAs);
+ *     GELU epilogue or one that reads C the ranges are made of whole half
+ *     tiles when k_tiles is even and at least 8, else a range boundary within
+ *     k_tiles / 4 of a tile's edge moves to the edge (a long epilogue should
+ *     not follow a few k-tiles of MMAs);
  *   - split_k = 0, and T * 8 <= C with K >= 2048 or T * 4 <= C with
  *     K >= 6144: split-K chosen by the plan (C / T slices, each at least 4
  *     k-tiles long);

@@ -358,35 +358,41 @@ def test_plan_stream_k_hand_values():
     assert p.eta_stream_k == pytest.approx((512 * 64 / 152) / (2 * 64 + math.ceil(208 * 64 / 152)), rel=1e-12)
 
 
-def test_plan_stream_k_gelu_moves_boundaries_to_tile_edges():
-    """4096^3 with a GELU epilogue or one that reads C: the 3328 tail
-    iterations are dealt 44 to clusters 0-59 and 43 to the rest, and a
-    boundary within 32 / 4 = 8 of a tile's edge moves to it -- 88 up to 96,
-    132 down to 128, 220 up to 224, 264 down to 256 -- so cluster 1 runs
-    [44, 96), 52 iterations: a 20-long piece of tile 1 and the whole of
-    tile 2.  The largest share is then 2 x 32 + 52 = 116.  ReLU or no
-    activation without C keep the even ranges (108)."""
-    ideal = 256 * 32 / 76
-    for act, beta, worst in ((g.ACTIVATIONS["gelu"], 0.0, 116), (g.ACTIVATIONS["gelu"], 1.0, 116),
-                             (g.ACTIVATIONS["none"], 1.0, 116), (g.ACTIVATIONS["relu"], 0.0, 108),
-                             (g.ACTIVATIONS["none"], 0.0, 108)):
-        epi = g.gemm_epilogue_t(alpha=1.0, beta=beta, bias=None, activation=act)
+def test_plan_stream_k_ranges_for_long_epilogues():
+    """With a GELU epilogue or one that reads C, the stream-K tail is dealt in
+    whole half tiles when k_tiles is even and at least 8.  4096^3: 104 tail
+    tiles are 208 halves of 16 iterations on 76 clusters, three to the first
+    56 and two to the rest (48 or 32 iterations), so the largest share is
+    2 x 32 + 48 = 112 k-iterations.  4097 x 4096 x 4096: 272 tiles, a tail of
+    76 + 44 = 120 tiles, 240 halves, four to the first 12 clusters: 2 x 32 +
+    64 = 128.  ReLU or no activation without C keep the even ranges (108 and
+    2 x 32 + 51 = 115)."""
+    cases = [((4096, 4096, 4096), ("gelu", 0.0), 112), ((4096, 4096, 4096), ("gelu", 1.0), 112),
+             ((4096, 4096, 4096), ("none", 1.0), 112), ((4096, 4096, 4096), ("relu", 0.0), 108),
+             ((4096, 4096, 4096), ("none", 0.0), 108), ((4097, 4096, 4096), ("gelu", 1.0), 128),
+             ((4097, 4096, 4096), ("relu", 0.0), 115)]
+    for (M, N, K), (act, beta), worst in cases:
+        epi = g.gemm_epilogue_t(alpha=1.0, beta=beta, bias=None, activation=g.ACTIVATIONS[act])
         o = g.options(split_k=0, kernel_variant=2, epilogue=ctypes.pointer(epi))
-        st, p = g.gemm_plan_for_device(4096, 4096, 4096, g.GEMM_ROW_MAJOR, g.GEMM_COL_MAJOR, g.GEMM_OUT_BF16, o,
+        st, p = g.gemm_plan_for_device(M, N, K, g.GEMM_ROW_MAJOR, g.GEMM_COL_MAJOR, g.GEMM_OUT_BF16, o,
                                        dev(), kern(2, 64, 0))
-        assert st == 0 and (p.stream_k_tiles, p.k_tiles) == (104, 32)
-        assert p.eta_stream_k == pytest.approx(ideal / worst, rel=1e-12), (act, beta)
-    # a short K: 4 k-tiles per tile, a reach of one iteration; the largest share
-    # is still a whole number of iterations and never below the even split's
-    for act in (g.ACTIVATIONS["gelu"], g.ACTIVATIONS["none"]):
-        epi = g.gemm_epilogue_t(alpha=1.0, beta=0.0, bias=None, activation=act)
+        assert st == 0 and p.k_tiles == 32 and p.stream_k_tiles == (104 if M == 4096 else 120)
+        assert p.eta_stream_k == pytest.approx(p.tiles * 32 / 76 / worst, rel=1e-12), (M, act, beta)
+
+
+def test_plan_stream_k_short_k_moves_boundaries_to_tile_edges():
+    """k_tiles below 8 (here 4, a reach of one iteration): a long epilogue's
+    boundaries within k_tiles / 4 of a tile's edge move to the edge.  The
+    3328 x 3072 x 512 tail of 80 tiles (320 iterations, 4.2 per cluster) after
+    one whole tile of 4 iterations per cluster: the longest range grows from 5
+    to 6, the largest share from 9 to 10; other epilogues keep 9."""
+    for act, beta, worst in (("gelu", 0.0, 10), ("none", 1.0, 10), ("none", 0.0, 9), ("relu", 0.0, 9)):
+        epi = g.gemm_epilogue_t(alpha=1.0, beta=beta, bias=None, activation=g.ACTIVATIONS[act])
         o = g.options(split_k=0, kernel_variant=2, no_stream_k=-1, epilogue=ctypes.pointer(epi))
         st, p = g.gemm_plan_for_device(3328, 3072, 512, g.GEMM_ROW_MAJOR, g.GEMM_COL_MAJOR, g.GEMM_OUT_BF16, o,
                                        dev(), kern(2, 64, 0))
-        assert st == 0 and p.stream_k_tiles > 0 and p.k_tiles == 4
-        even = math.ceil(p.dp_tiles / 76) * 4 + math.ceil(p.stream_k_tiles * 4 / 76)
-        worst = p.tiles * 4 / 76 / p.eta_stream_k
-        assert abs(worst - round(worst)) < 1e-9 and round(worst) >= even
+        assert st == 0 and (p.tiles, p.stream_k_tiles, p.k_tiles) == (156, 80, 4)
+        assert p.eta_stream_k == pytest.approx(156 * 4 / 76 / worst, rel=1e-12), (act, beta)
 
 
 def _call(M, N, K, A=16, lda=64, B=16, ldb=64, C=16, ldc=64, la=0, lb=1, out=0, split=1):

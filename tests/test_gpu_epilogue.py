@@ -163,10 +163,11 @@ def test_epilogue_on_stream_k_tiles(oracle_lib, variant, shape):
 @pytest.mark.parametrize("variant,shape", [(2, (3328, 3072, 512)), (2, (1800, 1500, 2000)), (1, (1800, 1500, 2000)),
                                            (0, (2200, 2600, 4100))])
 def test_gelu_on_snapped_stream_k_ranges(oracle_lib, variant, shape):
-    """With a GELU epilogue (or one that reads C) the stream-K boundaries that
-    fall within a quarter tile of a tile's edge move to the edge: ranges grow,
-    shrink or vanish, and owners and contributors change.  A partial sum lost or counted twice would
-    move entries by far more than the bound."""
+    """With a GELU epilogue (or one that reads C) the stream-K tail is dealt in
+    half tiles (k_tiles 16 and 32 here), or, for odd or short k_tiles (33, 4),
+    with boundaries near a tile's edge moved to it: ranges grow, shrink or
+    vanish, and owners and contributors change.  A partial sum lost or counted
+    twice would move entries by far more than the bound."""
     import dense_tensor_core_bf16_gb300 as g
     M, N, K = shape
     opts = g.options(kernel_variant=variant, no_stream_k=-1)
