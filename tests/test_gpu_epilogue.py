@@ -181,6 +181,28 @@ def test_gelu_on_snapped_stream_k_ranges(oracle_lib, variant, shape):
         check(oracle_lib, A, Bt, C, out, C0, bias, 1.0, 1.0, "gelu")
 
 
+# k_tiles 2, 5, 8, 9, 16 and 24 on the pair kernel: even ranges (no reach),
+# boundaries moved to tile edges (5, 9: a reach of 1 and 2), half tiles (8,
+# 16, 24: halves of 4, 8 and 12 k-tiles)
+TAIL_SHAPES = [(1300, 1100, 256), (1100, 1300, 520), (900, 1500, 1000), (1500, 900, 1100), (800, 1200, 2048),
+               (1200, 800, 3000)]
+
+
+@pytest.mark.parametrize("shape", TAIL_SHAPES)
+def test_long_epilogues_on_forced_stream_k_tails(oracle_lib, shape):
+    """Every way a long epilogue's stream-K tail is dealt, whole C against the
+    oracle: GELU with C, and ReLU with C / 2, on a tail forced over all tiles."""
+    import dense_tensor_core_bf16_gb300 as g
+    M, N, K = shape
+    st, plan = g.gemm_plan(M, N, K, opts=g.options(kernel_variant=2, no_stream_k=-1))
+    assert st == 0 and plan.stream_k_tiles > 0 and plan.k_tiles == -(-K // 128)
+    A, Bt = operands(M, N, K, "normal", True, SEED + 24)
+    C0, bias = c_old_and_bias(M, N, SEED + 25)
+    for out, act, beta in (("bf16", "gelu", 1.0), ("f32", "relu", 0.5)):
+        C = run(A, Bt, out, C0, bias, kernel_variant=2, force_stream_k=True, alpha=1.0, beta=beta, activation=act)
+        check(oracle_lib, A, Bt, C, out, C0, bias, 1.0, beta, act)
+
+
 @pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("non_persistent", [False, True])
 def test_previous_c_over_many_tiles_per_cta(oracle_lib, variant, non_persistent):
