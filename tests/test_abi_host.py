@@ -380,6 +380,19 @@ def test_plan_stream_k_ranges_for_long_epilogues():
         assert p.eta_stream_k == pytest.approx(p.tiles * 32 / 76 / worst, rel=1e-12), (M, act, beta)
 
 
+def test_plan_takes_no_stream_k_tail_beyond_160_clusters():
+    """The tail's range boundaries travel in the kernel's parameters, one per
+    cluster, for at most 160 clusters: a device with more resident clusters
+    (a made-up 400-SM part, one CTA per cluster) gets whole tiles or split-K,
+    never a tail, even when a tail is forced."""
+    big = dev(num_sms=400)
+    for no_sk in (0, -1):
+        p = _plan(8192, 8192, 4096, split=0, d=big, variant=1, no_sk=no_sk)
+        assert p.stream_k_tiles == 0 and p.eta_stream_k == 0
+    p = _plan(8192, 8192, 4096, split=0, variant=1, no_sk=-1)   # 152 clusters: the tail is there
+    assert p.stream_k_tiles > 0
+
+
 def test_plan_stream_k_short_k_moves_boundaries_to_tile_edges():
     """k_tiles below 8 (here 4, a reach of one iteration): a long epilogue's
     boundaries within k_tiles / 4 of a tile's edge move to the edge.  The
